@@ -1,0 +1,103 @@
+"""hwkv: per-head budgeted KV residency on one GB300.
+
+The grouped-cache runtime of "HeadWiseKV: Budgeted Per-Head Cache Residency for Hybrid
+Long-Context Language Models" (blog summary; abstract and section "Grouped-Cache
+Runtime"): every KV head of a global-attention layer keeps a static window of its most
+recent tokens in ceil(w / block_size) paged blocks, and decode attention reads only that
+resident window.
+
+``binding`` exposes the C ABI of ``include/hwkv.h`` under the same names; ``Pool`` below
+is a convenience wrapper that owns the device buffers (allocated with torch).
+"""
+from __future__ import annotations
+
+from typing import Optional
+
+import torch
+
+from . import binding
+from .binding import (HWKV_BF16, HWKV_F32, HWKV_KERNEL_AUTO, HWKV_KERNEL_SIMT, HWKV_KERNEL_TENSOR, HwkvError,
+                      hwkv_abi_version, hwkv_append, hwkv_block_table, hwkv_check_device_errors,
+                      hwkv_decode_attn, hwkv_decode_workspace_bytes, hwkv_materialize, hwkv_pool_bytes,
+                      hwkv_pool_create, hwkv_pool_destroy, hwkv_pool_geometry, hwkv_set_block_table,
+                      hwkv_set_decode_config)
+
+__all__ = [
+    "Pool", "HwkvError", "binding", "HWKV_F32", "HWKV_BF16", "HWKV_KERNEL_AUTO", "HWKV_KERNEL_TENSOR",
+    "HWKV_KERNEL_SIMT", "hwkv_abi_version", "hwkv_append", "hwkv_block_table", "hwkv_check_device_errors",
+    "hwkv_decode_attn", "hwkv_decode_workspace_bytes", "hwkv_materialize", "hwkv_pool_bytes", "hwkv_pool_create",
+    "hwkv_pool_destroy", "hwkv_pool_geometry", "hwkv_set_block_table", "hwkv_set_decode_config",
+]
+
+
+class Pool:
+    """A per-head paged KV pool on the current CUDA device.
+
+    The pool buffer is one torch uint8 allocation of exactly ``hwkv_pool_bytes`` bytes
+    (the pre-serving prediction), bound with ``hwkv_pool_create``.
+    """
+
+    def __init__(self, layers: int, kv_heads: int, head_dim: int, block_size: int, windows, num_seqs: int,
+                 dtype: torch.dtype, q_heads: Optional[int] = None, device=None, stream=None):
+        self.layers, self.kv_heads, self.head_dim = layers, kv_heads, head_dim
+        self.block_size, self.num_seqs, self.dtype = block_size, num_seqs, dtype
+        self.q_heads = q_heads or kv_heads
+        self.nbytes = hwkv_pool_bytes(layers, kv_heads, head_dim, block_size, windows, num_seqs, dtype)
+        device = torch.device(device or "cuda")
+        self.buffer = torch.empty(self.nbytes, dtype=torch.uint8, device=device)
+        self.handle = hwkv_pool_create(layers, kv_heads, head_dim, block_size, windows, num_seqs, dtype,
+                                       self.buffer, stream)
+        self.workspace = None
+        self._size_workspace()
+
+    def _size_workspace(self):
+        need = hwkv_decode_workspace_bytes(self.handle, self.q_heads)
+        if self.workspace is None or self.workspace.numel() < need:
+            self.workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=self.buffer.device)
+
+    def set_decode_config(self, split_tokens: int = 0, kernel: int = HWKV_KERNEL_AUTO):
+        hwkv_set_decode_config(self.handle, split_tokens, kernel)
+        self._size_workspace()
+
+    def geometry(self):
+        return hwkv_pool_geometry(self.handle)
+
+    def blocks(self) -> torch.Tensor:
+        """View of the pool as [total_blocks][2][block_size][head_dim] elements."""
+        _, total, _ = self.geometry()
+        return self.buffer.view(self.dtype).view(total, 2, self.block_size, self.head_dim)
+
+    def block_table(self, seq: int, layer: int, kv_head: int):
+        return hwkv_block_table(self.handle, seq, layer, kv_head)
+
+    def set_block_table(self, table, stream=None):
+        hwkv_set_block_table(self.handle, table, stream)
+
+    def materialize(self, layer: int, k_full, v_full, lens, stream=None):
+        hwkv_materialize(self.handle, layer, k_full, v_full, lens, stream)
+
+    def append(self, layer: int, k_new, v_new, pos, stream=None):
+        hwkv_append(self.handle, layer, k_new, v_new, pos, stream)
+
+    def decode(self, layer: int, q, scale: float, lens, out=None, stream=None):
+        if out is None:
+            out = torch.empty_like(q)
+        if q.shape[1] != self.q_heads:
+            self.q_heads = q.shape[1]
+            self._size_workspace()
+        hwkv_decode_attn(self.handle, layer, q, scale, lens, out, self.workspace, stream)
+        return out
+
+    def check_device_errors(self, stream=None) -> int:
+        return hwkv_check_device_errors(self.handle, stream)
+
+    def close(self):
+        if getattr(self, "handle", None):
+            hwkv_pool_destroy(self.handle)
+            self.handle = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass

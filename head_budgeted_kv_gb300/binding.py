@@ -1,0 +1,227 @@
+"""Thin ctypes binding of the hwkv C ABI (``include/hwkv.h``).
+
+Argument marshalling only: torch tensors become device pointers, torch streams become
+``cudaStream_t``.  Every step of the path runs in libhwkv.so; when the library is missing
+this module raises instead of computing anything itself.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional
+
+import numpy as np
+import torch
+
+from . import _build
+
+HWKV_OK = 0
+HWKV_ERR_INVALID_ARG = -1
+HWKV_ERR_ALIGNMENT = -2
+HWKV_ERR_POOL_TOO_SMALL = -3
+HWKV_ERR_CUDA = -4
+HWKV_ERR_DEVICE_CHECK = -5
+HWKV_ERR_UNSUPPORTED = -6
+HWKV_ERR_WORKSPACE_TOO_SMALL = -7
+
+HWKV_F32 = 0
+HWKV_BF16 = 1
+HWKV_KERNEL_AUTO, HWKV_KERNEL_TENSOR, HWKV_KERNEL_SIMT = 0, 1, 2
+HWKV_DEVERR_NEG_LENGTH, HWKV_DEVERR_BAD_BLOCK, HWKV_DEVERR_SRC_RANGE, HWKV_DEVERR_WAIT_TIMEOUT = 1, 2, 4, 8
+
+_c_i32p = ctypes.POINTER(ctypes.c_int32)
+_c_u64p = ctypes.POINTER(ctypes.c_uint64)
+_c_i64p = ctypes.POINTER(ctypes.c_int64)
+_vp = ctypes.c_void_p
+_i = ctypes.c_int
+_i64 = ctypes.c_int64
+_u64 = ctypes.c_uint64
+
+# (name, restype, argtypes) for every function declared in include/hwkv.h
+SIGNATURES = [
+    ("hwkv_abi_version", _i, []),
+    ("hwkv_last_error", ctypes.c_char_p, []),
+    ("hwkv_status_string", ctypes.c_char_p, [_i]),
+    ("hwkv_pool_bytes", _i, [_i, _i, _i, _i, _c_i32p, _i, _i, _c_u64p]),
+    ("hwkv_pool_create", _i, [_i, _i, _i, _i, _c_i32p, _i, _i, _vp, _u64, _vp, ctypes.POINTER(_vp)]),
+    ("hwkv_pool_destroy", _i, [_vp]),
+    ("hwkv_pool_geometry", _i, [_vp, _c_u64p, _c_i64p, _c_i64p]),
+    ("hwkv_block_table", _i, [_vp, _i, _i, _i, _c_i32p, _i, ctypes.POINTER(_i)]),
+    ("hwkv_set_block_table", _i, [_vp, _c_i32p, _i64, _vp]),
+    ("hwkv_materialize", _i, [_vp, _i, _vp, _vp, _i64, _i64, _i64, _vp, _vp]),
+    ("hwkv_append", _i, [_vp, _i, _vp, _vp, _vp, _vp]),
+    ("hwkv_decode_workspace_bytes", _i, [_vp, _i, _c_u64p]),
+    ("hwkv_decode_attn", _i, [_vp, _i, _vp, _i, ctypes.c_float, _vp, _vp, _vp, _u64, _vp]),
+    ("hwkv_set_decode_config", _i, [_vp, _i, _i]),
+    ("hwkv_check_device_errors", _i, [_vp, _vp, _c_i32p]),
+]
+
+_lib = None
+
+
+class HwkvError(RuntimeError):
+    def __init__(self, status: int, msg: str):
+        super().__init__(f"{status_string(status)} ({status}): {msg}")
+        self.status = status
+
+
+def library_path() -> str:
+    return _build.LIB
+
+
+def load(build_if_missing: bool = True):
+    """Load libhwkv.so (building it with nvcc first when it is missing)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    path = _build.LIB
+    if not os.path.exists(path):
+        if not build_if_missing:
+            raise RuntimeError(f"libhwkv.so not built ({path}); run __graft_entry__.build()")
+        _build.build()
+    lib = ctypes.CDLL(path)
+    for name, res, args in SIGNATURES:
+        fn = getattr(lib, name)
+        fn.restype = res
+        fn.argtypes = args
+    if lib.hwkv_abi_version() != 1:
+        raise RuntimeError("libhwkv.so ABI version mismatch")
+    _lib = lib
+    return lib
+
+
+def status_string(status: int) -> str:
+    return load().hwkv_status_string(status).decode()
+
+
+def last_error() -> str:
+    return load().hwkv_last_error().decode()
+
+
+def _check(status: int):
+    if status != HWKV_OK:
+        raise HwkvError(status, last_error())
+
+
+def _stream_ptr(stream) -> int:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def _ptr(t: Optional[torch.Tensor]) -> Optional[int]:
+    if t is None:
+        return None
+    if not isinstance(t, torch.Tensor):
+        return int(t)
+    return t.data_ptr()
+
+
+def _dtype_code(dtype) -> int:
+    if dtype in (HWKV_F32, HWKV_BF16):
+        return int(dtype)
+    if dtype in (torch.float32, "f32", "float32"):
+        return HWKV_F32
+    if dtype in (torch.bfloat16, "bf16", "bfloat16"):
+        return HWKV_BF16
+    raise ValueError(f"unsupported dtype {dtype}")
+
+
+def _windows(windows) -> np.ndarray:
+    return np.ascontiguousarray(np.asarray(windows, dtype=np.int32))
+
+
+# ------------------------------------------------------------------------------------
+# functions with the ABI's names
+# ------------------------------------------------------------------------------------
+def hwkv_abi_version() -> int:
+    return load().hwkv_abi_version()
+
+
+def hwkv_pool_bytes(layers, kv_heads, head_dim, block_size, windows, num_seqs, dtype) -> int:
+    w = _windows(windows)
+    out = ctypes.c_uint64(0)
+    _check(load().hwkv_pool_bytes(layers, kv_heads, head_dim, block_size, w.ctypes.data_as(_c_i32p), num_seqs,
+                                  _dtype_code(dtype), ctypes.byref(out)))
+    return out.value
+
+
+def hwkv_pool_create(layers, kv_heads, head_dim, block_size, windows, num_seqs, dtype, dev_pool: torch.Tensor,
+                     stream=None) -> int:
+    w = _windows(windows)
+    handle = ctypes.c_void_p(0)
+    nbytes = dev_pool.numel() * dev_pool.element_size()
+    _check(load().hwkv_pool_create(layers, kv_heads, head_dim, block_size, w.ctypes.data_as(_c_i32p), num_seqs,
+                                   _dtype_code(dtype), _ptr(dev_pool), nbytes, _stream_ptr(stream),
+                                   ctypes.byref(handle)))
+    return handle.value
+
+
+def hwkv_pool_destroy(pool: int):
+    _check(load().hwkv_pool_destroy(pool))
+
+
+def hwkv_pool_geometry(pool: int):
+    b, n, bb = ctypes.c_uint64(0), ctypes.c_int64(0), ctypes.c_int64(0)
+    _check(load().hwkv_pool_geometry(pool, ctypes.byref(b), ctypes.byref(n), ctypes.byref(bb)))
+    return b.value, n.value, bb.value
+
+
+def hwkv_block_table(pool: int, seq: int, layer: int, kv_head: int) -> np.ndarray:
+    n = ctypes.c_int(0)
+    _check(load().hwkv_block_table(pool, seq, layer, kv_head, None, 0, ctypes.byref(n)))
+    out = np.zeros(n.value, dtype=np.int32)
+    _check(load().hwkv_block_table(pool, seq, layer, kv_head, out.ctypes.data_as(_c_i32p), n.value, ctypes.byref(n)))
+    return out
+
+
+def hwkv_set_block_table(pool: int, table, stream=None):
+    t = np.ascontiguousarray(np.asarray(table, dtype=np.int32))
+    _check(load().hwkv_set_block_table(pool, t.ctypes.data_as(_c_i32p), t.size, _stream_ptr(stream)))
+
+
+def hwkv_materialize(pool: int, layer: int, k_full: torch.Tensor, v_full: torch.Tensor, lens: torch.Tensor,
+                     stream=None):
+    """k_full, v_full: [B][H][max_len][D] with contiguous rows; lens: int32 [B] on the device."""
+    if k_full.stride() != v_full.stride() or k_full.shape != v_full.shape:
+        raise ValueError("k_full and v_full must share shape and strides")
+    if k_full.stride(3) != 1 or k_full.stride(2) != k_full.shape[3]:
+        raise ValueError("rows of k_full must be contiguous")
+    _check(load().hwkv_materialize(pool, layer, _ptr(k_full), _ptr(v_full), k_full.stride(0), k_full.stride(1),
+                                   k_full.shape[2], _ptr(lens), _stream_ptr(stream)))
+
+
+def hwkv_append(pool: int, layer: int, k_new: torch.Tensor, v_new: torch.Tensor, pos: torch.Tensor, stream=None):
+    """k_new, v_new: contiguous [B][H][D]; pos: int32 [B] lengths before the append."""
+    if not (k_new.is_contiguous() and v_new.is_contiguous()):
+        raise ValueError("k_new and v_new must be contiguous")
+    _check(load().hwkv_append(pool, layer, _ptr(k_new), _ptr(v_new), _ptr(pos), _stream_ptr(stream)))
+
+
+def hwkv_decode_workspace_bytes(pool: int, q_heads: int) -> int:
+    out = ctypes.c_uint64(0)
+    _check(load().hwkv_decode_workspace_bytes(pool, q_heads, ctypes.byref(out)))
+    return out.value
+
+
+def hwkv_decode_attn(pool: int, layer: int, q: torch.Tensor, scale: float, lens: torch.Tensor, out: torch.Tensor,
+                     workspace: Optional[torch.Tensor], stream=None):
+    """q, out: contiguous [B][Hq][D]; lens: int32 [B] lengths after the append."""
+    if not (q.is_contiguous() and out.is_contiguous()):
+        raise ValueError("q and out must be contiguous")
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check(load().hwkv_decode_attn(pool, layer, _ptr(q), q.shape[1], float(scale), _ptr(lens), _ptr(out),
+                                   _ptr(workspace), ws_bytes, _stream_ptr(stream)))
+
+
+def hwkv_set_decode_config(pool: int, split_tokens: int = 0, kernel: int = HWKV_KERNEL_AUTO):
+    _check(load().hwkv_set_decode_config(pool, split_tokens, kernel))
+
+
+def hwkv_check_device_errors(pool: int, stream=None) -> int:
+    """Returns the device error bits (0 when clean) without raising."""
+    bits = ctypes.c_int32(0)
+    load().hwkv_check_device_errors(pool, _stream_ptr(stream), ctypes.byref(bits))
+    return bits.value

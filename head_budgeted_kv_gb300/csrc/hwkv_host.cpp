@@ -1,0 +1,531 @@
+// Host side of the hwkv C ABI: argument checks, pool geometry and block tables, the
+// tensor map of the pool, decode planning, and the launches.
+//
+// Geometry follows "HeadWiseKV: Budgeted Per-Head Cache Residency for Hybrid Long-Context
+// Language Models", section "Grouped-Cache Runtime" (ceil(w / block_size) blocks per head,
+// pre-allocated before serving) and abstract (the footprint is exact before serving).
+// Physical block ids start as the identity in (layer, seq, kv head, logical block) order.
+#include <cudaTypedefs.h>
+
+#include <algorithm>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <limits>
+#include <new>
+#include <string>
+#include <vector>
+
+#include "hwkv_internal.h"
+#include "../../include/hwkv.h"
+
+using namespace hwkv;
+
+namespace {
+
+thread_local std::string g_last_error;
+
+int fail(int code, const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof buf, fmt, ap);
+  va_end(ap);
+  g_last_error = buf;
+  return code;
+}
+
+int ok() {
+  g_last_error.clear();
+  return HWKV_OK;
+}
+
+#define HWKV_CUDA_TRY(expr, what)                                                           \
+  do {                                                                                     \
+    cudaError_t e_ = (expr);                                                               \
+    if (e_ != cudaSuccess) return fail(HWKV_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e_)); \
+  } while (0)
+
+struct Geometry {
+  int layers = 0, kv_heads = 0, head_dim = 0, block_size = 0, num_seqs = 0, dtype = 0, eb = 0;
+  std::vector<int32_t> windows, nblk;   // [layers * kv_heads]
+  std::vector<int64_t> tbl_base;        // [layers] table offset of (layer, seq 0, head 0)
+  std::vector<int32_t> seq_stride;      // [layers] sum_h nblk
+  int64_t total_blocks = 0;
+  uint64_t pool_bytes = 0;
+};
+
+constexpr int64_t kInt32Max = std::numeric_limits<int32_t>::max();
+
+int plan_geometry(int layers, int kv_heads, int head_dim, int block_size, const int32_t* windows, int num_seqs,
+                  int dtype, Geometry* g) {
+  if (layers < 1) return fail(HWKV_ERR_INVALID_ARG, "layers must be >= 1 (got %d)", layers);
+  if (kv_heads < 1 || kv_heads > kMaxKvHeads)
+    return fail(HWKV_ERR_UNSUPPORTED, "kv_heads must be in [1, %d] (got %d)", kMaxKvHeads, kv_heads);
+  if (head_dim != 64 && head_dim != 128)
+    return fail(HWKV_ERR_UNSUPPORTED, "head_dim must be 64 or 128 (got %d)", head_dim);
+  if (block_size < 1) return fail(HWKV_ERR_INVALID_ARG, "block_size must be >= 1 (got %d)", block_size);
+  if (num_seqs < 1) return fail(HWKV_ERR_INVALID_ARG, "num_seqs must be >= 1 (got %d)", num_seqs);
+  if (dtype != HWKV_F32 && dtype != HWKV_BF16) return fail(HWKV_ERR_INVALID_ARG, "unknown dtype %d", dtype);
+  if (!windows) return fail(HWKV_ERR_INVALID_ARG, "windows is NULL");
+  g->layers = layers;
+  g->kv_heads = kv_heads;
+  g->head_dim = head_dim;
+  g->block_size = block_size;
+  g->num_seqs = num_seqs;
+  g->dtype = dtype;
+  g->eb = dtype == HWKV_F32 ? 4 : 2;
+  g->windows.assign(windows, windows + (size_t)layers * kv_heads);
+  g->nblk.resize(g->windows.size());
+  g->tbl_base.resize(layers);
+  g->seq_stride.resize(layers);
+  int64_t blocks = 0;
+  for (int l = 0; l < layers; ++l) {
+    int64_t per_seq = 0;
+    for (int h = 0; h < kv_heads; ++h) {
+      const int64_t w = g->windows[(size_t)l * kv_heads + h];
+      if (w < 1) return fail(HWKV_ERR_INVALID_ARG, "window of layer %d head %d must be >= 1 (got %lld)", l, h, (long long)w);
+      const int64_t nb = (w + block_size - 1) / block_size;  // ceil(w / block_size)
+      if (nb * block_size > kInt32Max)
+        return fail(HWKV_ERR_UNSUPPORTED, "ring of layer %d head %d exceeds 2^31 tokens", l, h);
+      g->nblk[(size_t)l * kv_heads + h] = (int32_t)nb;
+      per_seq += nb;
+    }
+    if (per_seq > kInt32Max) return fail(HWKV_ERR_UNSUPPORTED, "layer %d has more than 2^31 blocks per sequence", l);
+    g->tbl_base[l] = blocks;
+    g->seq_stride[l] = (int32_t)per_seq;
+    blocks += per_seq * num_seqs;
+    if (blocks * 2 * (int64_t)block_size > kInt32Max)
+      return fail(HWKV_ERR_UNSUPPORTED, "pool exceeds 2^31 rows (blocks x 2 x block_size)");
+  }
+  g->total_blocks = blocks;
+  g->pool_bytes = (uint64_t)blocks * 2u * (uint64_t)block_size * (uint64_t)head_dim * (uint64_t)g->eb;
+  return HWKV_OK;
+}
+
+struct LayerPlan {
+  int32_t split = 0;
+  int32_t items = 0;
+  bool multi_chunk = false;
+  int32_t chunk_prefix[kMaxKvHeads + 1] = {};
+};
+
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  if (!fn) {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  }
+  return fn;
+}
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
+
+}  // namespace
+
+struct hwkv_pool {
+  Geometry g;
+  char* dev_pool = nullptr;
+  void* d_meta = nullptr;
+  int32_t* d_tbl = nullptr;
+  int32_t* d_err = nullptr;
+  std::vector<int32_t> h_tbl;
+  int device = 0;
+  int num_sms = 0;
+  int split_override = 0;
+  int kernel_choice = HWKV_KERNEL_AUTO;
+  std::vector<LayerPlan> plans;
+  bool has_tmap = false;
+  alignas(64) CUtensorMap tmap;
+};
+
+namespace {
+
+bool tc_eligible(const hwkv_pool* p) {
+  return p->g.dtype == HWKV_BF16 && p->g.block_size % 16 == 0 && p->has_tmap;
+}
+
+bool use_tc(const hwkv_pool* p) {
+  if (p->kernel_choice == HWKV_KERNEL_SIMT) return false;
+  return tc_eligible(p);
+}
+
+void plan_decode(hwkv_pool* p) {
+  const Geometry& g = p->g;
+  p->plans.assign(g.layers, LayerPlan());
+  for (int l = 0; l < g.layers; ++l) {
+    LayerPlan& lp = p->plans[l];
+    int64_t tokens = 0;
+    for (int h = 0; h < g.kv_heads; ++h) tokens += (int64_t)g.nblk[(size_t)l * g.kv_heads + h] * g.block_size;
+    tokens *= g.num_seqs;
+    int32_t split = p->split_override;
+    if (split == 0) {
+      // about four waves of two CTAs per SM; powers of two so the level-set windows
+      // (1K .. 64K) split into equal chunks
+      const int64_t want = tokens / std::max<int64_t>(1, 8LL * std::max(1, p->num_sms));
+      split = 256;
+      while (split < want && split < 2048) split <<= 1;
+    }
+    lp.split = split;
+    lp.chunk_prefix[0] = 0;
+    for (int h = 0; h < g.kv_heads; ++h) {
+      const int64_t C = (int64_t)g.nblk[(size_t)l * g.kv_heads + h] * g.block_size;
+      const int32_t n = (int32_t)((C + split - 1) / split);
+      lp.chunk_prefix[h + 1] = lp.chunk_prefix[h] + n;
+      if (n > 1) lp.multi_chunk = true;
+    }
+    lp.items = lp.chunk_prefix[g.kv_heads] * g.num_seqs;
+  }
+}
+
+uint64_t workspace_bytes(const hwkv_pool* p, int group) {
+  int64_t items = 0;
+  for (const LayerPlan& lp : p->plans)
+    if (lp.multi_chunk) items = std::max<int64_t>(items, lp.items);
+  return (uint64_t)items * group * (p->g.head_dim + 2) * sizeof(float);
+}
+
+int check_device(const hwkv_pool* p) {
+  int dev = -1;
+  HWKV_CUDA_TRY(cudaGetDevice(&dev), "cudaGetDevice");
+  if (dev != p->device) return fail(HWKV_ERR_INVALID_ARG, "pool lives on device %d but device %d is current", p->device, dev);
+  return HWKV_OK;
+}
+
+PoolView pool_view(const hwkv_pool* p) {
+  PoolView v;
+  v.pool = p->dev_pool;
+  v.tbl = p->d_tbl;
+  v.err = p->d_err;
+  v.total_blocks = p->g.total_blocks;
+  v.block_size = p->g.block_size;
+  v.head_dim = p->g.head_dim;
+  v.kv_heads = p->g.kv_heads;
+  v.num_seqs = p->g.num_seqs;
+  v.elem_bytes = p->g.eb;
+  return v;
+}
+
+LayerGeom layer_geom(const hwkv_pool* p, int layer) {
+  const Geometry& g = p->g;
+  LayerGeom lg;
+  std::memset(&lg, 0, sizeof lg);
+  lg.tbl_base = g.tbl_base[layer];
+  lg.tbl_seq_stride = g.seq_stride[layer];
+  lg.nblk_prefix[0] = 0;
+  for (int h = 0; h < g.kv_heads; ++h) {
+    lg.nblk_prefix[h + 1] = lg.nblk_prefix[h] + g.nblk[(size_t)layer * g.kv_heads + h];
+    lg.window[h] = g.windows[(size_t)layer * g.kv_heads + h];
+  }
+  return lg;
+}
+
+}  // namespace
+
+extern "C" {
+
+int hwkv_abi_version(void) { return HWKV_ABI_VERSION; }
+
+const char* hwkv_last_error(void) { return g_last_error.c_str(); }
+
+const char* hwkv_status_string(int status) {
+  switch (status) {
+    case HWKV_OK: return "HWKV_OK";
+    case HWKV_ERR_INVALID_ARG: return "HWKV_ERR_INVALID_ARG";
+    case HWKV_ERR_ALIGNMENT: return "HWKV_ERR_ALIGNMENT";
+    case HWKV_ERR_POOL_TOO_SMALL: return "HWKV_ERR_POOL_TOO_SMALL";
+    case HWKV_ERR_CUDA: return "HWKV_ERR_CUDA";
+    case HWKV_ERR_DEVICE_CHECK: return "HWKV_ERR_DEVICE_CHECK";
+    case HWKV_ERR_UNSUPPORTED: return "HWKV_ERR_UNSUPPORTED";
+    case HWKV_ERR_WORKSPACE_TOO_SMALL: return "HWKV_ERR_WORKSPACE_TOO_SMALL";
+    default: return "HWKV_ERR_UNKNOWN";
+  }
+}
+
+int hwkv_pool_bytes(int layers, int kv_heads, int head_dim, int block_size, const int32_t* windows, int num_seqs,
+                    int dtype, uint64_t* out_bytes) {
+  if (!out_bytes) return fail(HWKV_ERR_INVALID_ARG, "out_bytes is NULL");
+  Geometry g;
+  const int rc = plan_geometry(layers, kv_heads, head_dim, block_size, windows, num_seqs, dtype, &g);
+  if (rc != HWKV_OK) return rc;
+  *out_bytes = g.pool_bytes;
+  return ok();
+}
+
+int hwkv_pool_create(int layers, int kv_heads, int head_dim, int block_size, const int32_t* windows, int num_seqs,
+                     int dtype, void* dev_pool, uint64_t dev_pool_bytes, void* stream, hwkv_pool_t* out) {
+  if (!out) return fail(HWKV_ERR_INVALID_ARG, "out is NULL");
+  *out = nullptr;
+  Geometry g;
+  int rc = plan_geometry(layers, kv_heads, head_dim, block_size, windows, num_seqs, dtype, &g);
+  if (rc != HWKV_OK) return rc;
+  if (!dev_pool) return fail(HWKV_ERR_INVALID_ARG, "dev_pool is NULL");
+  if (!aligned(dev_pool, 256)) return fail(HWKV_ERR_ALIGNMENT, "dev_pool must be 256-byte aligned");
+  if (dev_pool_bytes < g.pool_bytes)
+    return fail(HWKV_ERR_POOL_TOO_SMALL, "pool buffer holds %llu bytes, the windows need %llu",
+                (unsigned long long)dev_pool_bytes, (unsigned long long)g.pool_bytes);
+  int dev = 0;
+  HWKV_CUDA_TRY(cudaGetDevice(&dev), "cudaGetDevice");
+  cudaPointerAttributes attr;
+  HWKV_CUDA_TRY(cudaPointerGetAttributes(&attr, dev_pool), "cudaPointerGetAttributes");
+  if ((attr.type != cudaMemoryTypeDevice && attr.type != cudaMemoryTypeManaged) || attr.device != dev)
+    return fail(HWKV_ERR_INVALID_ARG, "dev_pool is not device memory of the current device %d", dev);
+
+  hwkv_pool* p = new (std::nothrow) hwkv_pool();
+  if (!p) return fail(HWKV_ERR_INVALID_ARG, "out of host memory");
+  p->g = std::move(g);
+  p->dev_pool = static_cast<char*>(dev_pool);
+  p->device = dev;
+  cudaError_t e = cudaDeviceGetAttribute(&p->num_sms, cudaDevAttrMultiProcessorCount, dev);
+  if (e != cudaSuccess) {
+    delete p;
+    return fail(HWKV_ERR_CUDA, "cudaDeviceGetAttribute: %s", cudaGetErrorString(e));
+  }
+  const size_t tbl_bytes = ((size_t)p->g.total_blocks * sizeof(int32_t) + 255) & ~(size_t)255;
+  e = cudaMalloc(&p->d_meta, tbl_bytes + 256);
+  if (e != cudaSuccess) {
+    delete p;
+    return fail(HWKV_ERR_CUDA, "cudaMalloc of the block table: %s", cudaGetErrorString(e));
+  }
+  p->d_tbl = static_cast<int32_t*>(p->d_meta);
+  p->d_err = reinterpret_cast<int32_t*>(static_cast<char*>(p->d_meta) + tbl_bytes);
+  p->h_tbl.resize((size_t)p->g.total_blocks);
+  for (int64_t i = 0; i < p->g.total_blocks; ++i) p->h_tbl[(size_t)i] = (int32_t)i;
+
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  auto cleanup_fail = [&](const char* what, cudaError_t err) {
+    cudaStreamSynchronize(st);
+    cudaFree(p->d_meta);
+    delete p;
+    return fail(HWKV_ERR_CUDA, "%s: %s", what, cudaGetErrorString(err));
+  };
+  if ((e = cudaMemcpyAsync(p->d_tbl, p->h_tbl.data(), (size_t)p->g.total_blocks * sizeof(int32_t),
+                           cudaMemcpyHostToDevice, st)) != cudaSuccess)
+    return cleanup_fail("upload of the block table", e);
+  if ((e = cudaMemsetAsync(p->d_err, 0, sizeof(int32_t), st)) != cudaSuccess) return cleanup_fail("cudaMemsetAsync", e);
+  if ((e = cudaMemsetAsync(p->dev_pool, 0, p->g.pool_bytes, st)) != cudaSuccess)
+    return cleanup_fail("zero-fill of the pool", e);
+  if ((e = cudaStreamSynchronize(st)) != cudaSuccess) return cleanup_fail("cudaStreamSynchronize", e);
+
+  if (p->g.dtype == HWKV_BF16 && p->g.block_size % 16 == 0) {
+    PFN_cuTensorMapEncodeTiled_v12000 encode = tensor_map_encoder();
+    if (encode) {
+      const int64_t rows = p->g.total_blocks * 2 * p->g.block_size;
+      cuuint64_t dims[2] = {(cuuint64_t)p->g.head_dim, (cuuint64_t)rows};
+      cuuint64_t strides[1] = {(cuuint64_t)p->g.head_dim * 2};
+      cuuint32_t box[2] = {64, 16};
+      cuuint32_t estr[2] = {1, 1};
+      CUresult cr = encode(&p->tmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, p->dev_pool, dims, strides, box, estr,
+                           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+      p->has_tmap = cr == CUDA_SUCCESS;
+    }
+  }
+  if (p->has_tmap) {
+    e = configure_decode_tc(p->g.head_dim);
+    if (e != cudaSuccess) return cleanup_fail("cudaFuncSetAttribute", e);
+  }
+  plan_decode(p);
+  *out = p;
+  return ok();
+}
+
+int hwkv_pool_destroy(hwkv_pool_t p) {
+  if (!p) return ok();
+  cudaError_t e = cudaFree(p->d_meta);
+  delete p;
+  if (e != cudaSuccess) return fail(HWKV_ERR_CUDA, "cudaFree: %s", cudaGetErrorString(e));
+  return ok();
+}
+
+int hwkv_pool_geometry(hwkv_pool_t p, uint64_t* pool_bytes, int64_t* total_blocks, int64_t* block_bytes) {
+  if (!p) return fail(HWKV_ERR_INVALID_ARG, "pool is NULL");
+  if (pool_bytes) *pool_bytes = p->g.pool_bytes;
+  if (total_blocks) *total_blocks = p->g.total_blocks;
+  if (block_bytes) *block_bytes = 2LL * p->g.block_size * p->g.head_dim * p->g.eb;
+  return ok();
+}
+
+int hwkv_block_table(hwkv_pool_t p, int seq, int layer, int kv_head, int32_t* host_out, int cap, int* n) {
+  if (!p) return fail(HWKV_ERR_INVALID_ARG, "pool is NULL");
+  const Geometry& g = p->g;
+  if (seq < 0 || seq >= g.num_seqs || layer < 0 || layer >= g.layers || kv_head < 0 || kv_head >= g.kv_heads)
+    return fail(HWKV_ERR_INVALID_ARG, "seq/layer/kv_head out of range");
+  const int32_t nb = g.nblk[(size_t)layer * g.kv_heads + kv_head];
+  if (n) *n = nb;
+  if (!host_out && cap > 0) return fail(HWKV_ERR_INVALID_ARG, "host_out is NULL");
+  int64_t off = g.tbl_base[layer] + (int64_t)seq * g.seq_stride[layer];
+  for (int h = 0; h < kv_head; ++h) off += g.nblk[(size_t)layer * g.kv_heads + h];
+  for (int j = 0; j < nb && j < cap; ++j) host_out[j] = p->h_tbl[(size_t)(off + j)];
+  return ok();
+}
+
+int hwkv_set_block_table(hwkv_pool_t p, const int32_t* host_table, int64_t n, void* stream) {
+  if (!p) return fail(HWKV_ERR_INVALID_ARG, "pool is NULL");
+  if (!host_table) return fail(HWKV_ERR_INVALID_ARG, "host_table is NULL");
+  if (n != p->g.total_blocks)
+    return fail(HWKV_ERR_INVALID_ARG, "table has %lld entries, the pool %lld blocks", (long long)n,
+                (long long)p->g.total_blocks);
+  std::vector<char> seen((size_t)n, 0);
+  for (int64_t i = 0; i < n; ++i) {
+    const int32_t b = host_table[i];
+    if (b < 0 || b >= n || seen[(size_t)b])
+      return fail(HWKV_ERR_INVALID_ARG, "table entry %lld (%d) is out of range or repeated", (long long)i, b);
+    seen[(size_t)b] = 1;
+  }
+  int rc = check_device(p);
+  if (rc != HWKV_OK) return rc;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  HWKV_CUDA_TRY(cudaMemcpyAsync(p->d_tbl, host_table, (size_t)n * sizeof(int32_t), cudaMemcpyHostToDevice, st),
+                "upload of the block table");
+  HWKV_CUDA_TRY(cudaStreamSynchronize(st), "cudaStreamSynchronize");
+  p->h_tbl.assign(host_table, host_table + n);
+  return ok();
+}
+
+int hwkv_materialize(hwkv_pool_t p, int layer, const void* k_full, const void* v_full, int64_t seq_stride,
+                     int64_t head_stride, int64_t max_len, const int32_t* lens_dev, void* stream) {
+  if (!p) return fail(HWKV_ERR_INVALID_ARG, "pool is NULL");
+  const Geometry& g = p->g;
+  if (layer < 0 || layer >= g.layers) return fail(HWKV_ERR_INVALID_ARG, "layer %d out of range", layer);
+  if (!k_full || !v_full || !lens_dev) return fail(HWKV_ERR_INVALID_ARG, "NULL tensor argument");
+  if (!aligned(k_full, 16) || !aligned(v_full, 16) || !aligned(lens_dev, 4))
+    return fail(HWKV_ERR_ALIGNMENT, "k_full / v_full must be 16-byte aligned, lens 4-byte aligned");
+  if (seq_stride < 0 || head_stride < 0 || max_len < 0) return fail(HWKV_ERR_INVALID_ARG, "negative stride or max_len");
+  if ((seq_stride * g.eb) % 16 != 0 || (head_stride * g.eb) % 16 != 0)
+    return fail(HWKV_ERR_ALIGNMENT, "seq_stride and head_stride must be multiples of 16 bytes");
+  if (max_len > kInt32Max) return fail(HWKV_ERR_INVALID_ARG, "max_len must be below 2^31");
+  int rc = check_device(p);
+  if (rc != HWKV_OK) return rc;
+  CopyArgs a;
+  std::memset(&a, 0, sizeof a);
+  a.pv = pool_view(p);
+  a.g = layer_geom(p, layer);
+  a.k = k_full;
+  a.v = v_full;
+  a.seq_stride = seq_stride;
+  a.head_stride = head_stride;
+  a.max_len = max_len;
+  a.lens = lens_dev;
+  int64_t max_rows = 0;
+  for (int h = 0; h < g.kv_heads; ++h) max_rows = std::max<int64_t>(max_rows, a.g.window[h]);
+  max_rows = std::min<int64_t>(max_rows, max_len);
+  if (max_rows == 0) return ok();
+  HWKV_CUDA_TRY(launch_materialize(a, g.dtype, (int)max_rows, static_cast<cudaStream_t>(stream)), "materialize launch");
+  return ok();
+}
+
+int hwkv_append(hwkv_pool_t p, int layer, const void* k_new, const void* v_new, const int32_t* pos_dev, void* stream) {
+  if (!p) return fail(HWKV_ERR_INVALID_ARG, "pool is NULL");
+  const Geometry& g = p->g;
+  if (layer < 0 || layer >= g.layers) return fail(HWKV_ERR_INVALID_ARG, "layer %d out of range", layer);
+  if (!k_new || !v_new || !pos_dev) return fail(HWKV_ERR_INVALID_ARG, "NULL tensor argument");
+  if (!aligned(k_new, 16) || !aligned(v_new, 16) || !aligned(pos_dev, 4))
+    return fail(HWKV_ERR_ALIGNMENT, "k_new / v_new must be 16-byte aligned, pos 4-byte aligned");
+  int rc = check_device(p);
+  if (rc != HWKV_OK) return rc;
+  CopyArgs a;
+  std::memset(&a, 0, sizeof a);
+  a.pv = pool_view(p);
+  a.g = layer_geom(p, layer);
+  a.k = k_new;
+  a.v = v_new;
+  a.lens = pos_dev;
+  HWKV_CUDA_TRY(launch_append(a, g.dtype, static_cast<cudaStream_t>(stream)), "append launch");
+  return ok();
+}
+
+int hwkv_decode_workspace_bytes(hwkv_pool_t p, int q_heads, uint64_t* out) {
+  if (!p || !out) return fail(HWKV_ERR_INVALID_ARG, "NULL argument");
+  if (q_heads < p->g.kv_heads || q_heads % p->g.kv_heads != 0 || q_heads / p->g.kv_heads > kMaxGroup)
+    return fail(HWKV_ERR_UNSUPPORTED, "q_heads must be G * kv_heads with 1 <= G <= %d", kMaxGroup);
+  *out = workspace_bytes(p, q_heads / p->g.kv_heads);
+  return ok();
+}
+
+int hwkv_decode_attn(hwkv_pool_t p, int layer, const void* q, int q_heads, float scale, const int32_t* lens_dev,
+                     void* out, void* workspace, uint64_t ws_bytes, void* stream) {
+  if (!p) return fail(HWKV_ERR_INVALID_ARG, "pool is NULL");
+  const Geometry& g = p->g;
+  if (layer < 0 || layer >= g.layers) return fail(HWKV_ERR_INVALID_ARG, "layer %d out of range", layer);
+  if (q_heads < g.kv_heads || q_heads % g.kv_heads != 0 || q_heads / g.kv_heads > kMaxGroup)
+    return fail(HWKV_ERR_UNSUPPORTED, "q_heads must be G * kv_heads with 1 <= G <= %d (got %d)", kMaxGroup, q_heads);
+  if (!(scale == scale) || scale == std::numeric_limits<float>::infinity() ||
+      scale == -std::numeric_limits<float>::infinity())
+    return fail(HWKV_ERR_INVALID_ARG, "scale must be finite");
+  if (!q || !out || !lens_dev) return fail(HWKV_ERR_INVALID_ARG, "NULL tensor argument");
+  if (!aligned(q, 16) || !aligned(out, 16) || !aligned(lens_dev, 4))
+    return fail(HWKV_ERR_ALIGNMENT, "q / out must be 16-byte aligned, lens 4-byte aligned");
+  const int G = q_heads / g.kv_heads;
+  const LayerPlan& lp = p->plans[layer];
+  const uint64_t need = workspace_bytes(p, G);
+  if (lp.multi_chunk) {
+    if (!workspace || ws_bytes < need)
+      return fail(HWKV_ERR_WORKSPACE_TOO_SMALL, "workspace holds %llu bytes, decode needs %llu",
+                  (unsigned long long)ws_bytes, (unsigned long long)need);
+    if (!aligned(workspace, 16)) return fail(HWKV_ERR_ALIGNMENT, "workspace must be 16-byte aligned");
+  }
+  int rc = check_device(p);
+  if (rc != HWKV_OK) return rc;
+  if (p->kernel_choice == HWKV_KERNEL_TENSOR && !tc_eligible(p))
+    return fail(HWKV_ERR_UNSUPPORTED, "tensor-core decode needs bf16 and block_size % 16 == 0");
+
+  DecodeArgs a;
+  std::memset(&a, 0, sizeof a);
+  a.pv = pool_view(p);
+  a.g = layer_geom(p, layer);
+  a.q = q;
+  a.out = out;
+  a.lens = lens_dev;
+  int64_t items_max = 0;
+  for (const LayerPlan& x : p->plans)
+    if (x.multi_chunk) items_max = std::max<int64_t>(items_max, x.items);
+  a.part_acc = static_cast<float*>(workspace);
+  a.part_ml = workspace ? static_cast<float*>(workspace) + items_max * G * g.head_dim : nullptr;
+  a.scale_log2 = scale * 1.4426950408889634f;
+  a.group = G;
+  a.split_tokens = lp.split;
+  std::memcpy(a.chunk_prefix, lp.chunk_prefix, sizeof a.chunk_prefix);
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (use_tc(p)) {
+    HWKV_CUDA_TRY(launch_decode_tc(a, &p->tmap, lp.items, st), "decode launch");
+  } else {
+    HWKV_CUDA_TRY(launch_decode_simt(a, g.dtype, lp.items, st), "decode launch");
+  }
+  if (lp.multi_chunk) HWKV_CUDA_TRY(launch_combine(a, g.dtype, st), "combine launch");
+  return ok();
+}
+
+int hwkv_set_decode_config(hwkv_pool_t p, int split_tokens, int kernel) {
+  if (!p) return fail(HWKV_ERR_INVALID_ARG, "pool is NULL");
+  if (split_tokens != 0 &&
+      (split_tokens < 16 || split_tokens > 65536 || (split_tokens & (split_tokens - 1)) != 0))
+    return fail(HWKV_ERR_INVALID_ARG, "split_tokens must be 0 or a power of two in [16, 65536]");
+  if (kernel != HWKV_KERNEL_AUTO && kernel != HWKV_KERNEL_TENSOR && kernel != HWKV_KERNEL_SIMT)
+    return fail(HWKV_ERR_INVALID_ARG, "unknown kernel %d", kernel);
+  if (kernel == HWKV_KERNEL_TENSOR && !tc_eligible(p))
+    return fail(HWKV_ERR_UNSUPPORTED, "tensor-core decode needs bf16 and block_size % 16 == 0");
+  p->split_override = split_tokens;
+  p->kernel_choice = kernel;
+  plan_decode(p);
+  return ok();
+}
+
+int hwkv_check_device_errors(hwkv_pool_t p, void* stream, int32_t* out_bits) {
+  if (!p) return fail(HWKV_ERR_INVALID_ARG, "pool is NULL");
+  int rc = check_device(p);
+  if (rc != HWKV_OK) return rc;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  int32_t bits = 0;
+  HWKV_CUDA_TRY(cudaStreamSynchronize(st), "cudaStreamSynchronize");
+  HWKV_CUDA_TRY(cudaMemcpy(&bits, p->d_err, sizeof bits, cudaMemcpyDeviceToHost), "read of the error word");
+  HWKV_CUDA_TRY(cudaMemset(p->d_err, 0, sizeof bits), "reset of the error word");
+  if (out_bits) *out_bits = bits;
+  if (bits != 0) return fail(HWKV_ERR_DEVICE_CHECK, "device error bits 0x%x", bits);
+  return ok();
+}
+
+}  // extern "C"

@@ -1,0 +1,71 @@
+// Internal declarations shared by the host side of the C ABI (hwkv_host.cpp) and the
+// sm_103a kernels (hwkv_copy.cu, hwkv_decode.cu).  Not part of the public ABI.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace hwkv {
+
+constexpr int kMaxKvHeads = 32;
+constexpr int kMaxGroup = 8;
+
+// Geometry of one layer, passed by value to every kernel of that layer.
+//   table entry of (seq s, kv head h, logical block j) = tbl[tbl_base + s*tbl_seq_stride
+//                                                          + nblk_prefix[h] + j]
+struct LayerGeom {
+  int64_t tbl_base;
+  int32_t tbl_seq_stride;                 // sum_h nblk[h]
+  int32_t nblk_prefix[kMaxKvHeads + 1];   // prefix sums of nblk over heads
+  int32_t window[kMaxKvHeads];            // static window w per head
+};
+
+struct PoolView {
+  void* pool;              // physical blocks [total_blocks][2][bs][D]
+  const int32_t* tbl;      // flat block table
+  int32_t* err;            // device error word
+  int64_t total_blocks;
+  int32_t block_size;
+  int32_t head_dim;
+  int32_t kv_heads;
+  int32_t num_seqs;
+  int32_t elem_bytes;      // 4 (f32) or 2 (bf16)
+};
+
+struct CopyArgs {
+  PoolView pv;
+  LayerGeom g;
+  const void* k;           // materialise: full prefill; append: new token rows
+  const void* v;
+  int64_t seq_stride;      // elements (materialise only)
+  int64_t head_stride;     // elements (materialise only)
+  int64_t max_len;         // rows per (s, h) in the source (materialise only)
+  const int32_t* lens;     // materialise: prefill lengths; append: positions
+  int32_t rows_per_cta;    // materialise only
+};
+
+struct DecodeArgs {
+  PoolView pv;
+  LayerGeom g;
+  const void* q;           // [B][Hq][D]
+  void* out;               // [B][Hq][D]
+  const int32_t* lens;     // [B] lengths after the append
+  float* part_acc;         // [items][G][D]   unnormalised split accumulators
+  float* part_ml;          // [items][G][2]   (running max in log2 units, sum of weights)
+  float scale_log2;        // scale * log2(e)
+  int32_t group;           // G = Hq / H
+  int32_t split_tokens;    // tokens per split-K chunk (power of two, multiple of 16)
+  int32_t chunk_prefix[kMaxKvHeads + 1];  // prefix sums over heads of ceil(C_h / split)
+};
+
+// Launchers (hwkv_copy.cu, hwkv_decode.cu).  dtype: 0 = f32, 1 = bf16.
+cudaError_t launch_append(const CopyArgs& a, int dtype, cudaStream_t st);
+// max_rows: the most positions any (seq, head) of the layer copies, min(max window, max_len)
+cudaError_t launch_materialize(const CopyArgs& a, int dtype, int max_rows, cudaStream_t st);
+cudaError_t configure_decode_tc(int head_dim);  // once per device before the first launch
+cudaError_t launch_decode_tc(const DecodeArgs& a, const CUtensorMap* tmap, int items, cudaStream_t st);
+cudaError_t launch_decode_simt(const DecodeArgs& a, int dtype, int items, cudaStream_t st);
+cudaError_t launch_combine(const DecodeArgs& a, int dtype, cudaStream_t st);
+
+}  // namespace hwkv

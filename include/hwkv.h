@@ -1,0 +1,180 @@
+/*
+ * hwkv -- per-head budgeted KV residency on one GB300 (sm_103a).
+ *
+ * C ABI of the grouped-cache runtime described in "HeadWiseKV: Budgeted Per-Head Cache
+ * Residency for Hybrid Long-Context Language Models" (blog summary):
+ *
+ *   - abstract: every physical KV head of a residual global-attention layer gets a static
+ *     history window w; the runtime MATERIALISES that residency (it keeps only the window)
+ *     instead of masking a full cache, so the cache footprint is exact before serving;
+ *   - section "Grouped-Cache Runtime": a paged block table gives each head
+ *     ceil(w / block_size) KV blocks, pre-allocated before serving.
+ *
+ * Terms used below
+ *   L  layers (global-attention layers only), H kv heads, Hq query heads (Hq = G * H),
+ *   D  head_dim, bs block_size, B num_seqs, eb element bytes (4 for F32, 2 for BF16).
+ *   nblk[l][h] = ceil(w[l][h] / bs);  ring capacity C[l][h] = nblk[l][h] * bs tokens.
+ *   Token position p of (seq, layer, head) lives in ring slot p mod C; slot t is row
+ *   t mod bs of logical block t / bs, which the block table maps to a physical block.
+ *   A physical block is [2][bs][D] elements: bs K rows, then bs V rows (2*bs*D*eb bytes).
+ *   Query head q reads kv head q / G (consecutive groups).
+ *   Decode attention at length len covers positions [max(0, len - w), len): the last
+ *   min(w, len) tokens, including the one appended in the same step.
+ *
+ * Conventions
+ *   - Every function returns an int status (HWKV_OK or a negative HWKV_ERR_*); on error
+ *     hwkv_last_error() (thread-local) describes it.  Argument errors are reported before
+ *     anything is launched.
+ *   - Pointers named *_dev and every tensor argument are DEVICE pointers on the current
+ *     CUDA device; the caller owns them (e.g. torch tensors).  `stream` is a cudaStream_t
+ *     (NULL = legacy default stream).  Calls that take a stream are asynchronous on it.
+ *   - Lengths and positions live on the device so that a captured CUDA graph stays valid
+ *     across decode steps; kernels check them and record problems in a device error word
+ *     that hwkv_check_device_errors() reads.  Kernels never trap or spin without bound.
+ *   - Inputs must be finite: a masked pool row that holds Inf/NaN bits can still poison
+ *     a result (0 * Inf), as in any attention kernel.
+ */
+#ifndef HWKV_H
+#define HWKV_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define HWKV_ABI_VERSION 1
+
+/* status codes */
+#define HWKV_OK 0
+#define HWKV_ERR_INVALID_ARG (-1)
+#define HWKV_ERR_ALIGNMENT (-2)
+#define HWKV_ERR_POOL_TOO_SMALL (-3)
+#define HWKV_ERR_CUDA (-4)
+#define HWKV_ERR_DEVICE_CHECK (-5)
+#define HWKV_ERR_UNSUPPORTED (-6)
+#define HWKV_ERR_WORKSPACE_TOO_SMALL (-7)
+
+/* element types of the pool and of every tensor passed with it */
+#define HWKV_F32 0
+#define HWKV_BF16 1
+
+/* decode kernel selection for hwkv_set_decode_config */
+#define HWKV_KERNEL_AUTO 0   /* tensor-core kernel where supported, else CUDA-core kernel */
+#define HWKV_KERNEL_TENSOR 1 /* bf16, bs % 16 == 0 only                                     */
+#define HWKV_KERNEL_SIMT 2   /* CUDA-core kernel, any supported shape                          */
+
+/* bits of the device error word */
+#define HWKV_DEVERR_NEG_LENGTH 1     /* a length / position below 0                    */
+#define HWKV_DEVERR_BAD_BLOCK 2      /* a block-table entry outside the pool            */
+#define HWKV_DEVERR_SRC_RANGE 4      /* materialise length above max_len               */
+#define HWKV_DEVERR_WAIT_TIMEOUT 8   /* a pipeline wait gave up (work was skipped)      */
+
+typedef struct hwkv_pool* hwkv_pool_t;
+
+/* ABI / layout version (kernel-ABI compatibility check of the cache layout).  Returns
+ * HWKV_ABI_VERSION of the loaded library. */
+int hwkv_abi_version(void);
+
+/* Thread-local description of the last error on this thread ("" if none). */
+const char* hwkv_last_error(void);
+
+/* Short constant name of a status code. */
+const char* hwkv_status_string(int status);
+
+/* Pre-serving footprint prediction ("Grouped-Cache Runtime": ceil(w / bs) blocks per head;
+ * abstract: demand known exactly before serving).  Pure host, needs no GPU.
+ *   windows: host int32 [layers][kv_heads], each >= 1.
+ *   out_bytes = num_seqs * sum_{l,h} ceil(w[l][h]/bs) * bs * head_dim * 2 * eb.
+ * Supported: 1 <= kv_heads <= 32, head_dim in {64, 128}, block_size >= 1, dtype F32/BF16,
+ * every ring capacity below 2^31 tokens and at most 2^31 - 1 blocks in total.
+ * Errors: HWKV_ERR_INVALID_ARG, HWKV_ERR_UNSUPPORTED. */
+int hwkv_pool_bytes(int layers, int kv_heads, int head_dim, int block_size, const int32_t* windows,
+                    int num_seqs, int dtype, uint64_t* out_bytes);
+
+/* Binds a caller-owned device buffer as the per-head paged pool ("Grouped-Cache Runtime").
+ *   dev_pool: device pointer, 256-byte aligned, dev_pool_bytes >= hwkv_pool_bytes().
+ *   The pool is zero-filled on `stream`.  The block table starts as the identity map with
+ *   physical ids handed out in (layer, seq, kv head, logical block) order.
+ *   The library allocates its own small device metadata (block table, error word) and
+ *   frees it in hwkv_pool_destroy; the pool buffer itself is never freed by the library.
+ *   Synchronises `stream` before returning.
+ * Errors: HWKV_ERR_INVALID_ARG, HWKV_ERR_UNSUPPORTED, HWKV_ERR_ALIGNMENT (pool pointer),
+ *         HWKV_ERR_POOL_TOO_SMALL (checked before anything is written), HWKV_ERR_CUDA. */
+int hwkv_pool_create(int layers, int kv_heads, int head_dim, int block_size, const int32_t* windows,
+                     int num_seqs, int dtype, void* dev_pool, uint64_t dev_pool_bytes, void* stream,
+                     hwkv_pool_t* out);
+
+/* Frees the library-owned metadata.  The caller must make sure no work using the pool is
+ * still in flight.  NULL is accepted. */
+int hwkv_pool_destroy(hwkv_pool_t pool);
+
+/* Geometry of a created pool: bytes, physical block count, bytes per block. */
+int hwkv_pool_geometry(hwkv_pool_t pool, uint64_t* pool_bytes, int64_t* total_blocks, int64_t* block_bytes);
+
+/* Copies the physical block ids of (seq, layer, kv_head) -- nblk of them, logical block
+ * order -- into host_out[0 .. cap).  *n receives nblk.  Host copy of the library's table. */
+int hwkv_block_table(hwkv_pool_t pool, int seq, int layer, int kv_head, int32_t* host_out, int cap, int* n);
+
+/* Replaces the whole block table (the cache manager above the runtime chooses physical
+ * blocks).  host_table: int32 [total_blocks] in (layer, seq, kv head, logical block) order;
+ * it must be a permutation of 0 .. total_blocks-1 (checked; HWKV_ERR_INVALID_ARG otherwise).
+ * The pool bytes are NOT moved.  Copies on `stream` and synchronises it. */
+int hwkv_set_block_table(hwkv_pool_t pool, const int32_t* host_table, int64_t n, void* stream);
+
+/* Materialise ("Grouped-Cache Runtime", abstract): compacts one layer of a contiguous full
+ * prefill KV into the pool.  For every seq s and kv head h, the last min(w, L_s) positions
+ * p of the prefill are copied to ring slot p mod C (K and V rows); nothing else is written.
+ *   k_full, v_full: device, element (s, h, p, d) at s*seq_stride + h*head_stride + p*D + d
+ *                   (strides in elements; rows contiguous), 16-byte aligned, strides*eb
+ *                   multiples of 16.
+ *   max_len: rows available per (s, h) in the source; lens_dev[s] must be in [0, max_len]
+ *            (checked on the device: HWKV_DEVERR_NEG_LENGTH / HWKV_DEVERR_SRC_RANGE, the
+ *            sequence is skipped).
+ *   lens_dev: device int32 [num_seqs] prefill lengths L_s. */
+int hwkv_materialize(hwkv_pool_t pool, int layer, const void* k_full, const void* v_full,
+                     int64_t seq_stride, int64_t head_stride, int64_t max_len, const int32_t* lens_dev,
+                     void* stream);
+
+/* Append: writes the new token of every (seq, kv head) of one layer into its ring slot
+ * pos mod C (the slot of the oldest token, which has just left the window when C == w).
+ *   k_new, v_new: device [num_seqs][kv_heads][D], 16-byte aligned.
+ *   pos_dev: device int32 [num_seqs], the length BEFORE the append (position of the new
+ *            token); negative values are flagged (HWKV_DEVERR_NEG_LENGTH) and skipped. */
+int hwkv_append(hwkv_pool_t pool, int layer, const void* k_new, const void* v_new, const int32_t* pos_dev,
+                void* stream);
+
+/* Bytes of scratch hwkv_decode_attn needs for the current decode configuration (fp32
+ * split-K partials; maximum over layers). */
+int hwkv_decode_workspace_bytes(hwkv_pool_t pool, int q_heads, uint64_t* out);
+
+/* Split-K decode attention over the resident window of one layer (abstract: attention reads
+ * the materialised window, never a masked full cache).  For query head q of seq s, with
+ * h = q / G and w = w[layer][h]:
+ *     out[s][q] = sum_{p in [max(0,len_s-w), len_s)} softmax_p(scale * <q, k_p>) v_p
+ * computed with fp32 accumulation and an online softmax; out has the pool's dtype.
+ *   q, out: device [num_seqs][q_heads][D], 16-byte aligned; q_heads = G * kv_heads, G <= 8.
+ *   lens_dev: device int32 [num_seqs], lengths AFTER this step's append.  len 0 gives 0s.
+ *   workspace: device scratch of >= hwkv_decode_workspace_bytes(), 16-byte aligned; its
+ *              contents need no initialisation and are clobbered.
+ * Errors: HWKV_ERR_INVALID_ARG, HWKV_ERR_ALIGNMENT, HWKV_ERR_WORKSPACE_TOO_SMALL,
+ *         HWKV_ERR_UNSUPPORTED, HWKV_ERR_CUDA (launch failure). */
+int hwkv_decode_attn(hwkv_pool_t pool, int layer, const void* q, int q_heads, float scale,
+                     const int32_t* lens_dev, void* out, void* workspace, uint64_t workspace_bytes,
+                     void* stream);
+
+/* Decode configuration: split_tokens = tokens of one split-K chunk (0 = automatic; else a
+ * power of two in [16, 65536]); kernel = HWKV_KERNEL_*.  Changes the workspace size.
+ * Results differ between configurations only by floating-point rounding. */
+int hwkv_set_decode_config(hwkv_pool_t pool, int split_tokens, int kernel);
+
+/* Synchronises `stream`, reads and clears the device error word.  *out_bits receives the
+ * HWKV_DEVERR_* bits seen since the last call.  Returns HWKV_ERR_DEVICE_CHECK if any bit
+ * was set, HWKV_OK otherwise. */
+int hwkv_check_device_errors(hwkv_pool_t pool, void* stream, int32_t* out_bits);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* HWKV_H */

@@ -1,0 +1,145 @@
+"""Drives a workload through the CUDA path and computes the oracle's answer for the
+same seeded inputs.  Used by the GPU parity tests."""
+from __future__ import annotations
+
+import dataclasses
+from typing import Dict, Iterable, Optional
+
+import numpy as np
+import torch
+
+import oracle
+import workloads
+import head_budgeted_kv_gb300 as hw
+
+BF16_ATOL = 2e-2
+BF16_RTOL = 2e-2
+F32_ATOL = 1e-5
+
+
+def tolerance(cfg):
+    """(atol, rtol): pass iff |gpu - ref| <= atol + rtol * |ref| elementwise."""
+    return (F32_ATOL, 0.0) if cfg.dtype == "f32" else (BF16_ATOL, BF16_RTOL)
+
+
+def assert_close(got: np.ndarray, ref: np.ndarray, cfg, what: str = ""):
+    atol, rtol = tolerance(cfg)
+    bad = np.abs(got - ref) > atol + rtol * np.abs(ref)
+    if bad.any():
+        idx = np.argwhere(bad)[0]
+        raise AssertionError(f"{what}: {int(bad.sum())} of {bad.size} elements out of tolerance; first at "
+                             f"{tuple(idx)}: gpu {got[tuple(idx)]!r} oracle {ref[tuple(idx)]!r}; "
+                             f"max |err| {np.abs(got - ref).max():.3e}")
+
+
+def small_config(name="small", cfg_id=90, layers=1, kv_heads=2, group=4, head_dim=128, block_size=16,
+                 dtype="bf16", windows=((64, 200),), prefill=(300,), steps=2, spike_frac=0.0):
+    return workloads.Config(name, cfg_id, layers=layers, kv_heads=kv_heads, q_heads=kv_heads * group,
+                            head_dim=head_dim, block_size=block_size, dtype=dtype, batch=len(prefill),
+                            steps=steps, windows=tuple(tuple(int(x) for x in r) for r in windows),
+                            prefill=tuple(int(x) for x in prefill), spike_frac=spike_frac)
+
+
+class Run:
+    """One pool driven through materialise, then append + decode per step."""
+
+    def __init__(self, cfg, kernel=hw.HWKV_KERNEL_AUTO, split=0, canary: Optional[int] = None,
+                 keep_host_steps=True):
+        self.cfg = cfg
+        self.dev = torch.device("cuda", torch.cuda.current_device())
+        gen_dev = "cpu" if cfg.single_cpu_stream else self.dev
+        self.wl = workloads.Workload(cfg, device=gen_dev)
+        self.pool = hw.Pool(cfg.layers, cfg.kv_heads, cfg.head_dim, cfg.block_size, cfg.windows_array(), cfg.batch,
+                            cfg.torch_dtype, q_heads=cfg.q_heads, device=self.dev)
+        self.pool.set_decode_config(split, kernel)
+        if canary is not None:
+            self.pool.buffer.fill_(canary)
+            torch.cuda.synchronize()
+        self.prefill = torch.tensor(cfg.prefill, dtype=torch.int32, device=self.dev)
+        self.steps_done = 0
+        self.host_steps = [] if keep_host_steps else None
+        self._pre_cache: Dict = {}
+
+    # -- path --------------------------------------------------------------------------
+    def materialize(self, layers: Optional[Iterable[int]] = None):
+        for l in (range(self.cfg.layers) if layers is None else layers):
+            K, V = self.wl.prefill_layer(l, self.dev)
+            self.pool.materialize(l, K, V, self.prefill)
+            del K, V
+
+    def step(self, keep_layers: Iterable[int] = ()):
+        """One decode step over all layers; returns {layer: (q raw host, out host float64)}."""
+        i = self.steps_done
+        q, kn, vn = self.wl.step_inputs(i, self.dev)
+        if self.host_steps is not None:
+            self.host_steps.append((None, kn.cpu(), vn.cpu()))
+        pos = self.prefill + i
+        lens = pos + 1
+        keep = set(keep_layers)
+        res = {}
+        for l in range(self.cfg.layers):
+            self.pool.append(l, kn[l], vn[l], pos)
+            out = self.pool.decode(l, q[l], self.cfg.scale, lens)
+            if l in keep:
+                res[l] = (workloads.to_raw(q[l]), out.float().cpu().double().numpy())
+        self.steps_done += 1
+        return res
+
+    def device_errors(self) -> int:
+        return self.pool.check_device_errors()
+
+    # -- oracle side -------------------------------------------------------------------------
+    def _prefill_host(self, l, s):
+        key = (l, s)
+        if key not in self._pre_cache:
+            self._pre_cache = {k: v for k, v in self._pre_cache.items() if k[0] == l}
+            self._pre_cache[key] = self.wl.prefill_seq(l, s, self.dev)
+        return self._pre_cache[key]
+
+    def history(self, l, s, h, lo, hi):
+        return self.wl.history(l, s, h, lo, hi, prefill=self._prefill_host(l, s), steps=self.host_steps)
+
+    def reference(self, step: int, layer: int, q_raw: np.ndarray, seqs=None) -> np.ndarray:
+        """Oracle output [B][Hq][D] (fp64) of decode step ``step`` (0-based) of ``layer``."""
+        cfg = self.cfg
+        lens = [cfg.prefill[s] + step + 1 for s in range(cfg.batch)]
+        hist = {}
+        for s in range(cfg.batch):
+            for h in range(cfg.kv_heads):
+                lo, hi = oracle.window_span(lens[s], int(cfg.windows[layer][h]))
+                if seqs is not None and s not in seqs:
+                    lo = hi  # empty: not checked
+                hk, hv = self.history(layer, s, h, lo, hi)
+                hist[(s, h)] = (lo, hk, hv)
+        if seqs is None:
+            return oracle.attention_jobs(q_raw, hist, lens, cfg.windows[layer], cfg.scale)
+        lens_used = [lens[s] if s in seqs else 0 for s in range(cfg.batch)]
+        return oracle.attention_jobs(q_raw, hist, lens_used, cfg.windows[layer], cfg.scale)
+
+    def expected_ring_blocks(self, l, s, h):
+        """Oracle contents of the blocks of (layer, seq, head) after the steps so far."""
+        cfg = self.cfg
+        L = cfg.prefill[s]
+        w = int(cfg.windows[l][h])
+        C = int(oracle.ring_capacity([[w]], cfg.block_size)[0, 0])
+        writes = list(oracle.materialized_positions(L, w)) + list(oracle.appended_positions(L, self.steps_done))
+        lo = writes[0] if writes else 0
+        hk, hv = self.history(l, s, h, lo, L + self.steps_done)
+        rk, rv = oracle.ring_after_writes(hk, hv, lo, writes, C)
+        return oracle.ring_to_blocks(rk, rv, cfg.block_size), writes, C
+
+    def gpu_blocks(self, ids) -> np.ndarray:
+        blocks = self.pool.blocks()
+        idx = torch.as_tensor(np.asarray(ids, dtype=np.int64), device=self.dev)
+        return workloads.to_raw(blocks.index_select(0, idx))
+
+    def close(self):
+        self.pool.close()
+
+
+def oracle_table(cfg):
+    return oracle.block_tables(cfg.windows_array(), cfg.batch, cfg.block_size)
+
+
+def config_with(cfg, **kw):
+    return dataclasses.replace(cfg, **kw)

@@ -1,0 +1,264 @@
+"""GPU parity of the CUDA path against the CPU oracle, through the C ABI.
+
+Copies and tables are compared bit for bit; attention within |gpu - ref| <= 1e-5 (fp32
+inputs) or <= 2e-2 + 2e-2 |ref| (bf16 inputs, fp32 accumulation)."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import workloads
+import head_budgeted_kv_gb300 as hw
+from harness import Run, assert_close, oracle_table, small_config
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(autouse=True, scope="module")
+def _cuda():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    hw.binding.load()
+    yield
+    torch.cuda.synchronize()
+
+
+def _check_all_pool_blocks(run: Run):
+    cfg = run.cfg
+    tables = oracle_table(cfg)
+    for (l, s, h), ids in tables.items():
+        assert run.pool.block_table(s, l, h).tolist() == ids
+        exp, _, _ = run.expected_ring_blocks(l, s, h)
+        got = run.gpu_blocks(ids)
+        assert np.array_equal(got, exp), f"pool bytes of layer {l} seq {s} head {h}"
+
+
+# ---------------------------------------------------------------------------------------
+# the tiny fp32 workload: everything, every step
+# ---------------------------------------------------------------------------------------
+def test_tiny_fp32_every_step_every_head():
+    cfg = workloads.config("tiny")
+    run = Run(cfg)
+    exp_bytes = oracle.pool_bytes(cfg.windows_array(), cfg.batch, cfg.head_dim, cfg.block_size, cfg.elem_bytes)
+    assert run.pool.nbytes == exp_bytes == 81920
+    assert run.pool.geometry()[0] == exp_bytes
+    run.materialize()
+    _check_all_pool_blocks(run)
+    for i in range(cfg.steps):
+        res = run.step(keep_layers=[0])
+        q_raw, got = res[0]
+        ref = run.reference(i, 0, q_raw)
+        assert_close(got, ref, cfg, f"tiny step {i}")
+        _check_all_pool_blocks(run)
+    assert run.device_errors() == 0
+    run.close()
+
+
+# ---------------------------------------------------------------------------------------
+# the single-layer bf16 workload: whole pool bit-exact, every head's output
+# ---------------------------------------------------------------------------------------
+@pytest.mark.parametrize("kernel", [hw.HWKV_KERNEL_TENSOR, hw.HWKV_KERNEL_SIMT])
+def test_layer_bf16_full(kernel):
+    cfg = workloads.config("layer")
+    run = Run(cfg, kernel=kernel)
+    run.materialize()
+    res = run.step(keep_layers=[0])
+    q_raw, got = res[0]
+    ref = run.reference(0, 0, q_raw)
+    assert_close(got, ref, cfg, "layer bf16")
+    if kernel == hw.HWKV_KERNEL_TENSOR:
+        _check_all_pool_blocks(run)
+    assert run.device_errors() == 0
+    run.close()
+
+
+# ---------------------------------------------------------------------------------------
+# edge cases
+# ---------------------------------------------------------------------------------------
+EDGE = {
+    # windows larger than the context (clip to len), ragged lengths
+    "clip": dict(kv_heads=3, windows=((1024, 16, 4096),), prefill=(5, 40, 300, 17)),
+    # window not a multiple of the block size: ring of 48 slots holds a 40-token window
+    "ring_c_gt_w": dict(kv_heads=2, windows=((40, 24),), prefill=(300, 47), steps=5),
+    # windows of one token
+    "w1": dict(kv_heads=2, windows=((1, 1),), prefill=(50, 3)),
+    # GQA 1, 2, 8 and head_dim 64
+    "g1_d64": dict(kv_heads=4, group=1, head_dim=64, windows=((64, 128, 32, 512),), prefill=(700, 90)),
+    "g2": dict(kv_heads=2, group=2, windows=((256, 96),), prefill=(1000, 1000)),
+    "g8": dict(kv_heads=2, group=8, windows=((2048, 160),), prefill=(3000, 100)),
+    # bigger block size, several layers
+    "bs64_layers": dict(layers=3, kv_heads=2, block_size=64, windows=((128, 1024), (64, 256), (4096, 64)),
+                        prefill=(5000, 700, 64)),
+    # odd block size -> CUDA-core kernel
+    "bs5": dict(kv_heads=2, block_size=5, windows=((23, 60),), prefill=(100, 9)),
+    # fp32 with several layers and GQA 4
+    "f32": dict(layers=2, kv_heads=2, dtype="f32", head_dim=128, windows=((100, 37), (16, 300)), prefill=(400, 20)),
+    # spiky keys (x8) as in the ragged workload
+    "spikes": dict(kv_heads=2, windows=((1024, 512),), prefill=(2000, 1500), spike_frac=0.05),
+}
+
+
+@pytest.mark.parametrize("name", sorted(EDGE))
+@pytest.mark.parametrize("kernel", [hw.HWKV_KERNEL_AUTO, hw.HWKV_KERNEL_SIMT])
+def test_edge_cases(name, kernel):
+    spec = dict(EDGE[name])
+    steps = spec.pop("steps", 3)
+    cfg = small_config(name=name, steps=steps, **spec)
+    run = Run(cfg, kernel=kernel)
+    run.materialize()
+    for i in range(steps):
+        res = run.step(keep_layers=range(cfg.layers))
+        for l, (q_raw, got) in res.items():
+            ref = run.reference(i, l, q_raw)
+            assert_close(got, ref, cfg, f"{name} step {i} layer {l}")
+    _check_all_pool_blocks(run)
+    assert run.device_errors() == 0
+    run.close()
+
+
+def test_window_one_returns_the_new_value_exactly():
+    cfg = small_config(name="w1x", kv_heads=2, windows=((1, 1),), prefill=(50, 3))
+    run = Run(cfg)
+    run.materialize()
+    _, kn, vn = run.wl.step_inputs(0, run.dev)
+    res = run.step(keep_layers=[0])
+    _, got = res[0]
+    v = vn[0].float().cpu().double().numpy()          # [B][H][D]
+    exp = np.repeat(v, cfg.group, axis=1)             # query head q reads kv head q // G
+    assert np.array_equal(got, exp)
+    run.close()
+
+
+def test_empty_context_gives_zero_output():
+    cfg = small_config(name="empty", kv_heads=2, windows=((64, 32),), prefill=(0, 0))
+    run = Run(cfg)
+    run.materialize()
+    q = torch.randn(2, cfg.q_heads, cfg.head_dim, device=run.dev).to(torch.bfloat16)
+    lens = torch.zeros(2, dtype=torch.int32, device=run.dev)
+    out = torch.full_like(q, 7.0)
+    run.pool.decode(0, q, cfg.scale, lens, out=out)
+    torch.cuda.synchronize()
+    assert not out.float().abs().sum().item()
+    assert run.device_errors() == 0
+    run.close()
+
+
+@pytest.mark.parametrize("split", [16, 64, 256, 4096])
+@pytest.mark.parametrize("kernel", [hw.HWKV_KERNEL_TENSOR, hw.HWKV_KERNEL_SIMT])
+def test_split_size_changes_rounding_only(split, kernel):
+    cfg = small_config(name="split", kv_heads=4, windows=((4096, 1024, 256, 2000),), prefill=(5000, 1500, 300))
+    run = Run(cfg, kernel=kernel, split=split)
+    run.materialize()
+    res = run.step(keep_layers=[0])
+    q_raw, got = res[0]
+    assert_close(got, run.reference(0, 0, q_raw), cfg, f"split {split}")
+    assert run.device_errors() == 0
+    run.close()
+
+
+def test_block_permutation_leaves_output_bit_identical():
+    cfg = small_config(name="perm", layers=2, kv_heads=2, windows=((64, 512), (256, 32)), prefill=(600, 250))
+    base = Run(cfg)
+    base.materialize()
+    out_a = base.step(keep_layers=[0, 1])
+    # same inputs, then permute physical blocks: move the bytes and the table together
+    perm_run = Run(cfg)
+    perm_run.materialize()
+    _, total, _ = perm_run.pool.geometry()
+    rng = np.random.default_rng(0)
+    perm = rng.permutation(total).astype(np.int32)         # logical entry i -> new physical id perm[i]
+    blocks = perm_run.pool.blocks()
+    moved = torch.empty_like(blocks)
+    moved[torch.as_tensor(perm, device=perm_run.dev).long()] = blocks
+    blocks.copy_(moved)
+    perm_run.pool.set_block_table(perm)                    # identity table -> permuted ids
+    out_b = perm_run.step(keep_layers=[0, 1])
+    for l in (0, 1):
+        assert np.array_equal(out_a[l][1], out_b[l][1])
+    # the pool still decodes to the oracle's rings through the permuted table
+    for (l, s, h), ids in oracle_table(cfg).items():
+        exp, _, _ = perm_run.expected_ring_blocks(l, s, h)
+        got = perm_run.gpu_blocks(perm[np.asarray(ids)])
+        assert np.array_equal(got, exp)
+    base.close()
+    perm_run.close()
+
+
+def test_canary_outside_written_slots_is_untouched():
+    cfg = small_config(name="canary", kv_heads=2, windows=((40, 100),), prefill=(300, 30), steps=4)
+    run = Run(cfg, canary=0xA5)
+    run.materialize()
+    for _ in range(cfg.steps):
+        run.step()
+    canary = np.uint16(0xA5A5)
+    for (l, s, h), ids in oracle_table(cfg).items():
+        exp, writes, C = run.expected_ring_blocks(l, s, h)
+        got = run.gpu_blocks(ids)
+        written = {p % C for p in writes}
+        for t in range(C):
+            j, r = divmod(t, cfg.block_size)
+            if t in written:
+                assert np.array_equal(got[j, :, r], exp[j, :, r])
+            else:
+                assert (got[j, :, r] == canary).all(), (l, s, h, t)
+    run.close()
+
+
+def test_pool_bytes_equal_allocation():
+    cfg = small_config(name="alloc", layers=2, kv_heads=3, windows=((1024, 4096, 16), (64, 65536, 1)), prefill=(10,))
+    before = torch.cuda.memory_allocated()
+    pool = hw.Pool(cfg.layers, cfg.kv_heads, cfg.head_dim, cfg.block_size, cfg.windows_array(), cfg.batch,
+                   torch.bfloat16, q_heads=cfg.q_heads)
+    pred = oracle.pool_bytes(cfg.windows_array(), cfg.batch, cfg.head_dim, cfg.block_size, 2)
+    assert pool.nbytes == pred
+    assert pool.buffer.numel() == pred
+    ws = pool.workspace.numel()
+    assert torch.cuda.memory_allocated() - before == pred + ws or torch.cuda.memory_allocated() - before >= pred
+    pool.close()
+
+
+# ---------------------------------------------------------------------------------------
+# failures are reported, never faulted
+# ---------------------------------------------------------------------------------------
+def test_negative_position_and_oversized_prefill_are_flagged():
+    cfg = small_config(name="flags", kv_heads=2, windows=((64, 32),), prefill=(100,))
+    run = Run(cfg)
+    K = torch.zeros(1, 2, 100, cfg.head_dim, dtype=torch.bfloat16, device=run.dev)
+    bad_len = torch.tensor([101], dtype=torch.int32, device=run.dev)   # above max_len = 100
+    run.pool.materialize(0, K, K, bad_len)
+    assert run.device_errors() & hw.binding.HWKV_DEVERR_SRC_RANGE
+    kn = torch.zeros(1, 2, cfg.head_dim, dtype=torch.bfloat16, device=run.dev)
+    run.pool.append(0, kn, kn, torch.tensor([-3], dtype=torch.int32, device=run.dev))
+    assert run.device_errors() & hw.binding.HWKV_DEVERR_NEG_LENGTH
+    assert run.device_errors() == 0   # cleared by the previous read
+    assert not run.pool.buffer.any().item()  # nothing was written
+    run.close()
+
+
+def test_host_side_argument_errors():
+    cfg = small_config(name="args", kv_heads=2, windows=((4096, 64),), prefill=(100,))
+    run = Run(cfg)
+    q = torch.zeros(1, cfg.q_heads, cfg.head_dim, dtype=torch.bfloat16, device=run.dev)
+    lens = torch.ones(1, dtype=torch.int32, device=run.dev)
+    out = torch.empty_like(q)
+    small_ws = torch.empty(16, dtype=torch.uint8, device=run.dev)
+    with pytest.raises(hw.HwkvError) as e:
+        hw.hwkv_decode_attn(run.pool.handle, 0, q, cfg.scale, lens, out, small_ws)
+    assert e.value.status == hw.binding.HWKV_ERR_WORKSPACE_TOO_SMALL
+    with pytest.raises(hw.HwkvError) as e:
+        hw.hwkv_decode_attn(run.pool.handle, 1, q, cfg.scale, lens, out, run.pool.workspace)
+    assert e.value.status == hw.binding.HWKV_ERR_INVALID_ARG
+    big = torch.zeros(2 * q.numel() + 8, dtype=torch.bfloat16, device=run.dev)
+    qmis = big[1:1 + q.numel()].view_as(q)                     # 2-byte offset
+    with pytest.raises(hw.HwkvError) as e:
+        hw.hwkv_decode_attn(run.pool.handle, 0, qmis, cfg.scale, lens, out, run.pool.workspace)
+    assert e.value.status == hw.binding.HWKV_ERR_ALIGNMENT
+    with pytest.raises(hw.HwkvError) as e:
+        hw.hwkv_set_block_table(run.pool.handle, np.zeros(run.pool.geometry()[1], np.int32))
+    assert e.value.status == hw.binding.HWKV_ERR_INVALID_ARG
+    buf = torch.empty(run.pool.nbytes - 256, dtype=torch.uint8, device=run.dev)
+    with pytest.raises(hw.HwkvError) as e:
+        hw.hwkv_pool_create(1, 2, cfg.head_dim, 16, cfg.windows_array(), 1, torch.bfloat16, buf)
+    assert e.value.status == hw.binding.HWKV_ERR_POOL_TOO_SMALL
+    assert run.device_errors() == 0
+    run.close()
