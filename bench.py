@@ -1,0 +1,469 @@
+"""Decode benchmark of the per-head windowed KV path on GB300.
+
+One step = one decode step of the whole hot path over every global layer: append the new
+token's K/V into each head's ring, then split-K windowed attention (plus its combine) for
+every query head.  Inputs are synthetic (seeded N(0,1), shapes of the chosen workload)
+and already resident in HBM when the timed region starts; the prefill is materialised
+into the pool before timing (its bandwidth is reported separately).
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload full] [--impl hwkv|reference]
+
+Prints one JSON line on rank 0.  Under torchrun (N > 1) every rank runs an independent
+replica of the workload on its own GPU (the path has no exchange step); value is the
+tokens of all ranks over the slowest rank's time.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "decode tokens/s and resident-KV HBM GB/s (fraction of GB300 peak), 1 GPU"
+FALLBACK_HBM_GBS = 6800.0
+
+# dram__bytes_read.sum + dram__bytes_write.sum per decode launch from one ncu capture of
+# the tensor-core decode kernel, with the sha256 of hwkv_decode.cu it was taken on.  When
+# the kernel source changes the figure no longer applies and is reported as null.
+DECODE_TRAFFIC = {"source_sha256": None, "bytes_per_launch": None, "launch": None}
+
+
+def log(*a):
+    print(*a, file=sys.stderr, flush=True)
+
+
+# --------------------------------------------------------------------------------------
+# distributed helpers (replicas only)
+# --------------------------------------------------------------------------------------
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def aggregate(local_ms: float, local_units: float, world_size: int):
+    """(max time over ranks in ms, total units over ranks); needs an initialised process
+    group when world_size > 1."""
+    if world_size == 1:
+        return local_ms, local_units
+    import torch
+    import torch.distributed as dist
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([local_ms], dtype=torch.float64, device=dev)
+    u = torch.tensor([local_units], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    dist.all_reduce(u, op=dist.ReduceOp.SUM)
+    return float(t.item()), float(u.item())
+
+
+def barrier(world_size: int):
+    if world_size > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+# --------------------------------------------------------------------------------------
+# clocks during the timed region
+# --------------------------------------------------------------------------------------
+class ClockSampler:
+    FIELDS = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.lines = []
+        self.t0 = self.t1 = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+            time.sleep(0.5)
+        except (OSError, ValueError):
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append((time.time(), line.strip()))
+
+    def mark_start(self):
+        self.t0 = time.time()
+
+    def mark_end(self):
+        self.t1 = time.time()
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        sm, mx, reasons, power = [], [], set(), []
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        picked = [l for (t, l) in self.lines if self.t0 is not None and self.t0 - 0.15 <= t <= self.t1 + 0.15]
+        if not picked:
+            picked = [l for (_, l) in self.lines]
+        for line in picked:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 10:
+                continue
+            try:
+                sm.append(float(parts[2]))
+                mx.append(float(parts[3]))
+                power.append(float(parts[4]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[6:10]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        return {"sm_mhz": float(np.median(sm)) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": sorted(reasons), "samples": len(sm),
+                "power_w_median": float(np.median(power)) if power else None}
+
+
+def measured_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def decode_source_sha() -> str:
+    with open(os.path.join(ROOT, "head_budgeted_kv_gb300", "csrc", "hwkv_decode.cu"), "rb") as f:
+        return hashlib.sha256(f.read()).hexdigest()
+
+
+# --------------------------------------------------------------------------------------
+# algorithmic bytes
+# --------------------------------------------------------------------------------------
+def attention_bytes(cfg, layer: int, lens) -> int:
+    """Resident K and V bytes one decode launch of ``layer`` must read (each once), plus
+    q read and out written: sum_s sum_h min(w, len_s) * 2 * D * eb + 2 * B * Hq * D * eb."""
+    w = np.asarray(cfg.windows[layer], dtype=np.int64)
+    lens = np.asarray(lens, dtype=np.int64)
+    kv = int(np.minimum(w[None, :], lens[:, None]).sum()) * 2 * cfg.head_dim * cfg.elem_bytes
+    return kv + 2 * cfg.batch * cfg.q_heads * cfg.head_dim * cfg.elem_bytes
+
+
+def append_bytes(cfg) -> int:
+    """Read k_new, v_new and write them into the pool: 2 * (B * H * 2 * D * eb)."""
+    return 2 * cfg.batch * cfg.kv_heads * 2 * cfg.head_dim * cfg.elem_bytes
+
+
+def materialize_bytes(cfg, layer: int) -> int:
+    w = np.asarray(cfg.windows[layer], dtype=np.int64)
+    L = np.asarray(cfg.prefill, dtype=np.int64)
+    return 2 * int(np.minimum(w[None, :], L[:, None]).sum()) * 2 * cfg.head_dim * cfg.elem_bytes
+
+
+def workload_desc(cfg) -> str:
+    lens = sorted(set(cfg.prefill))
+    ctx = f"ctx {lens[0]}" if len(lens) == 1 else f"ctx {min(lens)}..{max(lens)}"
+    return (f"{cfg.name}: {cfg.layers} global layers x {cfg.kv_heads} KV heads, {cfg.q_heads} q heads, "
+            f"D{cfg.head_dim}, {cfg.dtype}, block {cfg.block_size}, batch {cfg.batch}, {ctx}, per-head windows "
+            f"{sorted(set(int(x) for r in cfg.windows for x in r))}")
+
+
+# --------------------------------------------------------------------------------------
+# CPU baseline: the oracle on a bounded sample of one decode step
+# --------------------------------------------------------------------------------------
+def oracle_sample(cfg, wl, budget_s: float, device, layers_order=None, step: int = 0, max_layers=None):
+    """Times the oracle on whole layers of decode step ``step`` until ``budget_s`` seconds
+    of oracle time are spent.  Returns (seconds, layers done, threads)."""
+    import oracle
+    import workloads
+    threads = oracle.default_threads()
+    st_in = wl.step_inputs(step, "cpu") if step == 0 else None
+    steps = [(None, st_in[1], st_in[2])] if st_in is not None else None
+    spent, done = 0.0, 0
+    order = layers_order or list(range(cfg.layers))
+    for l in order:
+        if max_layers is not None and done >= max_layers:
+            break
+        hist = {}
+        for s in range(cfg.batch):
+            k, v = wl.prefill_seq(l, s, device)
+            L = cfg.prefill[s]
+            for h in range(cfg.kv_heads):
+                lo, hi = oracle.window_span(L + step + 1, int(cfg.windows[l][h]))
+                hk, hv = wl.history(l, s, h, lo, hi, prefill=(k, v), steps=steps)
+                hist[(s, h)] = (lo, hk, hv)
+            del k, v
+        q = workloads.to_raw(st_in[0][l])
+        lens = [cfg.prefill[s] + step + 1 for s in range(cfg.batch)]
+        t0 = time.perf_counter()
+        oracle.attention_jobs(q, hist, lens, cfg.windows[l], cfg.scale, threads=threads)
+        spent += time.perf_counter() - t0
+        done += 1
+        if spent >= budget_s:
+            break
+    return spent, done, threads
+
+
+# --------------------------------------------------------------------------------------
+# reference arm: the oracle timed on the host cores
+# --------------------------------------------------------------------------------------
+def run_reference(args, cfg):
+    ws, rank, local = dist_env()
+    if rank != 0:
+        return
+    import torch
+    import workloads
+    device = torch.device("cuda", local) if torch.cuda.is_available() else torch.device("cpu")
+    wl = workloads.Workload(cfg, device="cpu" if cfg.single_cpu_stream or device.type == "cpu" else device)
+    times, per_layer = [], []
+    total_steps = args.warmup + args.steps
+    threads = None
+    for i in range(total_steps):
+        l = i % cfg.layers
+        t, done, threads = oracle_sample(cfg, wl, budget_s=0.0, device=device, layers_order=[l], max_layers=1)
+        if i >= args.warmup:
+            times.append(t)
+            per_layer.append(l)
+    mean_layer_s = float(np.mean(times))
+    step_s = mean_layer_s * cfg.layers
+    value = cfg.batch / step_s
+    sample = (f"one whole layer (all {cfg.batch} seqs x {cfg.q_heads} q heads, full resident windows) of decode "
+              f"step 0 per timed step, layers cycled; per-step time = mean layer time x {cfg.layers} layers")
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": ws,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": step_s * 1e3, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": workload_desc(cfg), "global_batch": cfg.batch, "seq_len": max(cfg.prefill),
+                   "parallelism": "replicas"},
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": threads, "kind": "oracle", "sample": sample},
+        "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+# --------------------------------------------------------------------------------------
+# the CUDA path
+# --------------------------------------------------------------------------------------
+def run_hwkv(args, cfg):
+    import torch
+    import workloads
+    import head_budgeted_kv_gb300 as hw
+
+    ws, rank, local = dist_env()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if ws > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+    hw.binding.load()
+    stream = torch.cuda.current_stream(dev)
+
+    total = args.warmup + args.steps
+    wl = workloads.Workload(cfg, device="cpu" if cfg.single_cpu_stream else dev)
+    pool = hw.Pool(cfg.layers, cfg.kv_heads, cfg.head_dim, cfg.block_size, cfg.windows_array(), cfg.batch,
+                   cfg.torch_dtype, q_heads=cfg.q_heads, device=dev)
+    if args.split or args.kernel:
+        pool.set_decode_config(args.split, args.kernel)
+
+    # ---- materialise every layer from a contiguous full prefill (timed per launch) ----
+    prefill = torch.tensor(cfg.prefill, dtype=torch.int32, device=dev)
+    mat_ms, mat_bytes = 0.0, 0
+    for l in range(cfg.layers):
+        K, V = wl.prefill_layer(l, dev)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        pool.materialize(l, K, V, prefill)
+        e1.record(stream)
+        e1.synchronize()
+        mat_ms += e0.elapsed_time(e1)
+        mat_bytes += materialize_bytes(cfg, l)
+        del K, V
+    torch.cuda.synchronize()
+
+    # ---- per-step inputs, drawn up front (resident before timing) ----
+    qs, kns, vns = [], [], []
+    for i in range(total + args.steps):  # the e2e pass continues after the device-timed pass
+        q, kn, vn = wl.step_inputs(i, dev)
+        qs.append(q)
+        kns.append(kn)
+        vns.append(vn)
+    outs = torch.empty((cfg.layers, cfg.batch, cfg.q_heads, cfg.head_dim), dtype=cfg.torch_dtype, device=dev)
+    pos_all = [(prefill + i).contiguous() for i in range(total + args.steps)]
+    lens_all = [(prefill + i + 1).contiguous() for i in range(total + args.steps)]
+    torch.cuda.synchronize()
+
+    def run_step(i, ev=None):
+        for l in range(cfg.layers):
+            pool.append(l, kns[i][l], vns[i][l], pos_all[i])
+            if ev is not None:
+                ev[l][0].record(stream)
+            pool.decode(l, qs[i][l], cfg.scale, lens_all[i], out=outs[l])
+            if ev is not None:
+                ev[l][1].record(stream)
+
+    for i in range(args.warmup):
+        run_step(i)
+    torch.cuda.synchronize()
+    bits = pool.check_device_errors()
+    if bits:
+        raise RuntimeError(f"device error bits {bits:#x} during warm-up")
+
+    clocks = ClockSampler(local)
+    if rank == 0:
+        clocks.start()
+    step_events = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                    for _ in range(cfg.layers)] for _ in range(args.steps)]
+    t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    launches0 = hw.binding.hwkv_kernel_launches()
+    barrier(ws)
+    torch.cuda.synchronize()
+    clocks.mark_start()
+    t_start.record(stream)
+    for k in range(args.steps):
+        run_step(args.warmup + k, step_events[k])
+    t_end.record(stream)
+    torch.cuda.synchronize()
+    clocks.mark_end()
+    barrier(ws)
+    launches = hw.binding.hwkv_kernel_launches() - launches0
+    clock_info = clocks.stop() if rank == 0 else None
+    local_ms = t_start.elapsed_time(t_end)
+    bits = pool.check_device_errors()
+    if bits:
+        raise RuntimeError(f"device error bits {bits:#x} in the timed region")
+
+    # dominant kernel: decode attention (+ its split-K combine), per launch
+    dec_ms, dec_bytes = 0.0, 0
+    for k in range(args.steps):
+        i = args.warmup + k
+        lens = [cfg.prefill[s] + i + 1 for s in range(cfg.batch)]
+        for l in range(cfg.layers):
+            dec_ms += step_events[k][l][0].elapsed_time(step_events[k][l][1])
+            dec_bytes += attention_bytes(cfg, l, lens)
+    n_dec = args.steps * cfg.layers
+    step_bytes = dec_bytes / args.steps + cfg.layers * append_bytes(cfg)
+
+    # ---- e2e: host (pinned) inputs in, host outputs back, every step ----
+    e2e_total = args.steps
+    h_q = [qs[total + k].cpu().pin_memory() for k in range(e2e_total)]
+    h_k = [kns[total + k].cpu().pin_memory() for k in range(e2e_total)]
+    h_v = [vns[total + k].cpu().pin_memory() for k in range(e2e_total)]
+    h_pos = [pos_all[total + k].cpu().pin_memory() for k in range(e2e_total)]
+    h_out = torch.empty(outs.shape, dtype=outs.dtype).pin_memory()
+    d_q, d_k, d_v = torch.empty_like(qs[0]), torch.empty_like(kns[0]), torch.empty_like(vns[0])
+    d_pos = torch.empty_like(prefill)
+    d_lens = torch.empty_like(prefill)
+    h2d = (h_q[0].numel() * h_q[0].element_size() + h_k[0].numel() * h_k[0].element_size() * 2
+           + h_pos[0].numel() * 4)
+    d2h = h_out.numel() * h_out.element_size()
+    torch.cuda.synchronize()
+    barrier(ws)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for k in range(e2e_total):
+        d_q.copy_(h_q[k], non_blocking=True)
+        d_k.copy_(h_k[k], non_blocking=True)
+        d_v.copy_(h_v[k], non_blocking=True)
+        d_pos.copy_(h_pos[k], non_blocking=True)
+        torch.add(d_pos, 1, out=d_lens)
+        for l in range(cfg.layers):
+            pool.append(l, d_k[l], d_v[l], d_pos)
+            pool.decode(l, d_q[l], cfg.scale, d_lens, out=outs[l])
+        h_out.copy_(outs, non_blocking=True)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    barrier(ws)
+    e2e_ms = e0.elapsed_time(e1)
+    bits = pool.check_device_errors()
+    if bits:
+        raise RuntimeError(f"device error bits {bits:#x} in the e2e pass")
+
+    max_ms, units = aggregate(local_ms, cfg.batch * args.steps, ws)
+    e2e_max_ms, e2e_units = aggregate(e2e_ms, cfg.batch * e2e_total, ws)
+
+    cpu = None
+    if rank == 0 and ws == 1 and not args.no_cpu_baseline:
+        spent, done, threads = oracle_sample(cfg, wl, budget_s=args.cpu_budget, device=dev)
+        step_s = spent / done * cfg.layers
+        cpu = {"value": cfg.batch / step_s, "unit": "tokens/s", "cores": threads, "kind": "oracle",
+               "sample": f"{done} of {cfg.layers} layers (all seqs and q heads) of decode step 0, "
+                         f"{spent:.1f} s of fp64 oracle time; per-step time scaled by {cfg.layers}/{done}"}
+
+    if rank != 0:
+        pool.close()
+        return
+    peak, peak_kind = measured_peak()
+    achieved = dec_bytes / (dec_ms / 1e3) / 1e9
+    sha = decode_source_sha()
+    traffic = DECODE_TRAFFIC["bytes_per_launch"] if DECODE_TRAFFIC["source_sha256"] == sha else None
+    value = units / (max_ms / 1e3)
+    line = {
+        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": ws, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": max_ms / args.steps, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": cfg.dtype, "data": "synthetic",
+        "config": {"workload": workload_desc(cfg), "global_batch": cfg.batch * ws,
+                   "seq_len": max(cfg.prefill), "parallelism": "replicas" if ws > 1 else "single",
+                   "l2": f"inputs larger than L2: {step_bytes / 1e9:.2f} GB of resident KV read per step",
+                   "split_tokens": args.split or "auto", "kernel": ["auto", "tensor", "simt"][args.kernel]},
+        "resident_kv_gbs": step_bytes / (max_ms / args.steps / 1e3) / 1e9,
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
+                     "traffic": traffic, "peak_kind": peak_kind,
+                     "kernel": "decode attention (tensor-core split-K + combine), per layer launch",
+                     "bytes_per_launch": dec_bytes / n_dec, "ms_per_launch": dec_ms / n_dec},
+        "cpu_baseline": cpu,
+        "e2e": {"value": e2e_units / (e2e_max_ms / 1e3), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h},
+        "gpu_launches": launches,
+        "clocks": clock_info,
+        "materialize": {"gbs": mat_bytes / (mat_ms / 1e3) / 1e9, "ms": mat_ms, "bytes": mat_bytes,
+                        "frac": mat_bytes / (mat_ms / 1e3) / 1e9 / peak},
+        "pool_bytes": pool.nbytes,
+    }
+    pool.close()
+    print(json.dumps(line), flush=True)
+
+
+def main(argv=None):
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=125)
+    p.add_argument("--warmup", type=int, default=3)
+    p.add_argument("--impl", choices=["hwkv", "reference"], default="hwkv")
+    p.add_argument("--workload", default="full")
+    p.add_argument("--layers", type=int, default=0, help="keep only the first N layers (profiling)")
+    p.add_argument("--split", type=int, default=0)
+    p.add_argument("--kernel", type=int, default=0)
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--cpu-budget", type=float, default=12.0)
+    args = p.parse_args(argv)
+    if args.warmup < 3:
+        raise SystemExit("--warmup must be >= 3")
+    import workloads
+    cfg = workloads.config(args.workload)
+    if args.layers:
+        cfg = cfg.with_layers(args.layers)
+    if args.impl == "reference":
+        run_reference(args, cfg)
+    else:
+        run_hwkv(args, cfg)
+
+
+if __name__ == "__main__":
+    main()

@@ -53,6 +53,7 @@ SIGNATURES = [
     ("hwkv_decode_workspace_bytes", _i, [_vp, _i, _c_u64p]),
     ("hwkv_decode_attn", _i, [_vp, _i, _vp, _i, ctypes.c_float, _vp, _vp, _vp, _u64, _vp]),
     ("hwkv_set_decode_config", _i, [_vp, _i, _i]),
+    ("hwkv_kernel_launches", _i, [_c_u64p]),
     ("hwkv_check_device_errors", _i, [_vp, _vp, _c_i32p]),
 ]
 
@@ -218,6 +219,12 @@ def hwkv_decode_attn(pool: int, layer: int, q: torch.Tensor, scale: float, lens:
 
 def hwkv_set_decode_config(pool: int, split_tokens: int = 0, kernel: int = HWKV_KERNEL_AUTO):
     _check(load().hwkv_set_decode_config(pool, split_tokens, kernel))
+
+
+def hwkv_kernel_launches() -> int:
+    out = ctypes.c_uint64(0)
+    _check(load().hwkv_kernel_launches(ctypes.byref(out)))
+    return out.value
 
 
 def hwkv_check_device_errors(pool: int, stream=None) -> int:

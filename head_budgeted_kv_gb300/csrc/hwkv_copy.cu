@@ -130,6 +130,7 @@ cudaError_t launch_append(const CopyArgs& a, int dtype, cudaStream_t st) {
   const int warps = a.pv.num_seqs * a.pv.kv_heads;
   const int blocks = (warps + 3) / 4;
   append_kernel<<<blocks, 128, 0, st>>>(a, row_bytes);
+  count_launches(1);
   return cudaGetLastError();
 }
 
@@ -142,6 +143,7 @@ cudaError_t launch_materialize(const CopyArgs& a, int dtype, int max_rows, cudaS
     case 32: materialize_kernel<32><<<grid, kMatThreads, 0, st>>>(a); break;
     default: return cudaErrorInvalidValue;
   }
+  count_launches(1);
   return cudaGetLastError();
 }
 

@@ -593,6 +593,7 @@ cudaError_t configure_tc() {
 template <int D, int W, int NS>
 cudaError_t launch_tc(const DecodeArgs& a, const CUtensorMap* tmap, int items, cudaStream_t st) {
   decode_tc_kernel<D, W, NS><<<items, W * 32, tc_smem_bytes<D, W, NS>(), st>>>(*tmap, a);
+  count_launches(1);
   return cudaGetLastError();
 }
 
@@ -623,6 +624,7 @@ cudaError_t launch_decode_simt(const DecodeArgs& a, int dtype, int items, cudaSt
   else if (dtype == HWKV_BF16 && D == 64) decode_simt_kernel<__nv_bfloat16, 64><<<items, kSimtWarps * 32, 0, st>>>(a);
   else if (dtype == HWKV_BF16 && D == 128) decode_simt_kernel<__nv_bfloat16, 128><<<items, kSimtWarps * 32, 0, st>>>(a);
   else return cudaErrorInvalidValue;
+  count_launches(1);
   return cudaGetLastError();
 }
 
@@ -634,6 +636,7 @@ cudaError_t launch_combine(const DecodeArgs& a, int dtype, cudaStream_t st) {
   else if (dtype == HWKV_BF16 && D == 64) combine_kernel<__nv_bfloat16, 64><<<blocks, 256, 0, st>>>(a);
   else if (dtype == HWKV_BF16 && D == 128) combine_kernel<__nv_bfloat16, 128><<<blocks, 256, 0, st>>>(a);
   else return cudaErrorInvalidValue;
+  count_launches(1);
   return cudaGetLastError();
 }
 

@@ -8,6 +8,7 @@
 #include <cudaTypedefs.h>
 
 #include <algorithm>
+#include <atomic>
 #include <cstdarg>
 #include <cstdio>
 #include <cstring>
@@ -24,6 +25,7 @@ using namespace hwkv;
 namespace {
 
 thread_local std::string g_last_error;
+std::atomic<uint64_t> g_launches{0};
 
 int fail(int code, const char* fmt, ...) {
   char buf[512];
@@ -125,6 +127,8 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
 bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
 
 }  // namespace
+
+void hwkv::count_launches(uint64_t n) { g_launches.fetch_add(n, std::memory_order_relaxed); }
 
 struct hwkv_pool {
   Geometry g;
@@ -391,10 +395,11 @@ int hwkv_materialize(hwkv_pool_t p, int layer, const void* k_full, const void* v
   if (!p) return fail(HWKV_ERR_INVALID_ARG, "pool is NULL");
   const Geometry& g = p->g;
   if (layer < 0 || layer >= g.layers) return fail(HWKV_ERR_INVALID_ARG, "layer %d out of range", layer);
+  if (seq_stride < 0 || head_stride < 0 || max_len < 0) return fail(HWKV_ERR_INVALID_ARG, "negative stride or max_len");
+  if (max_len == 0) return ok();  // an empty prefill: nothing is read or written
   if (!k_full || !v_full || !lens_dev) return fail(HWKV_ERR_INVALID_ARG, "NULL tensor argument");
   if (!aligned(k_full, 16) || !aligned(v_full, 16) || !aligned(lens_dev, 4))
     return fail(HWKV_ERR_ALIGNMENT, "k_full / v_full must be 16-byte aligned, lens 4-byte aligned");
-  if (seq_stride < 0 || head_stride < 0 || max_len < 0) return fail(HWKV_ERR_INVALID_ARG, "negative stride or max_len");
   if ((seq_stride * g.eb) % 16 != 0 || (head_stride * g.eb) % 16 != 0)
     return fail(HWKV_ERR_ALIGNMENT, "seq_stride and head_stride must be multiples of 16 bytes");
   if (max_len > kInt32Max) return fail(HWKV_ERR_INVALID_ARG, "max_len must be below 2^31");
@@ -511,6 +516,12 @@ int hwkv_set_decode_config(hwkv_pool_t p, int split_tokens, int kernel) {
   p->split_override = split_tokens;
   p->kernel_choice = kernel;
   plan_decode(p);
+  return ok();
+}
+
+int hwkv_kernel_launches(uint64_t* out) {
+  if (!out) return fail(HWKV_ERR_INVALID_ARG, "out is NULL");
+  *out = g_launches.load(std::memory_order_relaxed);
   return ok();
 }
 

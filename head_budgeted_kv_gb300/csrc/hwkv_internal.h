@@ -59,6 +59,9 @@ struct DecodeArgs {
   int32_t chunk_prefix[kMaxKvHeads + 1];  // prefix sums over heads of ceil(C_h / split)
 };
 
+// Counts every kernel launch the library makes (read by hwkv_kernel_launches).
+void count_launches(uint64_t n);
+
 // Launchers (hwkv_copy.cu, hwkv_decode.cu).  dtype: 0 = f32, 1 = bf16.
 cudaError_t launch_append(const CopyArgs& a, int dtype, cudaStream_t st);
 // max_rows: the most positions any (seq, head) of the layer copies, min(max window, max_len)

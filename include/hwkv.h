@@ -131,7 +131,8 @@ int hwkv_set_block_table(hwkv_pool_t pool, const int32_t* host_table, int64_t n,
  *   max_len: rows available per (s, h) in the source; lens_dev[s] must be in [0, max_len]
  *            (checked on the device: HWKV_DEVERR_NEG_LENGTH / HWKV_DEVERR_SRC_RANGE, the
  *            sequence is skipped).
- *   lens_dev: device int32 [num_seqs] prefill lengths L_s. */
+ *   lens_dev: device int32 [num_seqs] prefill lengths L_s.
+ * max_len == 0 is an empty prefill: nothing is read or written and the pointers may be NULL. */
 int hwkv_materialize(hwkv_pool_t pool, int layer, const void* k_full, const void* v_full,
                      int64_t seq_stride, int64_t head_stride, int64_t max_len, const int32_t* lens_dev,
                      void* stream);
@@ -167,6 +168,10 @@ int hwkv_decode_attn(hwkv_pool_t pool, int layer, const void* q, int q_heads, fl
  * power of two in [16, 65536]); kernel = HWKV_KERNEL_*.  Changes the workspace size.
  * Results differ between configurations only by floating-point rounding. */
 int hwkv_set_decode_config(hwkv_pool_t pool, int split_tokens, int kernel);
+
+/* Number of kernels this library has launched in this process (all pools, all devices).
+ * Lets a caller count the launches inside a timed region. */
+int hwkv_kernel_launches(uint64_t* out);
 
 /* Synchronises `stream`, reads and clears the device error word.  *out_bits receives the
  * HWKV_DEVERR_* bits seen since the last call.  Returns HWKV_ERR_DEVICE_CHECK if any bit
