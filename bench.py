@@ -1,8 +1,9 @@
 """Decode benchmark of the per-head windowed KV path on GB300.
 
 One step = one decode step of the whole hot path over every global layer: append the new
-token's K/V into each head's ring, then split-K windowed attention (plus its combine) for
-every query head.  Inputs are synthetic (seeded N(0,1), shapes of the chosen workload)
+token's K/V into each head's ring, then split-K windowed attention for every query head
+(by default through hwkv_append_decode_attn, one launch per layer; ``--path split`` calls
+hwkv_append and hwkv_decode_attn separately).  Inputs are synthetic (seeded N(0,1), shapes of the chosen workload)
 and already resident in HBM when the timed region starts; the prefill is materialised
 into the pool before timing (its bandwidth is reported separately).
 
@@ -33,7 +34,7 @@ METRIC = "decode tokens/s and resident-KV HBM GB/s (fraction of GB300 peak), 1 G
 FALLBACK_HBM_GBS = 6800.0
 
 # dram__bytes_read.sum + dram__bytes_write.sum per decode launch from one ncu capture of
-# the tensor-core decode kernel, with the sha256 of hwkv_decode.cu it was taken on.  When
+# the tensor-core decode kernel, with the sha256 of hwkv_decode_tc.cu it was taken on.  When
 # the kernel source changes the figure no longer applies and is reported as null.
 DECODE_TRAFFIC = {"source_sha256": None, "bytes_per_launch": None, "launch": None}
 
@@ -150,7 +151,7 @@ def measured_peak():
 
 
 def decode_source_sha() -> str:
-    with open(os.path.join(ROOT, "head_budgeted_kv_gb300", "csrc", "hwkv_decode.cu"), "rb") as f:
+    with open(os.path.join(ROOT, "head_budgeted_kv_gb300", "csrc", "hwkv_decode_tc.cu"), "rb") as f:
         return hashlib.sha256(f.read()).hexdigest()
 
 
@@ -279,8 +280,9 @@ def run_hwkv(args, cfg):
     wl = workloads.Workload(cfg, device="cpu" if cfg.single_cpu_stream else dev)
     pool = hw.Pool(cfg.layers, cfg.kv_heads, cfg.head_dim, cfg.block_size, cfg.windows_array(), cfg.batch,
                    cfg.torch_dtype, q_heads=cfg.q_heads, device=dev)
-    if args.split or args.kernel:
-        pool.set_decode_config(args.split, args.kernel)
+    if args.split or args.kernel or args.workers:
+        pool.set_decode_config(args.split, args.kernel, args.workers)
+    fused = args.path == "fused"
 
     # ---- materialise every layer from a contiguous full prefill (timed per launch) ----
     prefill = torch.tensor(cfg.prefill, dtype=torch.int32, device=dev)
@@ -298,23 +300,30 @@ def run_hwkv(args, cfg):
     torch.cuda.synchronize()
 
     # ---- per-step inputs, drawn up front (resident before timing) ----
+    # steps: warm-up, timed pass, kernel-timing pass, e2e pass (positions keep advancing)
+    n_steps = total + 2 * args.steps
     qs, kns, vns = [], [], []
-    for i in range(total + args.steps):  # the e2e pass continues after the device-timed pass
+    for i in range(n_steps):
         q, kn, vn = wl.step_inputs(i, dev)
         qs.append(q)
         kns.append(kn)
         vns.append(vn)
     outs = torch.empty((cfg.layers, cfg.batch, cfg.q_heads, cfg.head_dim), dtype=cfg.torch_dtype, device=dev)
-    pos_all = [(prefill + i).contiguous() for i in range(total + args.steps)]
-    lens_all = [(prefill + i + 1).contiguous() for i in range(total + args.steps)]
+    pos_all = [(prefill + i).contiguous() for i in range(n_steps)]
+    lens_all = [(prefill + i + 1).contiguous() for i in range(n_steps)]
     torch.cuda.synchronize()
 
     def run_step(i, ev=None):
         for l in range(cfg.layers):
-            pool.append(l, kns[i][l], vns[i][l], pos_all[i])
-            if ev is not None:
-                ev[l][0].record(stream)
-            pool.decode(l, qs[i][l], cfg.scale, lens_all[i], out=outs[l])
+            if fused:
+                if ev is not None:
+                    ev[l][0].record(stream)
+                pool.append_decode(l, qs[i][l], cfg.scale, kns[i][l], vns[i][l], pos_all[i], out=outs[l])
+            else:
+                pool.append(l, kns[i][l], vns[i][l], pos_all[i])
+                if ev is not None:
+                    ev[l][0].record(stream)
+                pool.decode(l, qs[i][l], cfg.scale, lens_all[i], out=outs[l])
             if ev is not None:
                 ev[l][1].record(stream)
 
@@ -328,8 +337,6 @@ def run_hwkv(args, cfg):
     clocks = ClockSampler(local)
     if rank == 0:
         clocks.start()
-    step_events = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-                    for _ in range(cfg.layers)] for _ in range(args.steps)]
     t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     launches0 = hw.binding.hwkv_kernel_launches()
     barrier(ws)
@@ -337,7 +344,7 @@ def run_hwkv(args, cfg):
     clocks.mark_start()
     t_start.record(stream)
     for k in range(args.steps):
-        run_step(args.warmup + k, step_events[k])
+        run_step(args.warmup + k)
     t_end.record(stream)
     torch.cuda.synchronize()
     clocks.mark_end()
@@ -349,23 +356,37 @@ def run_hwkv(args, cfg):
     if bits:
         raise RuntimeError(f"device error bits {bits:#x} in the timed region")
 
-    # dominant kernel: decode attention (+ its split-K combine), per launch
+    # algorithmic bytes of the timed steps (resident K/V + q + out, plus the appends)
+    step_bytes = 0
+    for k in range(args.steps):
+        lens = [cfg.prefill[s] + args.warmup + k + 1 for s in range(cfg.batch)]
+        step_bytes += sum(attention_bytes(cfg, l, lens) for l in range(cfg.layers))
+    step_bytes = step_bytes / args.steps + cfg.layers * append_bytes(cfg)
+
+    # ---- dominant kernel, per launch: the same steps again with events around each launch
+    # of the decode kernel (fused: the whole per-layer step; split: decode only) ----
+    step_events = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                    for _ in range(cfg.layers)] for _ in range(args.steps)]
+    torch.cuda.synchronize()
+    for k in range(args.steps):
+        run_step(total + k, step_events[k])
+    torch.cuda.synchronize()
     dec_ms, dec_bytes = 0.0, 0
     for k in range(args.steps):
-        i = args.warmup + k
+        i = total + k
         lens = [cfg.prefill[s] + i + 1 for s in range(cfg.batch)]
         for l in range(cfg.layers):
             dec_ms += step_events[k][l][0].elapsed_time(step_events[k][l][1])
-            dec_bytes += attention_bytes(cfg, l, lens)
+            dec_bytes += attention_bytes(cfg, l, lens) + (append_bytes(cfg) if fused else 0)
     n_dec = args.steps * cfg.layers
-    step_bytes = dec_bytes / args.steps + cfg.layers * append_bytes(cfg)
 
     # ---- e2e: host (pinned) inputs in, host outputs back, every step ----
     e2e_total = args.steps
-    h_q = [qs[total + k].cpu().pin_memory() for k in range(e2e_total)]
-    h_k = [kns[total + k].cpu().pin_memory() for k in range(e2e_total)]
-    h_v = [vns[total + k].cpu().pin_memory() for k in range(e2e_total)]
-    h_pos = [pos_all[total + k].cpu().pin_memory() for k in range(e2e_total)]
+    e2e0 = total + args.steps
+    h_q = [qs[e2e0 + k].cpu().pin_memory() for k in range(e2e_total)]
+    h_k = [kns[e2e0 + k].cpu().pin_memory() for k in range(e2e_total)]
+    h_v = [vns[e2e0 + k].cpu().pin_memory() for k in range(e2e_total)]
+    h_pos = [pos_all[e2e0 + k].cpu().pin_memory() for k in range(e2e_total)]
     h_out = torch.empty(outs.shape, dtype=outs.dtype).pin_memory()
     d_q, d_k, d_v = torch.empty_like(qs[0]), torch.empty_like(kns[0]), torch.empty_like(vns[0])
     d_pos = torch.empty_like(prefill)
@@ -382,10 +403,14 @@ def run_hwkv(args, cfg):
         d_k.copy_(h_k[k], non_blocking=True)
         d_v.copy_(h_v[k], non_blocking=True)
         d_pos.copy_(h_pos[k], non_blocking=True)
-        torch.add(d_pos, 1, out=d_lens)
-        for l in range(cfg.layers):
-            pool.append(l, d_k[l], d_v[l], d_pos)
-            pool.decode(l, d_q[l], cfg.scale, d_lens, out=outs[l])
+        if fused:
+            for l in range(cfg.layers):
+                pool.append_decode(l, d_q[l], cfg.scale, d_k[l], d_v[l], d_pos, out=outs[l])
+        else:
+            torch.add(d_pos, 1, out=d_lens)
+            for l in range(cfg.layers):
+                pool.append(l, d_k[l], d_v[l], d_pos)
+                pool.decode(l, d_q[l], cfg.scale, d_lens, out=outs[l])
         h_out.copy_(outs, non_blocking=True)
     e1.record(stream)
     torch.cuda.synchronize()
@@ -421,11 +446,13 @@ def run_hwkv(args, cfg):
         "config": {"workload": workload_desc(cfg), "global_batch": cfg.batch * ws,
                    "seq_len": max(cfg.prefill), "parallelism": "replicas" if ws > 1 else "single",
                    "l2": f"inputs larger than L2: {step_bytes / 1e9:.2f} GB of resident KV read per step",
-                   "split_tokens": args.split or "auto", "kernel": ["auto", "tensor", "simt"][args.kernel]},
+                   "path": args.path, "kernel": ["auto", "tensor", "simt"][args.kernel],
+                   "workers": args.workers or "auto", "split_tokens": args.split or "auto"},
         "resident_kv_gbs": step_bytes / (max_ms / args.steps / 1e3) / 1e9,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
                      "traffic": traffic, "peak_kind": peak_kind,
-                     "kernel": "decode attention (tensor-core split-K + combine), per layer launch",
+                     "kernel": ("fused append + split-K decode attention" if fused else "split-K decode attention")
+                               + " (one launch per layer; events in a separate pass of the same steps)",
                      "bytes_per_launch": dec_bytes / n_dec, "ms_per_launch": dec_ms / n_dec},
         "cpu_baseline": cpu,
         "e2e": {"value": e2e_units / (e2e_max_ms / 1e3), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
@@ -448,7 +475,9 @@ def main(argv=None):
     p.add_argument("--impl", choices=["hwkv", "reference"], default="hwkv")
     p.add_argument("--workload", default="full")
     p.add_argument("--layers", type=int, default=0, help="keep only the first N layers (profiling)")
-    p.add_argument("--split", type=int, default=0)
+    p.add_argument("--split", type=int, default=0, help="CUDA-core kernel: tokens per split-K chunk")
+    p.add_argument("--workers", type=int, default=0, help="tensor-core kernel: CTAs of the persistent grid")
+    p.add_argument("--path", choices=["fused", "split"], default="fused")
     p.add_argument("--kernel", type=int, default=0)
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--cpu-budget", type=float, default=12.0)

@@ -17,14 +17,16 @@ import torch
 
 from . import binding
 from .binding import (HWKV_BF16, HWKV_F32, HWKV_KERNEL_AUTO, HWKV_KERNEL_SIMT, HWKV_KERNEL_TENSOR, HwkvError,
-                      hwkv_abi_version, hwkv_append, hwkv_block_table, hwkv_check_device_errors,
+                      hwkv_abi_version, hwkv_append, hwkv_append_decode_attn, hwkv_block_table,
+                      hwkv_check_device_errors, hwkv_kernel_launches,
                       hwkv_decode_attn, hwkv_decode_workspace_bytes, hwkv_materialize, hwkv_pool_bytes,
                       hwkv_pool_create, hwkv_pool_destroy, hwkv_pool_geometry, hwkv_set_block_table,
                       hwkv_set_decode_config)
 
 __all__ = [
     "Pool", "HwkvError", "binding", "HWKV_F32", "HWKV_BF16", "HWKV_KERNEL_AUTO", "HWKV_KERNEL_TENSOR",
-    "HWKV_KERNEL_SIMT", "hwkv_abi_version", "hwkv_append", "hwkv_block_table", "hwkv_check_device_errors",
+    "HWKV_KERNEL_SIMT", "hwkv_abi_version", "hwkv_append", "hwkv_append_decode_attn", "hwkv_block_table",
+    "hwkv_check_device_errors", "hwkv_kernel_launches",
     "hwkv_decode_attn", "hwkv_decode_workspace_bytes", "hwkv_materialize", "hwkv_pool_bytes", "hwkv_pool_create",
     "hwkv_pool_destroy", "hwkv_pool_geometry", "hwkv_set_block_table", "hwkv_set_decode_config",
 ]
@@ -55,8 +57,8 @@ class Pool:
         if self.workspace is None or self.workspace.numel() < need:
             self.workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=self.buffer.device)
 
-    def set_decode_config(self, split_tokens: int = 0, kernel: int = HWKV_KERNEL_AUTO):
-        hwkv_set_decode_config(self.handle, split_tokens, kernel)
+    def set_decode_config(self, split_tokens: int = 0, kernel: int = HWKV_KERNEL_AUTO, workers: int = 0):
+        hwkv_set_decode_config(self.handle, split_tokens, workers, kernel)
         self._size_workspace()
 
     def geometry(self):
@@ -86,6 +88,16 @@ class Pool:
             self.q_heads = q.shape[1]
             self._size_workspace()
         hwkv_decode_attn(self.handle, layer, q, scale, lens, out, self.workspace, stream)
+        return out
+
+    def append_decode(self, layer: int, q, scale: float, k_new, v_new, pos, out=None, stream=None):
+        """Append the new token (positions ``pos``) and decode at ``pos + 1`` in one call."""
+        if out is None:
+            out = torch.empty_like(q)
+        if q.shape[1] != self.q_heads:
+            self.q_heads = q.shape[1]
+            self._size_workspace()
+        hwkv_append_decode_attn(self.handle, layer, q, scale, k_new, v_new, pos, out, self.workspace, stream)
         return out
 
     def check_device_errors(self, stream=None) -> int:

@@ -52,7 +52,8 @@ SIGNATURES = [
     ("hwkv_append", _i, [_vp, _i, _vp, _vp, _vp, _vp]),
     ("hwkv_decode_workspace_bytes", _i, [_vp, _i, _c_u64p]),
     ("hwkv_decode_attn", _i, [_vp, _i, _vp, _i, ctypes.c_float, _vp, _vp, _vp, _u64, _vp]),
-    ("hwkv_set_decode_config", _i, [_vp, _i, _i]),
+    ("hwkv_append_decode_attn", _i, [_vp, _i, _vp, _i, ctypes.c_float, _vp, _vp, _vp, _vp, _vp, _u64, _vp]),
+    ("hwkv_set_decode_config", _i, [_vp, _i, _i, _i]),
     ("hwkv_kernel_launches", _i, [_c_u64p]),
     ("hwkv_check_device_errors", _i, [_vp, _vp, _c_i32p]),
 ]
@@ -217,8 +218,19 @@ def hwkv_decode_attn(pool: int, layer: int, q: torch.Tensor, scale: float, lens:
                                    _ptr(workspace), ws_bytes, _stream_ptr(stream)))
 
 
-def hwkv_set_decode_config(pool: int, split_tokens: int = 0, kernel: int = HWKV_KERNEL_AUTO):
-    _check(load().hwkv_set_decode_config(pool, split_tokens, kernel))
+def hwkv_append_decode_attn(pool: int, layer: int, q: torch.Tensor, scale: float, k_new: torch.Tensor,
+                            v_new: torch.Tensor, pos: torch.Tensor, out: torch.Tensor,
+                            workspace: Optional[torch.Tensor], stream=None):
+    """Append (k_new, v_new at positions pos) then decode at pos + 1, in one call."""
+    if not (q.is_contiguous() and out.is_contiguous() and k_new.is_contiguous() and v_new.is_contiguous()):
+        raise ValueError("q, out, k_new and v_new must be contiguous")
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check(load().hwkv_append_decode_attn(pool, layer, _ptr(q), q.shape[1], float(scale), _ptr(k_new), _ptr(v_new),
+                                          _ptr(pos), _ptr(out), _ptr(workspace), ws_bytes, _stream_ptr(stream)))
+
+
+def hwkv_set_decode_config(pool: int, split_tokens: int = 0, workers: int = 0, kernel: int = HWKV_KERNEL_AUTO):
+    _check(load().hwkv_set_decode_config(pool, split_tokens, workers, kernel))
 
 
 def hwkv_kernel_launches() -> int:

@@ -1,0 +1,506 @@
+// Tensor-core split-K decode attention over per-head paged rings (bf16, block_size % 16 == 0,
+// head_dim 64 or 128), optionally fused with the append of the step's new token.
+//
+// "HeadWiseKV: Budgeted Per-Head Cache Residency for Hybrid Long-Context Language Models",
+// abstract and section "Grouped-Cache Runtime": attention reads only the materialised window
+// of each KV head (the last min(w, len) tokens), through the head's block table.
+//
+// Work decomposition ("stream-K"): every (seq, kv head) group contributes the 16-token ring
+// tiles that hold resident tokens -- a cyclic run of tiles starting at the tile of the oldest
+// resident slot.  Numbering those tiles group after group gives one line of T equal-cost
+// tiles; the persistent grid of N CTAs splits it into N equal contiguous ranges, so every
+// CTA streams the same number of bytes whatever the windows and lengths are.  A CTA walks its
+// range group by group ("segments"); its 4 warps take the segment's tiles round-robin, each
+// through its own TMA + mbarrier pipeline that runs on across segment boundaries.  At the end
+// of a segment the warps' online-softmax states are merged in shared memory; a group held by
+// one CTA is written out directly, otherwise the CTA stores a partial (m, l, acc) and bumps
+// the group's arrival counter, and the CTA that arrives last merges all partials of the group
+// and writes the output (no CTA ever waits for another).
+//
+// Per tile (16 tokens), per warp, with the GQA group (G <= 8 query heads, zero-padded to 8)
+// on the N side of mma.sync.m16n8k16 bf16 -> fp32:
+//   S[16 tok][8 q] = K_tile . Q^T over head_dim (K tile loaded with ldmatrix from the
+//   128-byte-swizzled TMA tile), masked to resident slots, online softmax in fp32 in the log2
+//   domain; P is moved from the accumulator layout to the operand layout with movmatrix.trans;
+//   O^T[D][8 q] = alpha * O^T + V_tile^T . P (V tile loaded with ldmatrix.trans).
+//
+// Waits are bounded (~2 s); a timeout records HWKV_DEVERR_WAIT_TIMEOUT and the warp stops.
+#include "hwkv_device.cuh"
+
+namespace hwkv {
+namespace {
+
+constexpr int kWarps = 4;
+
+// One (seq, kv head) group at this step: its resident window and needed tiles.
+struct Group {
+  int s, h;
+  int len;         // length after the append
+  Resident rs;     // resident slots
+  int C16;         // ring capacity in tiles
+  int t_first;     // tile of the oldest resident slot
+  int tiles;       // needed tiles, cyclically from t_first
+  const int32_t* tbl;
+};
+
+__device__ __forceinline__ Group load_group(const DecodeArgs& a, int g) {
+  Group gr;
+  const int H = a.pv.kv_heads;
+  gr.s = g / H;
+  gr.h = g - gr.s * H;
+  int len = a.lens[gr.s] + a.len_add;
+  gr.len = len < 0 ? 0 : len;
+  const int C = (a.g.nblk_prefix[gr.h + 1] - a.g.nblk_prefix[gr.h]) * a.pv.block_size;
+  gr.rs = resident(gr.len, a.g.window[gr.h], C);
+  gr.C16 = C >> 4;
+  gr.t_first = gr.rs.first_slot >> 4;
+  if (gr.rs.n > 0) {
+    const uint32_t last = (uint32_t)gr.rs.first_slot + (uint32_t)gr.rs.n - 1u;
+    gr.tiles = min(gr.C16, (int)(last >> 4) - gr.t_first + 1);
+  } else {
+    gr.tiles = 0;
+  }
+  gr.tbl = a.pv.tbl + a.g.tbl_base + (int64_t)gr.s * a.g.tbl_seq_stride + a.g.nblk_prefix[gr.h];
+  return gr;
+}
+
+// ring slot of the first token of the i-th needed tile of a group
+__device__ __forceinline__ int tile_slot(const Group& gr, long long i) {
+  int t = gr.t_first + (int)i;
+  if (t >= gr.C16) t -= gr.C16;
+  return t << 4;
+}
+
+// first tile of CTA c when T tiles are split over n CTAs
+__device__ __forceinline__ long long range_start(long long T, int c, int n) { return T * c / n; }
+
+// CTA whose range holds tile t
+__device__ __forceinline__ int cta_of(long long t, long long T, int n) { return (int)(((t + 1) * n - 1) / T); }
+
+// Byte offset of element (row, d) of a 16-row tile stored as D/64 TMA boxes of [16 rows][64
+// elements] with the 128-byte swizzle: box hf = d / 64 at hf * 2048; inside a box row r is
+// the 128-byte line r and its 16-byte chunk c sits at chunk c ^ (r % 8).
+__device__ __forceinline__ uint32_t swz(int row, int d) {
+  return (uint32_t)((d >> 6) * 2048 + row * 128 + ((((d & 63) >> 3) ^ (row & 7)) << 4) + (d & 7) * 2);
+}
+
+template <int W>
+__device__ __forceinline__ long long block_exclusive_scan(long long v, long long* s_warp, long long& total) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  long long x = v;
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+    const long long y = __shfl_up_sync(0xffffffffu, x, off);
+    if (lane >= off) x += y;
+  }
+  if (lane == 31) s_warp[warp] = x;
+  __syncthreads();
+  long long base = 0, tot = 0;
+#pragma unroll
+  for (int w = 0; w < W; ++w) {
+    const long long sw = s_warp[w];
+    if (w < warp) base += sw;
+    tot += sw;
+  }
+  total = tot;
+  __syncthreads();
+  return base + x - v;
+}
+
+template <int D, int GP, int NS>
+__global__ void __launch_bounds__(kWarps * 32) decode_sk_kernel(const __grid_constant__ CUtensorMap tmap,
+                                                                const __grid_constant__ DecodeArgs a) {
+  constexpr int W = kWarps;
+  constexpr int kHalves = D / 64;
+  constexpr int kTileBytes = kTile * D * 2;    // 16 rows of bf16
+  constexpr int kStageBytes = 2 * kTileBytes;  // K tile + V tile
+  constexpr int kSteps = D / 16;               // k-steps of QK, m-tiles of PV
+  constexpr int kRowVecs = D * 2 / 16;         // 16-byte vectors per row
+
+  extern __shared__ uint8_t smem_dyn[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_dyn) + 1023) & ~uintptr_t(1023));
+  float* sc_acc = reinterpret_cast<float*>(smem + W * NS * kStageBytes);  // [W][GP][D]
+  __shared__ __align__(8) uint64_t bars[W * NS];
+  __shared__ float sc_m[W * GP], sc_l[W * GP];
+  __shared__ long long s_scan[W];
+  __shared__ long long s_start[2];
+  __shared__ int s_last;
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int H = a.pv.kv_heads;
+  const int B = a.pv.num_seqs;
+  const int ngroups = B * H;
+  const int nctas = gridDim.x, cta = blockIdx.x;
+  const int G = a.group;
+  const int Hq = H * G;
+  const int bs = a.pv.block_size;
+  __nv_bfloat16* const out = static_cast<__nv_bfloat16*>(a.out);
+
+  if (cta == 0) {
+    for (int s = threadIdx.x; s < B; s += W * 32)
+      if (a.lens[s] + a.len_add < 0) atomicOr(a.pv.err, HWKV_DEVERR_NEG_LENGTH);
+  }
+
+  // ---- schedule: needed tiles per group, their prefix sums, this CTA's range ----------
+  if (threadIdx.x == 0) s_start[0] = -1;
+  const int per = (ngroups + W * 32 - 1) / (W * 32);
+  const int g_lo = min(ngroups, (int)threadIdx.x * per), g_hi = min(ngroups, g_lo + per);
+  long long mine = 0;
+  for (int g = g_lo; g < g_hi; ++g) mine += load_group(a, g).tiles;
+  long long T;
+  const long long excl = block_exclusive_scan<W>(mine, s_scan, T);
+  const long long t_lo = range_start(T, cta, nctas), t_hi = range_start(T, cta + 1, nctas);
+  if (t_lo < t_hi && excl <= t_lo && t_lo < excl + mine) {
+    long long pre = excl;
+    for (int g = g_lo; g < g_hi; ++g) {
+      const int c = load_group(a, g).tiles;
+      if (t_lo < pre + c) {
+        s_start[0] = g;
+        s_start[1] = pre;
+        break;
+      }
+      pre += c;
+    }
+  }
+  // groups with nothing resident (length 0) get a zero output, each from one CTA
+  for (int g = cta; g < ngroups; g += nctas) {
+    const Group gr = load_group(a, g);
+    if (gr.tiles == 0)
+      for (int e = threadIdx.x; e < G * D; e += W * 32)
+        out[((int64_t)gr.s * Hq + gr.h * G + e / D) * D + e % D] = __float2bfloat16_rn(0.f);
+  }
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < W * NS; ++i) mbar_init(&bars[i], 1);
+    fence_mbar_init();
+  }
+  __syncthreads();
+  if (t_lo >= t_hi || s_start[0] < 0) return;
+  const int g_start = (int)s_start[0];
+  const long long pre_start = s_start[1];
+
+  // ---- per-warp TMA pipeline ---------------------------------------------------------
+  uint64_t* wbar = bars + warp * NS;
+  const uint32_t wstage = smem_addr(smem + warp * NS * kStageBytes);
+  const uint64_t policy = evict_first_policy();
+
+  int ig = g_start;            // issue cursor: group, its first tile on the line, the group
+  long long ipre = pre_start;
+  Group igr = load_group(a, ig);
+  long long j_issue = t_lo + warp;
+  int issued = 0;
+  auto issue_next = [&]() {
+    while (j_issue >= ipre + igr.tiles) {
+      ipre += igr.tiles;
+      igr = load_group(a, ++ig);
+    }
+    if (lane == 0) {
+      const int st = issued % NS;
+      const int t0 = tile_slot(igr, j_issue - ipre);
+      const int jb = t0 / bs;
+      const int r0 = t0 - jb * bs;
+      int32_t blk = igr.tbl[jb];
+      if (blk < 0 || (int64_t)blk >= a.pv.total_blocks) {
+        atomicOr(a.pv.err, HWKV_DEVERR_BAD_BLOCK);
+        blk = 0;  // keep the barrier accounting intact; the result is flagged
+      }
+      const int row_k = blk * 2 * bs + r0;
+      const int row_v = row_k + bs;
+      const uint32_t dst = wstage + st * kStageBytes;
+      mbar_arrive_expect_tx(&wbar[st], kStageBytes);
+#pragma unroll
+      for (int hf = 0; hf < kHalves; ++hf) {
+        tma_load_2d(dst + hf * 2048, &tmap, hf * 64, row_k, &wbar[st], policy);
+        tma_load_2d(dst + kTileBytes + hf * 2048, &tmap, hf * 64, row_v, &wbar[st], policy);
+      }
+    }
+    j_issue += W;
+    ++issued;
+  };
+  for (int i = 0; i < NS && j_issue < t_hi; ++i) issue_next();
+
+  // ldmatrix lane roles: matrix mi = lane/8, row rr = lane%8
+  const int mi = lane >> 3, rr = lane & 7;
+  const int a_row = rr + ((mi & 1) << 3);   // K tile (non-transposed A operand): token row
+  const int a_dof = (mi >> 1) << 3;         //                                    +8 dims
+  const int v_row = rr + ((mi >> 1) << 3);  // V tile (transposed A operand): token row
+  const int v_dof = (mi & 1) << 3;          //                                +8 dims
+  const int gq = lane >> 2, q4 = lane & 3;  // accumulator roles: token/dim row, column pair
+  const float sl2 = a.scale_log2;
+
+  int sg = g_start;            // segment cursor (uniform in the CTA)
+  long long spre = pre_start;
+  Group sgr = load_group(a, sg);
+  long long j_cons = t_lo + warp;
+  int consumed = 0;
+  int drain_from = -1;         // set when a wait timed out
+  bool patched_stage = false;  // a generic-proxy write went into the stage just released
+
+  for (;;) {
+    const long long seg_begin = t_lo > spre ? t_lo : spre;
+    const long long seg_end = t_hi < spre + sgr.tiles ? t_hi : spre + sgr.tiles;
+
+    // Q of this group as the B operand of S = K . Q^T: lane holds q[g][16i + 2*q4 + {0,1}]
+    // and the same +8, g = lane/4; rows g >= G are zero.
+    uint32_t qf[kSteps][2];
+    {
+      const __nv_bfloat16* qrow =
+          static_cast<const __nv_bfloat16*>(a.q) + ((int64_t)sgr.s * Hq + sgr.h * G + gq) * D;
+#pragma unroll
+      for (int i = 0; i < kSteps; ++i) {
+        qf[i][0] = gq < G ? *reinterpret_cast<const uint32_t*>(qrow + 16 * i + 2 * q4) : 0u;
+        qf[i][1] = gq < G ? *reinterpret_cast<const uint32_t*>(qrow + 16 * i + 2 * q4 + 8) : 0u;
+      }
+    }
+    float acc[kSteps][4];
+#pragma unroll
+    for (int j = 0; j < kSteps; ++j) acc[j][0] = acc[j][1] = acc[j][2] = acc[j][3] = 0.f;
+    float m0 = kNegInf, m1 = kNegInf, l0 = 0.f, l1 = 0.f;  // columns g = 2*q4, 2*q4 + 1
+    const int new_slot = (a.k_new != nullptr) ? (sgr.len - 1) % sgr.rs.C : -1;
+
+    while (j_cons < seg_end) {
+      const int st = consumed % NS;
+      if (drain_from < 0 && !mbar_wait_bounded(&wbar[st], (uint32_t)(consumed / NS) & 1u)) {
+        drain_from = consumed;
+        if (lane == 0) atomicOr(a.pv.err, HWKV_DEVERR_WAIT_TIMEOUT);
+      }
+      if (drain_from < 0) {
+        const uint32_t sK = wstage + st * kStageBytes;
+        const uint32_t sV = sK + kTileBytes;
+        const int t0 = tile_slot(sgr, j_cons - spre);
+
+        // fused append: the new token's rows replace the tile's copy of its slot and go to
+        // the pool (no other CTA reads this tile in this launch)
+        if (new_slot >= t0 && new_slot < t0 + kTile) {
+          const int r = new_slot - t0;
+          const int jb = new_slot / bs;
+          const int32_t blk = sgr.tbl[jb];
+          const bool blk_ok = blk >= 0 && (int64_t)blk < a.pv.total_blocks;
+          const int64_t src = ((int64_t)sgr.s * H + sgr.h) * D * 2;
+          char* dstk = static_cast<char*>(a.pv.pool) +
+                       ((int64_t)(blk_ok ? blk : 0) * 2 * bs + (new_slot - jb * bs)) * D * 2;
+          for (int i = lane; i < 2 * kRowVecs; i += 32) {
+            const int kv = i / kRowVecs, c = i - kv * kRowVecs;
+            const uint4 val = *reinterpret_cast<const uint4*>(
+                static_cast<const char*>(kv ? a.v_new : a.k_new) + src + c * 16);
+            const uint32_t sa = (kv ? sV : sK) + swz(r, c * 8);
+            asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(sa), "r"(val.x), "r"(val.y), "r"(val.z),
+                         "r"(val.w)
+                         : "memory");
+            if (blk_ok) *reinterpret_cast<uint4*>(dstk + (int64_t)kv * bs * D * 2 + c * 16) = val;
+          }
+          __syncwarp();
+          patched_stage = true;
+        }
+
+        // S[16 tok][8 q] = K_tile . Q^T (two accumulation chains)
+        float sa[4] = {0.f, 0.f, 0.f, 0.f}, sb[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int i = 0; i < kSteps; ++i) {
+          uint32_t af[4];
+          ldsm_x4(af, sK + swz(a_row, 16 * i + a_dof));
+          if (i & 1) mma_bf16(sb, af, qf[i][0], qf[i][1]);
+          else mma_bf16(sa, af, qf[i][0], qf[i][1]);
+        }
+        const bool v0 = slot_valid(sgr.rs, t0 + gq), v1 = slot_valid(sgr.rs, t0 + gq + 8);
+        const float s0 = v0 ? sa[0] + sb[0] : kNegInf;
+        const float s1 = v0 ? sa[1] + sb[1] : kNegInf;
+        const float s2 = v1 ? sa[2] + sb[2] : kNegInf;
+        const float s3 = v1 ? sa[3] + sb[3] : kNegInf;
+        float mx0 = fmaxf(s0, s2), mx1 = fmaxf(s1, s3);
+#pragma unroll
+        for (int off = 4; off < 32; off <<= 1) {
+          mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, off));
+          mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, off));
+        }
+        const float n0 = fmaxf(m0, mx0 * sl2), n1 = fmaxf(m1, mx1 * sl2);
+        const float b0 = n0 == kNegInf ? 0.f : n0, b1 = n1 == kNegInf ? 0.f : n1;
+        const float al0 = ex2(m0 - b0), al1 = ex2(m1 - b1);
+        const float p0 = ex2(fmaf(s0, sl2, -b0)), p1 = ex2(fmaf(s1, sl2, -b1));
+        const float p2 = ex2(fmaf(s2, sl2, -b0)), p3 = ex2(fmaf(s3, sl2, -b1));
+        l0 = fmaf(l0, al0, p0 + p2);
+        l1 = fmaf(l1, al1, p1 + p3);
+        m0 = n0;
+        m1 = n1;
+        const uint32_t pb0 = movmatrix_trans(pack_bf16(p0, p1));
+        const uint32_t pb1 = movmatrix_trans(pack_bf16(p2, p3));
+
+        // O^T[D][8 q] = alpha * O^T + V_tile^T . P
+#pragma unroll
+        for (int j = 0; j < kSteps; ++j) {
+          acc[j][0] *= al0;
+          acc[j][1] *= al1;
+          acc[j][2] *= al0;
+          acc[j][3] *= al1;
+          uint32_t af[4];
+          ldsm_x4_trans(af, sV + swz(v_row, 16 * j + v_dof));
+          mma_bf16(acc[j], af, pb0, pb1);
+        }
+      }
+      __syncwarp();
+      ++consumed;
+      if (drain_from < 0 && j_issue < t_hi) {
+        if (patched_stage) {  // every lane orders its shared-memory writes before the next TMA
+          fence_proxy_async_smem();
+          __syncwarp();
+        }
+        issue_next();
+      }
+      patched_stage = false;
+      j_cons += W;
+    }
+
+    // ---- end of segment: merge the warps, then store output or partial -----------------
+#pragma unroll
+    for (int off = 4; off < 32; off <<= 1) {
+      l0 += __shfl_xor_sync(0xffffffffu, l0, off);
+      l1 += __shfl_xor_sync(0xffffffffu, l1, off);
+    }
+    if (2 * q4 < GP) {
+      if (gq == 0) {
+        sc_m[warp * GP + 2 * q4] = m0;
+        sc_m[warp * GP + 2 * q4 + 1] = m1;
+        sc_l[warp * GP + 2 * q4] = l0;
+        sc_l[warp * GP + 2 * q4 + 1] = l1;
+      }
+      float* wacc = sc_acc + warp * GP * D;
+#pragma unroll
+      for (int j = 0; j < kSteps; ++j) {
+        const int d = 16 * j + gq;
+        wacc[(2 * q4) * D + d] = acc[j][0];
+        wacc[(2 * q4 + 1) * D + d] = acc[j][1];
+        wacc[(2 * q4) * D + d + 8] = acc[j][2];
+        wacc[(2 * q4 + 1) * D + d + 8] = acc[j][3];
+      }
+    }
+    __syncthreads();
+
+    const bool whole = seg_begin == spre && seg_end == spre + sgr.tiles;
+    const long long slot = (long long)sg + cta;  // unique per (group, CTA) along the line
+    for (int e = threadIdx.x; e < G * D; e += W * 32) {
+      const int g = e / D, d = e - (e / D) * D;
+      float M = kNegInf;
+#pragma unroll
+      for (int w = 0; w < W; ++w) M = fmaxf(M, sc_m[w * GP + g]);
+      float Ls = 0.f, A = 0.f;
+      if (M != kNegInf) {
+#pragma unroll
+        for (int w = 0; w < W; ++w) {
+          const float f = ex2(sc_m[w * GP + g] - M);
+          Ls += sc_l[w * GP + g] * f;
+          A += sc_acc[(w * GP + g) * D + d] * f;
+        }
+      }
+      if (whole) {
+        out[((int64_t)sgr.s * Hq + sgr.h * G + g) * D + d] = __float2bfloat16_rn(Ls > 0.f ? A / Ls : 0.f);
+      } else {
+        a.part_acc[(slot * G + g) * D + d] = A;
+        if (d == 0) {
+          a.part_ml[(slot * G + g) * 2 + 0] = M;
+          a.part_ml[(slot * G + g) * 2 + 1] = Ls;
+        }
+      }
+    }
+    if (!whole) {
+      // publish the partial, count arrivals; the last CTA of the group merges them all
+      const int c_lo = cta_of(spre, T, nctas), c_hi = cta_of(spre + sgr.tiles - 1, T, nctas);
+      __threadfence();
+      __syncthreads();
+      if (threadIdx.x == 0) {
+        int expected = 0;
+        for (int c = c_lo; c <= c_hi; ++c) expected += range_start(T, c + 1, nctas) > range_start(T, c, nctas);
+        const unsigned old = atomicAdd(&a.counters[sg], 1u);
+        s_last = old + 1u == (unsigned)expected;
+        if (s_last) a.counters[sg] = 0u;
+      }
+      __syncthreads();
+      if (s_last) {
+        __threadfence();
+        for (int e = threadIdx.x; e < G * D; e += W * 32) {
+          const int g = e / D, d = e - (e / D) * D;
+          float M = kNegInf;
+          for (int c = c_lo; c <= c_hi; ++c)
+            if (range_start(T, c + 1, nctas) > range_start(T, c, nctas))
+              M = fmaxf(M, __ldcg(&a.part_ml[(((long long)sg + c) * G + g) * 2]));
+          float Ls = 0.f, A = 0.f;
+          if (M != kNegInf) {
+            for (int c = c_lo; c <= c_hi; ++c) {
+              if (range_start(T, c + 1, nctas) <= range_start(T, c, nctas)) continue;
+              const long long ig = ((long long)sg + c) * G + g;
+              const float f = ex2(__ldcg(&a.part_ml[ig * 2]) - M);
+              Ls += __ldcg(&a.part_ml[ig * 2 + 1]) * f;
+              A += __ldcg(&a.part_acc[ig * D + d]) * f;
+            }
+          }
+          out[((int64_t)sgr.s * Hq + sgr.h * G + g) * D + d] = __float2bfloat16_rn(Ls > 0.f ? A / Ls : 0.f);
+        }
+      }
+    }
+    __syncthreads();  // the merge scratch is rewritten by the next segment
+    if (seg_end >= t_hi) break;
+    do {
+      spre += sgr.tiles;
+      sgr = load_group(a, ++sg);
+    } while (sgr.tiles == 0);
+  }
+
+  if (drain_from >= 0) {
+    // let copies still in flight land before the shared memory is released
+    for (int c = drain_from; c < issued; ++c)
+      if (!mbar_wait_bounded(&wbar[c % NS], (uint32_t)(c / NS) & 1u)) break;
+  }
+}
+
+template <int D, int GP, int NS>
+constexpr int sk_smem_bytes() {
+  return kWarps * NS * (2 * kTile * D * 2) + kWarps * GP * D * 4 + 1024;  // stages + merge scratch + align slack
+}
+
+// pipeline depth: 3 (head_dim 128) or 6 (head_dim 64) stages of 16 tokens per warp
+template <int D>
+constexpr int stages() {
+  return D == 128 ? 3 : 6;
+}
+
+template <int D, int GP>
+cudaError_t configure_one(int* ctas_per_sm) {
+  constexpr int NS = stages<D>();
+  cudaError_t e = cudaFuncSetAttribute(decode_sk_kernel<D, GP, NS>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       sk_smem_bytes<D, GP, NS>());
+  if (e != cudaSuccess) return e;
+  return cudaOccupancyMaxActiveBlocksPerMultiprocessor(ctas_per_sm, decode_sk_kernel<D, GP, NS>, kWarps * 32,
+                                                       sk_smem_bytes<D, GP, NS>());
+}
+
+template <int D, int GP>
+cudaError_t launch_one(const DecodeArgs& a, const CUtensorMap* tmap, int ctas, cudaStream_t st) {
+  constexpr int NS = stages<D>();
+  decode_sk_kernel<D, GP, NS><<<ctas, kWarps * 32, sk_smem_bytes<D, GP, NS>(), st>>>(*tmap, a);
+  count_launches(1);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+int decode_tc_group_pad(int group) { return group <= 4 ? 4 : 8; }
+
+cudaError_t configure_decode_tc(int head_dim, int* ctas_per_sm_gp4, int* ctas_per_sm_gp8) {
+  cudaError_t e;
+  if (head_dim == 128) {
+    if ((e = configure_one<128, 4>(ctas_per_sm_gp4)) != cudaSuccess) return e;
+    return configure_one<128, 8>(ctas_per_sm_gp8);
+  }
+  if (head_dim == 64) {
+    if ((e = configure_one<64, 4>(ctas_per_sm_gp4)) != cudaSuccess) return e;
+    return configure_one<64, 8>(ctas_per_sm_gp8);
+  }
+  return cudaErrorInvalidValue;
+}
+
+cudaError_t launch_decode_tc(const DecodeArgs& a, const CUtensorMap* tmap, int ctas, cudaStream_t st) {
+  const int gp = decode_tc_group_pad(a.group);
+  if (a.pv.head_dim == 128) return gp == 4 ? launch_one<128, 4>(a, tmap, ctas, st) : launch_one<128, 8>(a, tmap, ctas, st);
+  if (a.pv.head_dim == 64) return gp == 4 ? launch_one<64, 4>(a, tmap, ctas, st) : launch_one<64, 8>(a, tmap, ctas, st);
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace hwkv

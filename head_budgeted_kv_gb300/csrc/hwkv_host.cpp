@@ -136,10 +136,13 @@ struct hwkv_pool {
   void* d_meta = nullptr;
   int32_t* d_tbl = nullptr;
   int32_t* d_err = nullptr;
+  uint32_t* d_counters = nullptr;  // [layers][num_seqs * kv_heads] arrival counters, kept at 0
   std::vector<int32_t> h_tbl;
   int device = 0;
   int num_sms = 0;
+  int ctas_per_sm_gp4 = 0, ctas_per_sm_gp8 = 0;
   int split_override = 0;
+  int workers_override = 0;
   int kernel_choice = HWKV_KERNEL_AUTO;
   std::vector<LayerPlan> plans;
   bool has_tmap = false;
@@ -185,11 +188,25 @@ void plan_decode(hwkv_pool* p) {
   }
 }
 
-uint64_t workspace_bytes(const hwkv_pool* p, int group) {
+// persistent CTAs of the tensor-core kernel
+int tc_workers(const hwkv_pool* p, int group) {
+  if (p->workers_override > 0) return p->workers_override;
+  const int per_sm = decode_tc_group_pad(group) == 4 ? p->ctas_per_sm_gp4 : p->ctas_per_sm_gp8;
+  return std::max(1, p->num_sms * std::max(1, per_sm));
+}
+
+// partial slots: CUDA-core kernel one per chunk item; tensor-core kernel one per (group,
+// CTA) pair along the tile line, at most groups + CTAs
+int64_t partial_slots(const hwkv_pool* p, int group) {
+  if (use_tc(p)) return (int64_t)p->g.num_seqs * p->g.kv_heads + tc_workers(p, group);
   int64_t items = 0;
   for (const LayerPlan& lp : p->plans)
     if (lp.multi_chunk) items = std::max<int64_t>(items, lp.items);
-  return (uint64_t)items * group * (p->g.head_dim + 2) * sizeof(float);
+  return items;
+}
+
+uint64_t workspace_bytes(const hwkv_pool* p, int group) {
+  return (uint64_t)partial_slots(p, group) * group * (p->g.head_dim + 2) * sizeof(float);
 }
 
 int check_device(const hwkv_pool* p) {
@@ -289,13 +306,15 @@ int hwkv_pool_create(int layers, int kv_heads, int head_dim, int block_size, con
     return fail(HWKV_ERR_CUDA, "cudaDeviceGetAttribute: %s", cudaGetErrorString(e));
   }
   const size_t tbl_bytes = ((size_t)p->g.total_blocks * sizeof(int32_t) + 255) & ~(size_t)255;
-  e = cudaMalloc(&p->d_meta, tbl_bytes + 256);
+  const size_t cnt_bytes = (size_t)p->g.layers * p->g.num_seqs * p->g.kv_heads * sizeof(uint32_t);
+  e = cudaMalloc(&p->d_meta, tbl_bytes + 256 + cnt_bytes);
   if (e != cudaSuccess) {
     delete p;
     return fail(HWKV_ERR_CUDA, "cudaMalloc of the block table: %s", cudaGetErrorString(e));
   }
   p->d_tbl = static_cast<int32_t*>(p->d_meta);
   p->d_err = reinterpret_cast<int32_t*>(static_cast<char*>(p->d_meta) + tbl_bytes);
+  p->d_counters = reinterpret_cast<uint32_t*>(static_cast<char*>(p->d_meta) + tbl_bytes + 256);
   p->h_tbl.resize((size_t)p->g.total_blocks);
   for (int64_t i = 0; i < p->g.total_blocks; ++i) p->h_tbl[(size_t)i] = (int32_t)i;
 
@@ -309,7 +328,7 @@ int hwkv_pool_create(int layers, int kv_heads, int head_dim, int block_size, con
   if ((e = cudaMemcpyAsync(p->d_tbl, p->h_tbl.data(), (size_t)p->g.total_blocks * sizeof(int32_t),
                            cudaMemcpyHostToDevice, st)) != cudaSuccess)
     return cleanup_fail("upload of the block table", e);
-  if ((e = cudaMemsetAsync(p->d_err, 0, sizeof(int32_t), st)) != cudaSuccess) return cleanup_fail("cudaMemsetAsync", e);
+  if ((e = cudaMemsetAsync(p->d_err, 0, 256 + cnt_bytes, st)) != cudaSuccess) return cleanup_fail("cudaMemsetAsync", e);
   if ((e = cudaMemsetAsync(p->dev_pool, 0, p->g.pool_bytes, st)) != cudaSuccess)
     return cleanup_fail("zero-fill of the pool", e);
   if ((e = cudaStreamSynchronize(st)) != cudaSuccess) return cleanup_fail("cudaStreamSynchronize", e);
@@ -329,7 +348,7 @@ int hwkv_pool_create(int layers, int kv_heads, int head_dim, int block_size, con
     }
   }
   if (p->has_tmap) {
-    e = configure_decode_tc(p->g.head_dim);
+    e = configure_decode_tc(p->g.head_dim, &p->ctas_per_sm_gp4, &p->ctas_per_sm_gp8);
     if (e != cudaSuccess) return cleanup_fail("cudaFuncSetAttribute", e);
   }
   plan_decode(p);
@@ -451,8 +470,15 @@ int hwkv_decode_workspace_bytes(hwkv_pool_t p, int q_heads, uint64_t* out) {
   return ok();
 }
 
-int hwkv_decode_attn(hwkv_pool_t p, int layer, const void* q, int q_heads, float scale, const int32_t* lens_dev,
-                     void* out, void* workspace, uint64_t ws_bytes, void* stream) {
+}  // extern "C"
+
+namespace {
+
+// Shared body of hwkv_decode_attn (len_add 0, no new rows) and hwkv_append_decode_attn
+// (len_add 1: lens are the positions before the append, k_new / v_new are appended).
+int decode_common(hwkv_pool_t p, int layer, const void* q, int q_heads, float scale, const int32_t* lens_dev,
+                  int len_add, const void* k_new, const void* v_new, void* out, void* workspace, uint64_t ws_bytes,
+                  void* stream) {
   if (!p) return fail(HWKV_ERR_INVALID_ARG, "pool is NULL");
   const Geometry& g = p->g;
   if (layer < 0 || layer >= g.layers) return fail(HWKV_ERR_INVALID_ARG, "layer %d out of range", layer);
@@ -464,10 +490,15 @@ int hwkv_decode_attn(hwkv_pool_t p, int layer, const void* q, int q_heads, float
   if (!q || !out || !lens_dev) return fail(HWKV_ERR_INVALID_ARG, "NULL tensor argument");
   if (!aligned(q, 16) || !aligned(out, 16) || !aligned(lens_dev, 4))
     return fail(HWKV_ERR_ALIGNMENT, "q / out must be 16-byte aligned, lens 4-byte aligned");
+  if (len_add) {
+    if (!k_new || !v_new) return fail(HWKV_ERR_INVALID_ARG, "NULL k_new / v_new");
+    if (!aligned(k_new, 16) || !aligned(v_new, 16)) return fail(HWKV_ERR_ALIGNMENT, "k_new / v_new must be 16-byte aligned");
+  }
   const int G = q_heads / g.kv_heads;
   const LayerPlan& lp = p->plans[layer];
+  const bool tc = use_tc(p);
   const uint64_t need = workspace_bytes(p, G);
-  if (lp.multi_chunk) {
+  if (tc || lp.multi_chunk) {
     if (!workspace || ws_bytes < need)
       return fail(HWKV_ERR_WORKSPACE_TOO_SMALL, "workspace holds %llu bytes, decode needs %llu",
                   (unsigned long long)ws_bytes, (unsigned long long)need);
@@ -485,27 +516,55 @@ int hwkv_decode_attn(hwkv_pool_t p, int layer, const void* q, int q_heads, float
   a.q = q;
   a.out = out;
   a.lens = lens_dev;
-  int64_t items_max = 0;
-  for (const LayerPlan& x : p->plans)
-    if (x.multi_chunk) items_max = std::max<int64_t>(items_max, x.items);
+  a.len_add = len_add;
+  const int64_t slots = partial_slots(p, G);
   a.part_acc = static_cast<float*>(workspace);
-  a.part_ml = workspace ? static_cast<float*>(workspace) + items_max * G * g.head_dim : nullptr;
+  a.part_ml = workspace ? static_cast<float*>(workspace) + slots * G * g.head_dim : nullptr;
+  a.counters = p->d_counters + (int64_t)layer * g.num_seqs * g.kv_heads;
   a.scale_log2 = scale * 1.4426950408889634f;
   a.group = G;
   a.split_tokens = lp.split;
   std::memcpy(a.chunk_prefix, lp.chunk_prefix, sizeof a.chunk_prefix);
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  if (use_tc(p)) {
-    HWKV_CUDA_TRY(launch_decode_tc(a, &p->tmap, lp.items, st), "decode launch");
-  } else {
-    HWKV_CUDA_TRY(launch_decode_simt(a, g.dtype, lp.items, st), "decode launch");
+  if (tc) {
+    a.k_new = len_add ? k_new : nullptr;  // appended inside the kernel
+    a.v_new = len_add ? v_new : nullptr;
+    HWKV_CUDA_TRY(launch_decode_tc(a, &p->tmap, tc_workers(p, G), st), "decode launch");
+    return ok();
   }
+  if (len_add) {
+    CopyArgs c;
+    std::memset(&c, 0, sizeof c);
+    c.pv = a.pv;
+    c.g = a.g;
+    c.k = k_new;
+    c.v = v_new;
+    c.lens = lens_dev;
+    HWKV_CUDA_TRY(launch_append(c, g.dtype, st), "append launch");
+  }
+  HWKV_CUDA_TRY(launch_decode_simt(a, g.dtype, lp.items, st), "decode launch");
   if (lp.multi_chunk) HWKV_CUDA_TRY(launch_combine(a, g.dtype, st), "combine launch");
   return ok();
 }
 
-int hwkv_set_decode_config(hwkv_pool_t p, int split_tokens, int kernel) {
+}  // namespace
+
+extern "C" {
+
+int hwkv_decode_attn(hwkv_pool_t p, int layer, const void* q, int q_heads, float scale, const int32_t* lens_dev,
+                     void* out, void* workspace, uint64_t ws_bytes, void* stream) {
+  return decode_common(p, layer, q, q_heads, scale, lens_dev, 0, nullptr, nullptr, out, workspace, ws_bytes, stream);
+}
+
+int hwkv_append_decode_attn(hwkv_pool_t p, int layer, const void* q, int q_heads, float scale, const void* k_new,
+                            const void* v_new, const int32_t* pos_dev, void* out, void* workspace, uint64_t ws_bytes,
+                            void* stream) {
+  return decode_common(p, layer, q, q_heads, scale, pos_dev, 1, k_new, v_new, out, workspace, ws_bytes, stream);
+}
+
+int hwkv_set_decode_config(hwkv_pool_t p, int split_tokens, int workers, int kernel) {
   if (!p) return fail(HWKV_ERR_INVALID_ARG, "pool is NULL");
+  if (workers < 0 || workers > (1 << 20)) return fail(HWKV_ERR_INVALID_ARG, "workers must be in [0, 2^20]");
   if (split_tokens != 0 &&
       (split_tokens < 16 || split_tokens > 65536 || (split_tokens & (split_tokens - 1)) != 0))
     return fail(HWKV_ERR_INVALID_ARG, "split_tokens must be 0 or a power of two in [16, 65536]");
@@ -514,6 +573,7 @@ int hwkv_set_decode_config(hwkv_pool_t p, int split_tokens, int kernel) {
   if (kernel == HWKV_KERNEL_TENSOR && !tc_eligible(p))
     return fail(HWKV_ERR_UNSUPPORTED, "tensor-core decode needs bf16 and block_size % 16 == 0");
   p->split_override = split_tokens;
+  p->workers_override = workers;
   p->kernel_choice = kernel;
   plan_decode(p);
   return ok();
@@ -535,7 +595,12 @@ int hwkv_check_device_errors(hwkv_pool_t p, void* stream, int32_t* out_bits) {
   HWKV_CUDA_TRY(cudaMemcpy(&bits, p->d_err, sizeof bits, cudaMemcpyDeviceToHost), "read of the error word");
   HWKV_CUDA_TRY(cudaMemset(p->d_err, 0, sizeof bits), "reset of the error word");
   if (out_bits) *out_bits = bits;
-  if (bits != 0) return fail(HWKV_ERR_DEVICE_CHECK, "device error bits 0x%x", bits);
+  if (bits != 0) {
+    // an aborted launch can leave arrival counters behind: start the next launch from zero
+    HWKV_CUDA_TRY(cudaMemset(p->d_counters, 0, (size_t)p->g.layers * p->g.num_seqs * p->g.kv_heads * sizeof(uint32_t)),
+                  "reset of the arrival counters");
+    return fail(HWKV_ERR_DEVICE_CHECK, "device error bits 0x%x", bits);
+  }
   return ok();
 }
 

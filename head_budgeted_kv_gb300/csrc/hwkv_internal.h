@@ -50,13 +50,17 @@ struct DecodeArgs {
   LayerGeom g;
   const void* q;           // [B][Hq][D]
   void* out;               // [B][Hq][D]
-  const int32_t* lens;     // [B] lengths after the append
-  float* part_acc;         // [items][G][D]   unnormalised split accumulators
-  float* part_ml;          // [items][G][2]   (running max in log2 units, sum of weights)
+  const int32_t* lens;     // [B]; length after the append = lens[s] + len_add
+  int32_t len_add;         // 0: lens are lengths after the append; 1: positions (fused append)
+  const void* k_new;       // fused append: new K / V rows [B][H][D], else null
+  const void* v_new;
+  float* part_acc;         // [slots][G][D]   unnormalised split accumulators
+  float* part_ml;          // [slots][G][2]   (running max in log2 units, sum of weights)
+  uint32_t* counters;      // [B*H] arrival counters of this layer (tensor-core kernel), all 0
   float scale_log2;        // scale * log2(e)
   int32_t group;           // G = Hq / H
-  int32_t split_tokens;    // tokens per split-K chunk (power of two, multiple of 16)
-  int32_t chunk_prefix[kMaxKvHeads + 1];  // prefix sums over heads of ceil(C_h / split)
+  int32_t split_tokens;    // CUDA-core kernel: tokens per split-K chunk (power of two)
+  int32_t chunk_prefix[kMaxKvHeads + 1];  // CUDA-core kernel: prefix over heads of ceil(C_h / split)
 };
 
 // Counts every kernel launch the library makes (read by hwkv_kernel_launches).
@@ -66,8 +70,11 @@ void count_launches(uint64_t n);
 cudaError_t launch_append(const CopyArgs& a, int dtype, cudaStream_t st);
 // max_rows: the most positions any (seq, head) of the layer copies, min(max window, max_len)
 cudaError_t launch_materialize(const CopyArgs& a, int dtype, int max_rows, cudaStream_t st);
-cudaError_t configure_decode_tc(int head_dim);  // once per device before the first launch
-cudaError_t launch_decode_tc(const DecodeArgs& a, const CUtensorMap* tmap, int items, cudaStream_t st);
+// once per device before the first launch; returns resident CTAs per SM of both instances
+cudaError_t configure_decode_tc(int head_dim, int* ctas_per_sm_gp4, int* ctas_per_sm_gp8);
+// tensor-core kernel: `ctas` persistent CTAs split the resident tiles of the layer evenly
+cudaError_t launch_decode_tc(const DecodeArgs& a, const CUtensorMap* tmap, int ctas, cudaStream_t st);
+int decode_tc_group_pad(int group);  // query-head columns the kernel instance holds (4 or 8)
 cudaError_t launch_decode_simt(const DecodeArgs& a, int dtype, int items, cudaStream_t st);
 cudaError_t launch_combine(const DecodeArgs& a, int dtype, cudaStream_t st);
 

@@ -145,8 +145,8 @@ int hwkv_materialize(hwkv_pool_t pool, int layer, const void* k_full, const void
 int hwkv_append(hwkv_pool_t pool, int layer, const void* k_new, const void* v_new, const int32_t* pos_dev,
                 void* stream);
 
-/* Bytes of scratch hwkv_decode_attn needs for the current decode configuration (fp32
- * split-K partials; maximum over layers). */
+/* Bytes of scratch hwkv_decode_attn / hwkv_append_decode_attn need for the current decode
+ * configuration (fp32 split-K partials; maximum over layers). */
 int hwkv_decode_workspace_bytes(hwkv_pool_t pool, int q_heads, uint64_t* out);
 
 /* Split-K decode attention over the resident window of one layer (abstract: attention reads
@@ -157,17 +157,30 @@ int hwkv_decode_workspace_bytes(hwkv_pool_t pool, int q_heads, uint64_t* out);
  *   q, out: device [num_seqs][q_heads][D], 16-byte aligned; q_heads = G * kv_heads, G <= 8.
  *   lens_dev: device int32 [num_seqs], lengths AFTER this step's append.  len 0 gives 0s.
  *   workspace: device scratch of >= hwkv_decode_workspace_bytes(), 16-byte aligned; its
- *              contents need no initialisation and are clobbered.
+ *              contents need no initialisation and are clobbered.  Launches that may run
+ *              at the same time need distinct workspaces.
+ * The tensor-core kernel splits the layer's resident tiles evenly over a persistent grid and
+ * merges partial results through per-(seq, head) arrival counters that the library keeps in
+ * its own device memory (one set per layer); concurrent launches of the SAME layer race.
  * Errors: HWKV_ERR_INVALID_ARG, HWKV_ERR_ALIGNMENT, HWKV_ERR_WORKSPACE_TOO_SMALL,
  *         HWKV_ERR_UNSUPPORTED, HWKV_ERR_CUDA (launch failure). */
 int hwkv_decode_attn(hwkv_pool_t pool, int layer, const void* q, int q_heads, float scale,
                      const int32_t* lens_dev, void* out, void* workspace, uint64_t workspace_bytes,
                      void* stream);
 
-/* Decode configuration: split_tokens = tokens of one split-K chunk (0 = automatic; else a
- * power of two in [16, 65536]); kernel = HWKV_KERNEL_*.  Changes the workspace size.
- * Results differ between configurations only by floating-point rounding. */
-int hwkv_set_decode_config(hwkv_pool_t pool, int split_tokens, int kernel);
+/* One decode step of one layer: hwkv_append followed by hwkv_decode_attn, with the same
+ * results.  pos_dev holds the lengths BEFORE the append; attention runs at pos + 1.  On the
+ * tensor-core path this is a single kernel: the CTA that streams the tile holding the new
+ * token's slot takes the new rows from k_new / v_new and also writes them into the pool. */
+int hwkv_append_decode_attn(hwkv_pool_t pool, int layer, const void* q, int q_heads, float scale,
+                            const void* k_new, const void* v_new, const int32_t* pos_dev, void* out,
+                            void* workspace, uint64_t workspace_bytes, void* stream);
+
+/* Decode configuration.  kernel = HWKV_KERNEL_*.  split_tokens: tokens of one split-K chunk of
+ * the CUDA-core kernel (0 = automatic; else a power of two in [16, 65536]).  workers: CTAs of
+ * the tensor-core kernel's persistent grid (0 = automatic: every SM, as many CTAs as fit).
+ * Changes the workspace size.  Results differ between configurations only by rounding. */
+int hwkv_set_decode_config(hwkv_pool_t pool, int split_tokens, int workers, int kernel);
 
 /* Number of kernels this library has launched in this process (all pools, all devices).
  * Lets a caller count the launches inside a timed region. */

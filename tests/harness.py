@@ -44,14 +44,15 @@ class Run:
     """One pool driven through materialise, then append + decode per step."""
 
     def __init__(self, cfg, kernel=hw.HWKV_KERNEL_AUTO, split=0, canary: Optional[int] = None,
-                 keep_host_steps=True):
+                 keep_host_steps=True, workers=0, fused=False):
         self.cfg = cfg
         self.dev = torch.device("cuda", torch.cuda.current_device())
         gen_dev = "cpu" if cfg.single_cpu_stream else self.dev
         self.wl = workloads.Workload(cfg, device=gen_dev)
         self.pool = hw.Pool(cfg.layers, cfg.kv_heads, cfg.head_dim, cfg.block_size, cfg.windows_array(), cfg.batch,
                             cfg.torch_dtype, q_heads=cfg.q_heads, device=self.dev)
-        self.pool.set_decode_config(split, kernel)
+        self.pool.set_decode_config(split, kernel, workers)
+        self.fused = fused
         if canary is not None:
             self.pool.buffer.fill_(canary)
             torch.cuda.synchronize()
@@ -78,8 +79,11 @@ class Run:
         keep = set(keep_layers)
         res = {}
         for l in range(self.cfg.layers):
-            self.pool.append(l, kn[l], vn[l], pos)
-            out = self.pool.decode(l, q[l], self.cfg.scale, lens)
+            if self.fused:
+                out = self.pool.append_decode(l, q[l], self.cfg.scale, kn[l], vn[l], pos)
+            else:
+                self.pool.append(l, kn[l], vn[l], pos)
+                out = self.pool.decode(l, q[l], self.cfg.scale, lens)
             if l in keep:
                 res[l] = (workloads.to_raw(q[l]), out.float().cpu().double().numpy())
         self.steps_done += 1

@@ -110,7 +110,8 @@ def test_null_pool_handles_are_rejected(lib):
     assert lib.hwkv_pool_destroy(None) == binding.HWKV_OK
     assert lib.hwkv_decode_attn(None, 0, None, 4, 1.0, None, None, None, 0, None) == binding.HWKV_ERR_INVALID_ARG
     assert lib.hwkv_append(None, 0, None, None, None, None) == binding.HWKV_ERR_INVALID_ARG
-    assert lib.hwkv_set_decode_config(None, 0, 0) == binding.HWKV_ERR_INVALID_ARG
+    assert lib.hwkv_set_decode_config(None, 0, 0, 0) == binding.HWKV_ERR_INVALID_ARG
+    assert lib.hwkv_append_decode_attn(None, 0, None, 4, 1.0, None, None, None, None, None, 0, None) == binding.HWKV_ERR_INVALID_ARG
 
 
 def test_last_error_is_thread_local(lib):

@@ -144,16 +144,53 @@ def test_empty_context_gives_zero_output():
 
 
 @pytest.mark.parametrize("split", [16, 64, 256, 4096])
-@pytest.mark.parametrize("kernel", [hw.HWKV_KERNEL_TENSOR, hw.HWKV_KERNEL_SIMT])
-def test_split_size_changes_rounding_only(split, kernel):
+def test_simt_split_size_changes_rounding_only(split):
     cfg = small_config(name="split", kv_heads=4, windows=((4096, 1024, 256, 2000),), prefill=(5000, 1500, 300))
-    run = Run(cfg, kernel=kernel, split=split)
+    run = Run(cfg, kernel=hw.HWKV_KERNEL_SIMT, split=split)
     run.materialize()
     res = run.step(keep_layers=[0])
     q_raw, got = res[0]
     assert_close(got, run.reference(0, 0, q_raw), cfg, f"split {split}")
     assert run.device_errors() == 0
     run.close()
+
+
+@pytest.mark.parametrize("workers", [1, 2, 3, 7, 64, 1000, 5000])
+def test_tensor_core_partition_changes_rounding_only(workers):
+    """The persistent grid's size decides how the resident tiles are split into ranges and
+    how many partials each head merges; more workers than tiles leaves some empty."""
+    cfg = small_config(name="workers", kv_heads=4, windows=((4096, 1024, 256, 2000),), prefill=(5000, 1500, 300))
+    run = Run(cfg, kernel=hw.HWKV_KERNEL_TENSOR, workers=workers)
+    run.materialize()
+    for i in range(2):
+        res = run.step(keep_layers=[0])
+        q_raw, got = res[0]
+        assert_close(got, run.reference(i, 0, q_raw), cfg, f"workers {workers} step {i}")
+    assert run.device_errors() == 0
+    run.close()
+
+
+@pytest.mark.parametrize("name", ["clip", "ring_c_gt_w", "g8", "bs64_layers", "bs5", "f32"])
+def test_fused_append_decode_equals_append_then_decode(name):
+    """hwkv_append_decode_attn gives the same pool bytes and the same outputs as hwkv_append
+    followed by hwkv_decode_attn, and matches the oracle."""
+    spec = dict(EDGE[name])
+    steps = spec.pop("steps", 3)
+    cfg = small_config(name=name, steps=steps, **spec)
+    split, fused = Run(cfg), Run(cfg, fused=True)
+    split.materialize()
+    fused.materialize()
+    for i in range(steps):
+        ra = split.step(keep_layers=range(cfg.layers))
+        rb = fused.step(keep_layers=range(cfg.layers))
+        for l in range(cfg.layers):
+            assert np.array_equal(ra[l][1], rb[l][1]), f"{name} step {i} layer {l}"
+            assert_close(rb[l][1], fused.reference(i, l, rb[l][0]), cfg, f"fused {name} step {i} layer {l}")
+    torch.cuda.synchronize()
+    assert torch.equal(split.pool.buffer, fused.pool.buffer)
+    assert split.device_errors() == 0 and fused.device_errors() == 0
+    split.close()
+    fused.close()
 
 
 def test_block_permutation_leaves_output_bit_identical():
