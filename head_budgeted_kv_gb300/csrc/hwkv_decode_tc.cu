@@ -107,6 +107,47 @@ __device__ __forceinline__ long long block_exclusive_scan(long long v, long long
   return base + x - v;
 }
 
+// Final merge of one group by the last CTA to arrive: the group's partials sit in slots
+// g + c for the contributing CTAs c in [c_lo, c_hi].  One pass: every thread owns 4
+// consecutive output columns of one query head and folds the partials in with the online
+// rule (running max M, weight sum L, accumulator A rescaled by 2^(M_old - M_new)); the
+// loads of all partials are independent, 16 bytes each for the accumulators.
+template <int D>
+__device__ __forceinline__ void merge_partials(const DecodeArgs& a, int g, int c_lo, int c_hi, long long T, int nctas,
+                                               bool all_live, __nv_bfloat16* out_grp) {
+  const int G = a.group;
+  constexpr int kV = D / 4;  // float4 columns per query head
+  const float* pm = a.part_ml;
+  for (int e = threadIdx.x; e < G * kV; e += blockDim.x) {
+    const int q = e / kV, d4 = e - (e / kV) * kV;
+    float M = kNegInf, L = 0.f;
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll 4
+    for (int c = c_lo; c <= c_hi; ++c) {
+      if (!all_live && range_start(T, c + 1, nctas) <= range_start(T, c, nctas)) continue;
+      const long long slot = ((long long)g + c) * G + q;
+      const float2 ml = __ldcg(reinterpret_cast<const float2*>(pm) + slot);
+      const float4 v = __ldcg(reinterpret_cast<const float4*>(a.part_acc + slot * D) + d4);
+      const float Mn = fmaxf(M, ml.x);
+      if (Mn == kNegInf) continue;
+      const float fo = ex2(M - Mn), fn = ex2(ml.x - Mn);
+      L = fmaf(L, fo, ml.y * fn);
+      acc.x = fmaf(acc.x, fo, v.x * fn);
+      acc.y = fmaf(acc.y, fo, v.y * fn);
+      acc.z = fmaf(acc.z, fo, v.z * fn);
+      acc.w = fmaf(acc.w, fo, v.w * fn);
+      M = Mn;
+    }
+    const float inv = L > 0.f ? 1.f / L : 0.f;
+    __nv_bfloat162 lo = __floats2bfloat162_rn(acc.x * inv, acc.y * inv);
+    __nv_bfloat162 hi = __floats2bfloat162_rn(acc.z * inv, acc.w * inv);
+    uint2 packed;
+    packed.x = *reinterpret_cast<uint32_t*>(&lo);
+    packed.y = *reinterpret_cast<uint32_t*>(&hi);
+    *reinterpret_cast<uint2*>(out_grp + (int64_t)q * D + d4 * 4) = packed;
+  }
+}
+
 template <int D, int GP, int NS>
 __global__ void __launch_bounds__(kWarps * 32) decode_sk_kernel(const __grid_constant__ CUtensorMap tmap,
                                                                 const __grid_constant__ DecodeArgs a) {
@@ -135,6 +176,9 @@ __global__ void __launch_bounds__(kWarps * 32) decode_sk_kernel(const __grid_con
   const int Hq = H * G;
   const int bs = a.pv.block_size;
   __nv_bfloat16* const out = static_cast<__nv_bfloat16*>(a.out);
+
+  // launched as a programmatic dependent: everything below reads what earlier kernels wrote
+  griddep_wait();
 
   if (cta == 0) {
     for (int s = threadIdx.x; s < B; s += W * 32)
@@ -188,12 +232,12 @@ __global__ void __launch_bounds__(kWarps * 32) decode_sk_kernel(const __grid_con
   Group igr = load_group(a, ig);
   long long j_issue = t_lo + warp;
   int issued = 0;
-  auto issue_next = [&]() {
+  auto issue_next = [&](int issuer) {
     while (j_issue >= ipre + igr.tiles) {
       ipre += igr.tiles;
       igr = load_group(a, ++ig);
     }
-    if (lane == 0) {
+    if (lane == issuer) {
       const int st = issued % NS;
       const int t0 = tile_slot(igr, j_issue - ipre);
       const int jb = t0 / bs;
@@ -216,7 +260,8 @@ __global__ void __launch_bounds__(kWarps * 32) decode_sk_kernel(const __grid_con
     j_issue += W;
     ++issued;
   };
-  for (int i = 0; i < NS && j_issue < t_hi; ++i) issue_next();
+  // the first stages are issued by different lanes so their table lookups overlap
+  for (int i = 0; i < NS && j_issue < t_hi; ++i) issue_next(i);
 
   // ldmatrix lane roles: matrix mi = lane/8, row rr = lane%8
   const int mi = lane >> 3, rr = lane & 7;
@@ -343,13 +388,14 @@ __global__ void __launch_bounds__(kWarps * 32) decode_sk_kernel(const __grid_con
           fence_proxy_async_smem();
           __syncwarp();
         }
-        issue_next();
+        issue_next(0);
       }
       patched_stage = false;
       j_cons += W;
     }
 
     // ---- end of segment: merge the warps, then store output or partial -----------------
+    if (seg_end >= t_hi) griddep_launch_dependents();  // this CTA reads no more tiles
 #pragma unroll
     for (int off = 4; off < 32; off <<= 1) {
       l0 += __shfl_xor_sync(0xffffffffu, l0, off);
@@ -403,11 +449,15 @@ __global__ void __launch_bounds__(kWarps * 32) decode_sk_kernel(const __grid_con
     if (!whole) {
       // publish the partial, count arrivals; the last CTA of the group merges them all
       const int c_lo = cta_of(spre, T, nctas), c_hi = cta_of(spre + sgr.tiles - 1, T, nctas);
+      const bool all_live = T >= nctas;  // then no CTA range is empty
       __threadfence();
       __syncthreads();
       if (threadIdx.x == 0) {
-        int expected = 0;
-        for (int c = c_lo; c <= c_hi; ++c) expected += range_start(T, c + 1, nctas) > range_start(T, c, nctas);
+        int expected = c_hi - c_lo + 1;
+        if (!all_live) {
+          expected = 0;
+          for (int c = c_lo; c <= c_hi; ++c) expected += range_start(T, c + 1, nctas) > range_start(T, c, nctas);
+        }
         const unsigned old = atomicAdd(&a.counters[sg], 1u);
         s_last = old + 1u == (unsigned)expected;
         if (s_last) a.counters[sg] = 0u;
@@ -415,24 +465,7 @@ __global__ void __launch_bounds__(kWarps * 32) decode_sk_kernel(const __grid_con
       __syncthreads();
       if (s_last) {
         __threadfence();
-        for (int e = threadIdx.x; e < G * D; e += W * 32) {
-          const int g = e / D, d = e - (e / D) * D;
-          float M = kNegInf;
-          for (int c = c_lo; c <= c_hi; ++c)
-            if (range_start(T, c + 1, nctas) > range_start(T, c, nctas))
-              M = fmaxf(M, __ldcg(&a.part_ml[(((long long)sg + c) * G + g) * 2]));
-          float Ls = 0.f, A = 0.f;
-          if (M != kNegInf) {
-            for (int c = c_lo; c <= c_hi; ++c) {
-              if (range_start(T, c + 1, nctas) <= range_start(T, c, nctas)) continue;
-              const long long ig = ((long long)sg + c) * G + g;
-              const float f = ex2(__ldcg(&a.part_ml[ig * 2]) - M);
-              Ls += __ldcg(&a.part_ml[ig * 2 + 1]) * f;
-              A += __ldcg(&a.part_acc[ig * D + d]) * f;
-            }
-          }
-          out[((int64_t)sgr.s * Hq + sgr.h * G + g) * D + d] = __float2bfloat16_rn(Ls > 0.f ? A / Ls : 0.f);
-        }
+        merge_partials<D>(a, sg, c_lo, c_hi, T, nctas, all_live, out + ((int64_t)sgr.s * Hq + sgr.h * G) * D);
       }
     }
     __syncthreads();  // the merge scratch is rewritten by the next segment
@@ -474,9 +507,21 @@ cudaError_t configure_one(int* ctas_per_sm) {
 template <int D, int GP>
 cudaError_t launch_one(const DecodeArgs& a, const CUtensorMap* tmap, int ctas, cudaStream_t st) {
   constexpr int NS = stages<D>();
-  decode_sk_kernel<D, GP, NS><<<ctas, kWarps * 32, sk_smem_bytes<D, GP, NS>(), st>>>(*tmap, a);
+  // programmatic dependent launch: the CTAs may become resident while the previous kernel in
+  // the stream finishes; they wait for it (griddepcontrol.wait) before reading anything
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)ctas);
+  cfg.blockDim = dim3(kWarps * 32);
+  cfg.dynamicSmemBytes = sk_smem_bytes<D, GP, NS>();
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  cudaError_t e = cudaLaunchKernelEx(&cfg, decode_sk_kernel<D, GP, NS>, *tmap, a);
   count_launches(1);
-  return cudaGetLastError();
+  return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 }  // namespace
