@@ -53,6 +53,7 @@ SIGNATURES = [
     ("hwkv_decode_workspace_bytes", _i, [_vp, _i, _c_u64p]),
     ("hwkv_decode_attn", _i, [_vp, _i, _vp, _i, ctypes.c_float, _vp, _vp, _vp, _u64, _vp]),
     ("hwkv_append_decode_attn", _i, [_vp, _i, _vp, _i, ctypes.c_float, _vp, _vp, _vp, _vp, _vp, _u64, _vp]),
+    ("hwkv_decode_attn_noalloc", _i, [_vp, _i, _vp, _i, ctypes.c_float, _vp, _vp, _vp]),
     ("hwkv_set_decode_config", _i, [_vp, _i, _i, _i]),
     ("hwkv_kernel_launches", _i, [_c_u64p]),
     ("hwkv_check_device_errors", _i, [_vp, _vp, _c_i32p]),
@@ -227,6 +228,15 @@ def hwkv_append_decode_attn(pool: int, layer: int, q: torch.Tensor, scale: float
     ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
     _check(load().hwkv_append_decode_attn(pool, layer, _ptr(q), q.shape[1], float(scale), _ptr(k_new), _ptr(v_new),
                                           _ptr(pos), _ptr(out), _ptr(workspace), ws_bytes, _stream_ptr(stream)))
+
+
+def hwkv_decode_attn_noalloc(pool: int, layer: int, q: torch.Tensor, scale: float, lens: torch.Tensor,
+                             out: torch.Tensor, stream=None):
+    """hwkv_decode_attn with the library's static scratch instead of a caller workspace."""
+    if not (q.is_contiguous() and out.is_contiguous()):
+        raise ValueError("q and out must be contiguous")
+    _check(load().hwkv_decode_attn_noalloc(pool, layer, _ptr(q), q.shape[1], float(scale), _ptr(lens), _ptr(out),
+                                           _stream_ptr(stream)))
 
 
 def hwkv_set_decode_config(pool: int, split_tokens: int = 0, workers: int = 0, kernel: int = HWKV_KERNEL_AUTO):

@@ -130,6 +130,16 @@ bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p
 
 void hwkv::count_launches(uint64_t n) { g_launches.fetch_add(n, std::memory_order_relaxed); }
 
+int hwkv::set_error(int code, const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof buf, fmt, ap);
+  va_end(ap);
+  g_last_error = buf;
+  return code;
+}
+
 struct hwkv_pool {
   Geometry g;
   char* dev_pool = nullptr;

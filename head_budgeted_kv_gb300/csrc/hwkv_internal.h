@@ -66,6 +66,9 @@ struct DecodeArgs {
 // Counts every kernel launch the library makes (read by hwkv_kernel_launches).
 void count_launches(uint64_t n);
 
+// Records a message for hwkv_last_error() on this thread and returns `code`.
+int set_error(int code, const char* fmt, ...);
+
 // Launchers (hwkv_copy.cu, hwkv_decode.cu).  dtype: 0 = f32, 1 = bf16.
 cudaError_t launch_append(const CopyArgs& a, int dtype, cudaStream_t st);
 // max_rows: the most positions any (seq, head) of the layer copies, min(max window, max_len)

@@ -176,6 +176,27 @@ int hwkv_append_decode_attn(hwkv_pool_t pool, int layer, const void* q, int q_he
                             const void* k_new, const void* v_new, const int32_t* pos_dev, void* out,
                             void* workspace, uint64_t workspace_bytes, void* stream);
 
+/* Bytes of the static scratch array behind hwkv_decode_attn_noalloc. */
+#define HWKV_NOALLOC_SCRATCH_BYTES (4u << 20)
+
+/* hwkv_decode_attn without a workspace argument, for callers that cannot allocate device
+ * memory where they run attention (during CUDA graph capture, under an allocator that owns
+ * all device memory, inside hosts that forbid allocation after start-up).  The pages have
+ * no counterpart: this is a service of this library, not a step of the method.
+ *   Results are those of hwkv_decode_attn with the same arguments.  The split-K scratch is a
+ *   fixed array of HWKV_NOALLOC_SCRATCH_BYTES (4 MiB) inside the library, present on every
+ *   GPU that loads the library until the process exits; the call itself allocates nothing
+ *   (no cudaMalloc / cudaFree, no allocating library routine).
+ *   A configuration whose scratch (hwkv_decode_workspace_bytes) exceeds the array is
+ *   rejected with HWKV_ERR_WORKSPACE_TOO_SMALL before anything is launched.
+ *   The first call on a device looks up the array's device address on that device (with
+ *   that device current): make that first call before any stream capture.
+ *   All calls share the one array and it keeps the last call's contents; nothing in it has
+ *   to start at zero.  Calls whose kernels overlap on the GPU (other streams, other threads)
+ *   race on the array: serialise them. */
+int hwkv_decode_attn_noalloc(hwkv_pool_t pool, int layer, const void* q, int q_heads, float scale,
+                             const int32_t* lens_dev, void* out, void* stream);
+
 /* Decode configuration.  kernel = HWKV_KERNEL_*.  split_tokens: tokens of one split-K chunk of
  * the CUDA-core kernel (0 = automatic; else a power of two in [16, 65536]).  workers: CTAs of
  * the tensor-core kernel's persistent grid (0 = automatic: every SM, as many CTAs as fit).
