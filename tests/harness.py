@@ -101,7 +101,11 @@ class Run:
         return self._pre_cache[key]
 
     def history(self, l, s, h, lo, hi):
-        return self.wl.history(l, s, h, lo, hi, prefill=self._prefill_host(l, s), steps=self.host_steps)
+        if hi <= lo:
+            empty = workloads.to_raw(torch.zeros((0, self.cfg.head_dim), dtype=self.cfg.torch_dtype))
+            return empty, empty
+        pre = self._prefill_host(l, s) if lo < self.cfg.prefill[s] else None
+        return self.wl.history(l, s, h, lo, hi, prefill=pre, steps=self.host_steps)
 
     def reference(self, step: int, layer: int, q_raw: np.ndarray, seqs=None) -> np.ndarray:
         """Oracle output [B][Hq][D] (fp64) of decode step ``step`` (0-based) of ``layer``."""
