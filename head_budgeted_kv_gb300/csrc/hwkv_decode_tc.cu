@@ -31,6 +31,7 @@ namespace hwkv {
 namespace {
 
 constexpr int kWarps = 4;
+constexpr int kFlatMerge = 24;  // most contributors one CTA merges directly
 
 // One (seq, kv head) group at this step: its resident window and needed tiles.
 struct Group {
@@ -107,49 +108,84 @@ __device__ __forceinline__ long long block_exclusive_scan(long long v, long long
   return base + x - v;
 }
 
-// Final merge of one group by the last CTA to arrive: the group's partials sit in slots
-// g + c for the contributing CTAs c in [c_lo, c_hi].  One pass: every thread owns 4
-// consecutive output columns of one query head and folds the partials in with the online
-// rule (running max M, weight sum L, accumulator A rescaled by 2^(M_old - M_new)); the
-// loads of all partials are independent, 16 bytes each for the accumulators.
-template <int D>
-__device__ __forceinline__ void merge_partials(const DecodeArgs& a, int g, int c_lo, int c_hi, long long T, int nctas,
-                                               bool all_live, __nv_bfloat16* out_grp) {
-  const int G = a.group;
+// Folds `count` consecutive partial slots [first, first + count) of a partial buffer with the
+// online rule (running max M, weight sum L, accumulator rescaled by 2^(M_old - M_new)).  Each
+// thread owns 4 consecutive output columns of one query head and keeps 8 slots' loads in
+// flight.  The result goes to the normalised bf16 output `out_grp` when it is non-null, else
+// to partial slot `dst_slot` of (dst_acc, dst_ml).  `live(i)` tells whether slot first + i
+// holds a partial.
+template <int D, typename Live>
+__device__ __forceinline__ void merge_slots(const float* src_acc, const float* src_ml, long long first, int count,
+                                            int G, Live live, __nv_bfloat16* out_grp, float* dst_acc, float* dst_ml,
+                                            long long dst_slot) {
   constexpr int kV = D / 4;  // float4 columns per query head
-  const float* pm = a.part_ml;
+  constexpr int kBatch = 8;
   for (int e = threadIdx.x; e < G * kV; e += blockDim.x) {
     const int q = e / kV, d4 = e - (e / kV) * kV;
     float M = kNegInf, L = 0.f;
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll 4
-    for (int c = c_lo; c <= c_hi; ++c) {
-      if (!all_live && range_start(T, c + 1, nctas) <= range_start(T, c, nctas)) continue;
-      const long long slot = ((long long)g + c) * G + q;
-      const float2 ml = __ldcg(reinterpret_cast<const float2*>(pm) + slot);
-      const float4 v = __ldcg(reinterpret_cast<const float4*>(a.part_acc + slot * D) + d4);
-      const float Mn = fmaxf(M, ml.x);
-      if (Mn == kNegInf) continue;
-      const float fo = ex2(M - Mn), fn = ex2(ml.x - Mn);
-      L = fmaf(L, fo, ml.y * fn);
-      acc.x = fmaf(acc.x, fo, v.x * fn);
-      acc.y = fmaf(acc.y, fo, v.y * fn);
-      acc.z = fmaf(acc.z, fo, v.z * fn);
-      acc.w = fmaf(acc.w, fo, v.w * fn);
-      M = Mn;
+    for (int i0 = 0; i0 < count; i0 += kBatch) {
+      float2 ml[kBatch];
+      float4 v[kBatch];
+#pragma unroll
+      for (int j = 0; j < kBatch; ++j) {
+        const int i = i0 + j;
+        if (i < count && live(i)) {
+          const long long slot = (first + i) * G + q;
+          ml[j] = __ldcg(reinterpret_cast<const float2*>(src_ml) + slot);
+          v[j] = __ldcg(reinterpret_cast<const float4*>(src_acc + slot * D) + d4);
+        } else {
+          ml[j] = make_float2(kNegInf, 0.f);
+          v[j] = make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+      }
+#pragma unroll
+      for (int j = 0; j < kBatch; ++j) {
+        const float Mn = fmaxf(M, ml[j].x);
+        if (Mn == kNegInf) continue;
+        const float fo = ex2(M - Mn), fn = ex2(ml[j].x - Mn);
+        L = fmaf(L, fo, ml[j].y * fn);
+        acc.x = fmaf(acc.x, fo, v[j].x * fn);
+        acc.y = fmaf(acc.y, fo, v[j].y * fn);
+        acc.z = fmaf(acc.z, fo, v[j].z * fn);
+        acc.w = fmaf(acc.w, fo, v[j].w * fn);
+        M = Mn;
+      }
     }
-    const float inv = L > 0.f ? 1.f / L : 0.f;
-    __nv_bfloat162 lo = __floats2bfloat162_rn(acc.x * inv, acc.y * inv);
-    __nv_bfloat162 hi = __floats2bfloat162_rn(acc.z * inv, acc.w * inv);
-    uint2 packed;
-    packed.x = *reinterpret_cast<uint32_t*>(&lo);
-    packed.y = *reinterpret_cast<uint32_t*>(&hi);
-    *reinterpret_cast<uint2*>(out_grp + (int64_t)q * D + d4 * 4) = packed;
+    if (out_grp != nullptr) {
+      const float inv = L > 0.f ? 1.f / L : 0.f;
+      __nv_bfloat162 lo = __floats2bfloat162_rn(acc.x * inv, acc.y * inv);
+      __nv_bfloat162 hi = __floats2bfloat162_rn(acc.z * inv, acc.w * inv);
+      uint2 packed;
+      packed.x = *reinterpret_cast<uint32_t*>(&lo);
+      packed.y = *reinterpret_cast<uint32_t*>(&hi);
+      *reinterpret_cast<uint2*>(out_grp + (int64_t)q * D + d4 * 4) = packed;
+    } else {
+      const long long slot = dst_slot * G + q;
+      reinterpret_cast<float4*>(dst_acc + slot * D)[d4] = acc;
+      if (d4 == 0) reinterpret_cast<float2*>(dst_ml)[slot] = make_float2(M, L);
+    }
   }
 }
 
+// Bumps an arrival counter (thread 0) and tells the whole CTA whether it arrived last; the
+// last arriver resets the counter to 0 for the next launch.  Call after the CTA's partial is
+// written and fenced.
+__device__ __forceinline__ bool arrive_last(uint32_t* counter, int expected, int* s_flag) {
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    const unsigned old = atomicAdd(counter, 1u);
+    *s_flag = old + 1u == (unsigned)expected;
+    if (*s_flag) *counter = 0u;
+  }
+  __syncthreads();
+  const bool last = *s_flag != 0;
+  if (last) __threadfence();
+  return last;
+}
+
 template <int D, int GP, int NS>
-__global__ void __launch_bounds__(kWarps * 32) decode_sk_kernel(const __grid_constant__ CUtensorMap tmap,
+__global__ void __launch_bounds__(kWarps * 32, 2) decode_sk_kernel(const __grid_constant__ CUtensorMap tmap,
                                                                 const __grid_constant__ DecodeArgs a) {
   constexpr int W = kWarps;
   constexpr int kHalves = D / 64;
@@ -447,25 +483,42 @@ __global__ void __launch_bounds__(kWarps * 32) decode_sk_kernel(const __grid_con
       }
     }
     if (!whole) {
-      // publish the partial, count arrivals; the last CTA of the group merges them all
+      // The partial is published; count arrivals.  Up to kFlatMerge contributors: the last
+      // CTA of the group merges them all.  More (long windows at small batch): blocks of
+      // kMergeBlock consecutive contributors are merged by their last arriver into a second-
+      // level partial, and the last of those merges the blocks.
       const int c_lo = cta_of(spre, T, nctas), c_hi = cta_of(spre + sgr.tiles - 1, T, nctas);
       const bool all_live = T >= nctas;  // then no CTA range is empty
+      const int k = c_hi - c_lo + 1;
+      __nv_bfloat16* const out_grp = out + ((int64_t)sgr.s * Hq + sgr.h * G) * D;
       __threadfence();
-      __syncthreads();
-      if (threadIdx.x == 0) {
-        int expected = c_hi - c_lo + 1;
+      if (!all_live || k <= kFlatMerge) {
+        int expected = k;
         if (!all_live) {
           expected = 0;
           for (int c = c_lo; c <= c_hi; ++c) expected += range_start(T, c + 1, nctas) > range_start(T, c, nctas);
         }
-        const unsigned old = atomicAdd(&a.counters[sg], 1u);
-        s_last = old + 1u == (unsigned)expected;
-        if (s_last) a.counters[sg] = 0u;
-      }
-      __syncthreads();
-      if (s_last) {
-        __threadfence();
-        merge_partials<D>(a, sg, c_lo, c_hi, T, nctas, all_live, out + ((int64_t)sgr.s * Hq + sgr.h * G) * D);
+        if (arrive_last(&a.counters[sg], expected, &s_last)) {
+          auto live = [&](int i) {
+            return all_live || range_start(T, c_lo + i + 1, nctas) > range_start(T, c_lo + i, nctas);
+          };
+          merge_slots<D>(a.part_acc, a.part_ml, (long long)sg + c_lo, k, G, live, out_grp, nullptr, nullptr, 0);
+        }
+      } else {
+        auto live = [](int) { return true; };
+        const int nb = (k + kMergeBlock - 1) / kMergeBlock;
+        const int b = (cta - c_lo) / kMergeBlock;
+        const int b_lo = c_lo + b * kMergeBlock;
+        const int b_n = min(kMergeBlock, c_hi - b_lo + 1);
+        const long long slot2 = (long long)sg * a.merge_blocks + b;
+        if (arrive_last(&a.counters1[slot2], b_n, &s_last)) {
+          merge_slots<D>(a.part_acc, a.part_ml, (long long)sg + b_lo, b_n, G, live, nullptr, a.part2_acc,
+                         a.part2_ml, slot2);
+          __threadfence();
+          if (arrive_last(&a.counters[sg], nb, &s_last))
+            merge_slots<D>(a.part2_acc, a.part2_ml, (long long)sg * a.merge_blocks, nb, G, live, out_grp, nullptr,
+                           nullptr, 0);
+        }
       }
     }
     __syncthreads();  // the merge scratch is rewritten by the next segment

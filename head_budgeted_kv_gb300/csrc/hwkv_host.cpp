@@ -146,7 +146,10 @@ struct hwkv_pool {
   void* d_meta = nullptr;
   int32_t* d_tbl = nullptr;
   int32_t* d_err = nullptr;
-  uint32_t* d_counters = nullptr;  // [layers][num_seqs * kv_heads] arrival counters, kept at 0
+  // arrival counters of the tensor-core kernel, all kept at 0 between launches:
+  // [layers][groups] final counters, then [layers][groups][merge_blocks] first-level ones
+  uint32_t* d_counters = nullptr;
+  int counter_merge_blocks = 0;
   std::vector<int32_t> h_tbl;
   int device = 0;
   int num_sms = 0;
@@ -205,18 +208,67 @@ int tc_workers(const hwkv_pool* p, int group) {
   return std::max(1, p->num_sms * std::max(1, per_sm));
 }
 
-// partial slots: CUDA-core kernel one per chunk item; tensor-core kernel one per (group,
-// CTA) pair along the tile line, at most groups + CTAs
-int64_t partial_slots(const hwkv_pool* p, int group) {
-  if (use_tc(p)) return (int64_t)p->g.num_seqs * p->g.kv_heads + tc_workers(p, group);
-  int64_t items = 0;
-  for (const LayerPlan& lp : p->plans)
-    if (lp.multi_chunk) items = std::max<int64_t>(items, lp.items);
-  return items;
+// first-level merge blocks per head for a grid of `workers` CTAs
+int merge_blocks_for(int workers) { return (workers + kMergeBlock - 1) / kMergeBlock + 1; }
+
+int max_tc_workers(const hwkv_pool* p) { return std::max(tc_workers(p, 4), tc_workers(p, 8)); }
+
+// Workspace regions (each 256-byte aligned): partials [slots][G][D] floats, their (m, l)
+// [slots][G][2]; for the tensor-core kernel also the second-level partials and (m, l).
+// Partial slots: CUDA-core kernel one per chunk item; tensor-core kernel one per (group, CTA)
+// pair along the tile line (at most groups + CTAs), second level groups x merge blocks.
+struct WorkspaceLayout {
+  int64_t slots1 = 0, slots2 = 0;
+  uint64_t acc1 = 0, ml1 = 0, acc2 = 0, ml2 = 0, total = 0;
+};
+
+uint64_t align256(uint64_t x) { return (x + 255) & ~uint64_t(255); }
+
+WorkspaceLayout workspace_layout(const hwkv_pool* p, int group) {
+  WorkspaceLayout w;
+  const int64_t groups = (int64_t)p->g.num_seqs * p->g.kv_heads;
+  if (use_tc(p)) {
+    w.slots1 = groups + tc_workers(p, group);
+    w.slots2 = groups * merge_blocks_for(tc_workers(p, group));
+  } else {
+    for (const LayerPlan& lp : p->plans)
+      if (lp.multi_chunk) w.slots1 = std::max<int64_t>(w.slots1, lp.items);
+  }
+  const uint64_t D = (uint64_t)p->g.head_dim;
+  w.acc1 = 0;
+  w.ml1 = align256(w.acc1 + (uint64_t)w.slots1 * group * D * 4);
+  w.acc2 = align256(w.ml1 + (uint64_t)w.slots1 * group * 2 * 4);
+  w.ml2 = align256(w.acc2 + (uint64_t)w.slots2 * group * D * 4);
+  w.total = w.slots1 + w.slots2 > 0 ? align256(w.ml2 + (uint64_t)w.slots2 * group * 2 * 4) : 0;
+  return w;
 }
 
-uint64_t workspace_bytes(const hwkv_pool* p, int group) {
-  return (uint64_t)partial_slots(p, group) * group * (p->g.head_dim + 2) * sizeof(float);
+uint64_t workspace_bytes(const hwkv_pool* p, int group) { return workspace_layout(p, group).total; }
+
+// (Re)allocates the arrival counters for the current grid size, zeroed.
+int ensure_counters(hwkv_pool* p) {
+  const int mb = merge_blocks_for(max_tc_workers(p));
+  if (p->d_counters && mb <= p->counter_merge_blocks) return HWKV_OK;
+  const size_t groups = (size_t)p->g.num_seqs * p->g.kv_heads;
+  const size_t n = (size_t)p->g.layers * groups * (1 + (size_t)mb);
+  uint32_t* c = nullptr;
+  HWKV_CUDA_TRY(cudaMalloc(&c, n * sizeof(uint32_t)), "cudaMalloc of the arrival counters");
+  cudaError_t e = cudaMemset(c, 0, n * sizeof(uint32_t));
+  if (e != cudaSuccess) {
+    cudaFree(c);
+    return fail(HWKV_ERR_CUDA, "cudaMemset of the arrival counters: %s", cudaGetErrorString(e));
+  }
+  if (p->d_counters) {
+    cudaDeviceSynchronize();  // no launch may still use the old counters
+    cudaFree(p->d_counters);
+  }
+  p->d_counters = c;
+  p->counter_merge_blocks = mb;
+  return HWKV_OK;
+}
+
+size_t counter_count(const hwkv_pool* p) {
+  return (size_t)p->g.layers * p->g.num_seqs * p->g.kv_heads * (1 + (size_t)p->counter_merge_blocks);
 }
 
 int check_device(const hwkv_pool* p) {
@@ -316,15 +368,13 @@ int hwkv_pool_create(int layers, int kv_heads, int head_dim, int block_size, con
     return fail(HWKV_ERR_CUDA, "cudaDeviceGetAttribute: %s", cudaGetErrorString(e));
   }
   const size_t tbl_bytes = ((size_t)p->g.total_blocks * sizeof(int32_t) + 255) & ~(size_t)255;
-  const size_t cnt_bytes = (size_t)p->g.layers * p->g.num_seqs * p->g.kv_heads * sizeof(uint32_t);
-  e = cudaMalloc(&p->d_meta, tbl_bytes + 256 + cnt_bytes);
+  e = cudaMalloc(&p->d_meta, tbl_bytes + 256);
   if (e != cudaSuccess) {
     delete p;
     return fail(HWKV_ERR_CUDA, "cudaMalloc of the block table: %s", cudaGetErrorString(e));
   }
   p->d_tbl = static_cast<int32_t*>(p->d_meta);
   p->d_err = reinterpret_cast<int32_t*>(static_cast<char*>(p->d_meta) + tbl_bytes);
-  p->d_counters = reinterpret_cast<uint32_t*>(static_cast<char*>(p->d_meta) + tbl_bytes + 256);
   p->h_tbl.resize((size_t)p->g.total_blocks);
   for (int64_t i = 0; i < p->g.total_blocks; ++i) p->h_tbl[(size_t)i] = (int32_t)i;
 
@@ -338,7 +388,7 @@ int hwkv_pool_create(int layers, int kv_heads, int head_dim, int block_size, con
   if ((e = cudaMemcpyAsync(p->d_tbl, p->h_tbl.data(), (size_t)p->g.total_blocks * sizeof(int32_t),
                            cudaMemcpyHostToDevice, st)) != cudaSuccess)
     return cleanup_fail("upload of the block table", e);
-  if ((e = cudaMemsetAsync(p->d_err, 0, 256 + cnt_bytes, st)) != cudaSuccess) return cleanup_fail("cudaMemsetAsync", e);
+  if ((e = cudaMemsetAsync(p->d_err, 0, 256, st)) != cudaSuccess) return cleanup_fail("cudaMemsetAsync", e);
   if ((e = cudaMemsetAsync(p->dev_pool, 0, p->g.pool_bytes, st)) != cudaSuccess)
     return cleanup_fail("zero-fill of the pool", e);
   if ((e = cudaStreamSynchronize(st)) != cudaSuccess) return cleanup_fail("cudaStreamSynchronize", e);
@@ -362,12 +412,22 @@ int hwkv_pool_create(int layers, int kv_heads, int head_dim, int block_size, con
     if (e != cudaSuccess) return cleanup_fail("cudaFuncSetAttribute", e);
   }
   plan_decode(p);
+  if (p->has_tmap) {
+    const int crc = ensure_counters(p);
+    if (crc != HWKV_OK) {
+      const std::string msg = g_last_error;
+      cudaFree(p->d_meta);
+      delete p;
+      return fail(crc, "%s", msg.c_str());
+    }
+  }
   *out = p;
   return ok();
 }
 
 int hwkv_pool_destroy(hwkv_pool_t p) {
   if (!p) return ok();
+  if (p->d_counters) cudaFree(p->d_counters);
   cudaError_t e = cudaFree(p->d_meta);
   delete p;
   if (e != cudaSuccess) return fail(HWKV_ERR_CUDA, "cudaFree: %s", cudaGetErrorString(e));
@@ -527,10 +587,18 @@ int decode_common(hwkv_pool_t p, int layer, const void* q, int q_heads, float sc
   a.out = out;
   a.lens = lens_dev;
   a.len_add = len_add;
-  const int64_t slots = partial_slots(p, G);
-  a.part_acc = static_cast<float*>(workspace);
-  a.part_ml = workspace ? static_cast<float*>(workspace) + slots * G * g.head_dim : nullptr;
-  a.counters = p->d_counters + (int64_t)layer * g.num_seqs * g.kv_heads;
+  const WorkspaceLayout wl = workspace_layout(p, G);
+  char* ws = static_cast<char*>(workspace);
+  a.part_acc = ws ? reinterpret_cast<float*>(ws + wl.acc1) : nullptr;
+  a.part_ml = ws ? reinterpret_cast<float*>(ws + wl.ml1) : nullptr;
+  a.part2_acc = ws ? reinterpret_cast<float*>(ws + wl.acc2) : nullptr;
+  a.part2_ml = ws ? reinterpret_cast<float*>(ws + wl.ml2) : nullptr;
+  if (tc) {
+    const int64_t groups = (int64_t)g.num_seqs * g.kv_heads;
+    a.merge_blocks = merge_blocks_for(tc_workers(p, G));
+    a.counters = p->d_counters + (int64_t)layer * groups;
+    a.counters1 = p->d_counters + (int64_t)g.layers * groups + (int64_t)layer * groups * p->counter_merge_blocks;
+  }
   a.scale_log2 = scale * 1.4426950408889634f;
   a.group = G;
   a.split_tokens = lp.split;
@@ -586,6 +654,10 @@ int hwkv_set_decode_config(hwkv_pool_t p, int split_tokens, int workers, int ker
   p->workers_override = workers;
   p->kernel_choice = kernel;
   plan_decode(p);
+  if (p->has_tmap) {
+    const int rc = ensure_counters(p);
+    if (rc != HWKV_OK) return rc;
+  }
   return ok();
 }
 
@@ -607,8 +679,8 @@ int hwkv_check_device_errors(hwkv_pool_t p, void* stream, int32_t* out_bits) {
   if (out_bits) *out_bits = bits;
   if (bits != 0) {
     // an aborted launch can leave arrival counters behind: start the next launch from zero
-    HWKV_CUDA_TRY(cudaMemset(p->d_counters, 0, (size_t)p->g.layers * p->g.num_seqs * p->g.kv_heads * sizeof(uint32_t)),
-                  "reset of the arrival counters");
+    if (p->d_counters)
+      HWKV_CUDA_TRY(cudaMemset(p->d_counters, 0, counter_count(p) * sizeof(uint32_t)), "reset of the arrival counters");
     return fail(HWKV_ERR_DEVICE_CHECK, "device error bits 0x%x", bits);
   }
   return ok();

@@ -9,6 +9,7 @@
 namespace hwkv {
 
 constexpr int kMaxKvHeads = 32;
+constexpr int kMergeBlock = 16;  // CTAs whose partials one first-level merge folds
 constexpr int kMaxGroup = 8;
 
 // Geometry of one layer, passed by value to every kernel of that layer.
@@ -57,6 +58,10 @@ struct DecodeArgs {
   float* part_acc;         // [slots][G][D]   unnormalised split accumulators
   float* part_ml;          // [slots][G][2]   (running max in log2 units, sum of weights)
   uint32_t* counters;      // [B*H] arrival counters of this layer (tensor-core kernel), all 0
+  uint32_t* counters1;     // [B*H][merge_blocks] first-level arrival counters, all 0
+  float* part2_acc;        // [B*H*merge_blocks][G][D] second-level partials
+  float* part2_ml;         // [B*H*merge_blocks][G][2]
+  int32_t merge_blocks;    // first-level merge blocks per head: ceil(CTAs / kMergeBlock) + 1
   float scale_log2;        // scale * log2(e)
   int32_t group;           // G = Hq / H
   int32_t split_tokens;    // CUDA-core kernel: tokens per split-K chunk (power of two)
