@@ -315,7 +315,22 @@ def run_hwkv(args, cfg):
     lens_all = [(prefill + i + 1).contiguous() for i in range(n_steps)]
     torch.cuda.synchronize()
 
+    graph = None
+    launches_per_step = None
+    if args.graph:
+        from head_budgeted_kv_gb300.graph import DecodeStepGraph
+        before = hw.binding.hwkv_kernel_launches()
+        graph = DecodeStepGraph(pool, cfg.scale, cfg.q_heads, pos_all[0], fused=fused)
+        launches_per_step = hw.binding.hwkv_kernel_launches() - before  # kernels recorded per step
+
     def run_step(i, ev=None):
+        if graph is not None and ev is None:
+            # the step's inputs land in the graph's static buffers; positions advance in-graph
+            graph.q.copy_(qs[i], non_blocking=True)
+            graph.k_new.copy_(kns[i], non_blocking=True)
+            graph.v_new.copy_(vns[i], non_blocking=True)
+            graph.replay()
+            return
         for l in range(cfg.layers):
             if fused:
                 if ev is not None:
@@ -352,6 +367,8 @@ def run_hwkv(args, cfg):
     clocks.mark_end()
     barrier(ws)
     launches = hw.binding.hwkv_kernel_launches() - launches0
+    if graph is not None:
+        launches = launches_per_step * args.steps
     clock_info = clocks.stop() if rank == 0 else None
     local_ms = t_start.elapsed_time(t_end)
     bits = pool.check_device_errors()
@@ -401,6 +418,14 @@ def run_hwkv(args, cfg):
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record(stream)
     for k in range(e2e_total):
+        if graph is not None:
+            graph.q.copy_(h_q[k], non_blocking=True)
+            graph.k_new.copy_(h_k[k], non_blocking=True)
+            graph.v_new.copy_(h_v[k], non_blocking=True)
+            graph.pos.copy_(h_pos[k], non_blocking=True)
+            graph.replay()
+            h_out.copy_(graph.out, non_blocking=True)
+            continue
         d_q.copy_(h_q[k], non_blocking=True)
         d_k.copy_(h_k[k], non_blocking=True)
         d_v.copy_(h_v[k], non_blocking=True)
@@ -448,7 +473,8 @@ def run_hwkv(args, cfg):
         "config": {"workload": workload_desc(cfg), "global_batch": cfg.batch * ws,
                    "seq_len": max(cfg.prefill), "parallelism": "replicas" if ws > 1 else "single",
                    "l2": f"inputs larger than L2: {step_bytes / 1e9:.2f} GB of resident KV read per step",
-                   "path": args.path, "kernel": ["auto", "tensor", "simt"][args.kernel],
+                   "path": args.path + (" (CUDA graph per step)" if graph is not None else ""),
+                   "kernel": ["auto", "tensor", "simt"][args.kernel],
                    "workers": args.workers or "auto", "split_tokens": args.split or "auto"},
         "resident_kv_gbs": step_bytes / (max_ms / args.steps / 1e3) / 1e9,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
@@ -480,6 +506,7 @@ def main(argv=None):
     p.add_argument("--split", type=int, default=0, help="CUDA-core kernel: tokens per split-K chunk")
     p.add_argument("--workers", type=int, default=0, help="tensor-core kernel: CTAs of the persistent grid")
     p.add_argument("--path", choices=["fused", "split"], default="fused")
+    p.add_argument("--graph", action="store_true", help="replay each decode step as one captured CUDA graph")
     p.add_argument("--kernel", type=int, default=0)
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--cpu-budget", type=float, default=12.0)
