@@ -23,6 +23,10 @@ HWKV_ERR_CUDA = -4
 HWKV_ERR_DEVICE_CHECK = -5
 HWKV_ERR_UNSUPPORTED = -6
 HWKV_ERR_WORKSPACE_TOO_SMALL = -7
+HWKV_ERR_BUDGET = -8
+
+DISTORTION_FN = ctypes.CFUNCTYPE(ctypes.c_double, ctypes.c_void_p, ctypes.c_int, ctypes.POINTER(ctypes.c_int32),
+                                 ctypes.POINTER(ctypes.c_int32))
 
 HWKV_F32 = 0
 HWKV_BF16 = 1
@@ -56,6 +60,7 @@ SIGNATURES = [
     ("hwkv_decode_attn_noalloc", _i, [_vp, _i, _vp, _i, ctypes.c_float, _vp, _vp, _vp]),
     ("hwkv_set_decode_config", _i, [_vp, _i, _i, _i]),
     ("hwkv_kernel_launches", _i, [_c_u64p]),
+    ("hwkv_seqcalib", _i, [_i, _i, _i, _i, _i, _i, _i, _c_i32p, DISTORTION_FN, _vp, _u64, _c_i32p, _c_i32p, _c_u64p]),
     ("hwkv_check_device_errors", _i, [_vp, _vp, _c_i32p]),
 ]
 
@@ -241,6 +246,43 @@ def hwkv_decode_attn_noalloc(pool: int, layer: int, q: torch.Tensor, scale: floa
 
 def hwkv_set_decode_config(pool: int, split_tokens: int = 0, workers: int = 0, kernel: int = HWKV_KERNEL_AUTO):
     _check(load().hwkv_set_decode_config(pool, split_tokens, workers, kernel))
+
+
+def hwkv_seqcalib(candidates, distortion, budget_bytes: int, head_dim: int, block_size: int, num_seqs: int,
+                  dtype):
+    """SeqCalib greedy over candidate window vectors.
+
+    candidates: int array [layers][num_candidates][kv_heads].
+    distortion: either a float array [layers][num_candidates] (a fixed table) or a callable
+    (layer, windows[kv_heads], chosen[layer][kv_heads]) -> float.
+    Returns (windows [layers][kv_heads], choice [layers], pool bytes).
+    """
+    cand = np.ascontiguousarray(np.asarray(candidates, dtype=np.int32))
+    L, C, H = cand.shape
+    if callable(distortion):
+        def cb(_user, layer, w_ptr, chosen_ptr):
+            w = np.ctypeslib.as_array(w_ptr, shape=(H,)).copy()
+            chosen = np.ctypeslib.as_array(chosen_ptr, shape=(L * H,)).reshape(L, H)[:layer].copy()
+            return float(distortion(layer, w, chosen))
+    else:
+        table = np.asarray(distortion, dtype=np.float64)
+        if table.shape != (L, C):
+            raise ValueError("distortion table must be [layers][num_candidates]")
+
+        base = cand.ctypes.data
+
+        def cb(_user, layer, w_ptr, chosen_ptr):
+            # the library passes a pointer into `cand`: its offset names the candidate
+            row = (ctypes.cast(w_ptr, ctypes.c_void_p).value - base) // (4 * H)
+            return float(table[layer, row % C])
+    fn = DISTORTION_FN(cb)
+    out_w = np.zeros((L, H), dtype=np.int32)
+    choice = np.zeros(L, dtype=np.int32)
+    nbytes = ctypes.c_uint64(0)
+    _check(load().hwkv_seqcalib(L, H, head_dim, block_size, num_seqs, _dtype_code(dtype), C,
+                                cand.ctypes.data_as(_c_i32p), fn, None, int(budget_bytes),
+                                out_w.ctypes.data_as(_c_i32p), choice.ctypes.data_as(_c_i32p), ctypes.byref(nbytes)))
+    return out_w, choice, nbytes.value
 
 
 def hwkv_kernel_launches() -> int:

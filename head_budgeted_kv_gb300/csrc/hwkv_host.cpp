@@ -324,6 +324,7 @@ const char* hwkv_status_string(int status) {
     case HWKV_ERR_DEVICE_CHECK: return "HWKV_ERR_DEVICE_CHECK";
     case HWKV_ERR_UNSUPPORTED: return "HWKV_ERR_UNSUPPORTED";
     case HWKV_ERR_WORKSPACE_TOO_SMALL: return "HWKV_ERR_WORKSPACE_TOO_SMALL";
+    case HWKV_ERR_BUDGET: return "HWKV_ERR_BUDGET";
     default: return "HWKV_ERR_UNKNOWN";
   }
 }
@@ -658,6 +659,50 @@ int hwkv_set_decode_config(hwkv_pool_t p, int split_tokens, int workers, int ker
     const int rc = ensure_counters(p);
     if (rc != HWKV_OK) return rc;
   }
+  return ok();
+}
+
+int hwkv_seqcalib(int layers, int kv_heads, int head_dim, int block_size, int num_seqs, int dtype,
+                  int num_candidates, const int32_t* candidates, hwkv_distortion_fn distortion, void* user,
+                  uint64_t budget_bytes, int32_t* out_windows, int32_t* out_choice, uint64_t* out_bytes) {
+  if (num_candidates < 1) return fail(HWKV_ERR_INVALID_ARG, "num_candidates must be >= 1");
+  if (!candidates || !distortion || !out_windows) return fail(HWKV_ERR_INVALID_ARG, "NULL argument");
+  // every candidate must be a valid window vector; its cost is the one-layer pool footprint
+  std::vector<uint64_t> cost((size_t)layers * num_candidates);
+  for (int l = 0; l < layers; ++l) {
+    for (int c = 0; c < num_candidates; ++c) {
+      const int32_t* w = candidates + ((size_t)l * num_candidates + c) * kv_heads;
+      Geometry g;
+      const int rc = plan_geometry(1, kv_heads, head_dim, block_size, w, num_seqs, dtype, &g);
+      if (rc != HWKV_OK) return rc;
+      cost[(size_t)l * num_candidates + c] = g.pool_bytes;
+    }
+  }
+  std::vector<int32_t> chosen((size_t)layers * kv_heads);
+  uint64_t remaining = budget_bytes, total = 0;
+  for (int l = 0; l < layers; ++l) {
+    int best = -1;
+    double best_d = std::numeric_limits<double>::infinity();
+    for (int c = 0; c < num_candidates; ++c) {
+      const int32_t* w = candidates + ((size_t)l * num_candidates + c) * kv_heads;
+      const double d = distortion(user, l, w, chosen.data());
+      if (cost[(size_t)l * num_candidates + c] <= remaining && d < best_d) {
+        best = c;
+        best_d = d;
+      }
+    }
+    if (best < 0)
+      return fail(HWKV_ERR_BUDGET, "no candidate window vector of layer %d fits the remaining budget of %llu bytes", l,
+                  (unsigned long long)remaining);
+    const uint64_t cb = cost[(size_t)l * num_candidates + best];
+    remaining -= cb;
+    total += cb;
+    std::memcpy(&chosen[(size_t)l * kv_heads], candidates + ((size_t)l * num_candidates + best) * kv_heads,
+                sizeof(int32_t) * (size_t)kv_heads);
+    if (out_choice) out_choice[l] = best;
+  }
+  std::memcpy(out_windows, chosen.data(), sizeof(int32_t) * chosen.size());
+  if (out_bytes) *out_bytes = total;
   return ok();
 }
 

@@ -54,6 +54,7 @@ extern "C" {
 #define HWKV_ERR_DEVICE_CHECK (-5)
 #define HWKV_ERR_UNSUPPORTED (-6)
 #define HWKV_ERR_WORKSPACE_TOO_SMALL (-7)
+#define HWKV_ERR_BUDGET (-8)
 
 /* element types of the pool and of every tensor passed with it */
 #define HWKV_F32 0
@@ -206,6 +207,27 @@ int hwkv_set_decode_config(hwkv_pool_t pool, int split_tokens, int workers, int 
 /* Number of kernels this library has launched in this process (all pools, all devices).
  * Lets a caller count the launches inside a timed region. */
 int hwkv_kernel_launches(uint64_t* out);
+
+/* Distortion of a candidate window vector, supplied by the caller (e.g. measured with a
+ * model).  windows: [kv_heads] candidate of `layer`; chosen: [layer][kv_heads] window vectors
+ * already chosen for layers 0 .. layer-1 (execution order), so the distortion may depend on
+ * them.  Return the distortion; smaller is better. */
+typedef double (*hwkv_distortion_fn)(void* user, int layer, const int32_t* windows, const int32_t* chosen);
+
+/* Host-side policy search of "HeadWiseKV: Budgeted Per-Head Cache Residency for Hybrid
+ * Long-Context Language Models", section "SeqCalib": layers are visited in execution order;
+ * for each layer the candidate window vector of smallest distortion whose cost fits the
+ * remaining budget is chosen (ties: the first such candidate), and its cost is taken off the
+ * budget.  The cost of a vector is its exact pool footprint, the bytes hwkv_pool_bytes predicts:
+ * num_seqs * sum_h ceil(w_h / block_size) * block_size * head_dim * 2 * eb.
+ *   candidates: host int32 [layers][num_candidates][kv_heads], every window >= 1.
+ *   out_windows: host int32 [layers][kv_heads] (may be the windows argument of pool_create);
+ *   out_choice: host int32 [layers] chosen candidate index; out_bytes: total pool bytes.
+ * Pure host, needs no GPU.  Errors: HWKV_ERR_INVALID_ARG, HWKV_ERR_UNSUPPORTED, HWKV_ERR_BUDGET
+ * (no candidate of some layer fits what is left of the budget; the message names the layer). */
+int hwkv_seqcalib(int layers, int kv_heads, int head_dim, int block_size, int num_seqs, int dtype,
+                  int num_candidates, const int32_t* candidates, hwkv_distortion_fn distortion, void* user,
+                  uint64_t budget_bytes, int32_t* out_windows, int32_t* out_choice, uint64_t* out_bytes);
 
 /* Synchronises `stream`, reads and clears the device error word.  *out_bits receives the
  * HWKV_DEVERR_* bits seen since the last call.  Returns HWKV_ERR_DEVICE_CHECK if any bit

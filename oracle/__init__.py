@@ -7,7 +7,9 @@ Plain, slow CPU restatement of what the pages fix, written from
   keeps a static window of its most recent tokens, the footprint is known before serving,
   and the runtime materialises the residency rather than masking a full cache;
 * same page, section "Grouped-Cache Runtime" -- a paged block table gives each head
-  ceil(window / block_size) blocks.
+  ceil(window / block_size) blocks;
+* same page, section "SeqCalib" -- the layer-by-layer greedy choice of window vectors under
+  a memory budget (``seqcalib_greedy``).
 
 Where the pages are silent the oracle takes these readings:
 
@@ -267,3 +269,36 @@ def widen(raw: np.ndarray) -> np.ndarray:
         return (raw.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
     return raw.astype(np.float64)
 
+
+
+# ------------------------------------------------------------------------------------
+# SeqCalib (section "SeqCalib"): greedy, layer by layer in execution order
+# ------------------------------------------------------------------------------------
+def layer_cost(window_vector, num_seqs: int, head_dim: int, block_size: int, elem_bytes: int) -> int:
+    """R_i(w_i): bytes one layer's window vector occupies in the pool."""
+    return pool_bytes([list(window_vector)], num_seqs, head_dim, block_size, elem_bytes)
+
+
+def seqcalib_greedy(candidates, distortion_fn, budget: int, cost_fn):
+    """Walks the layers in order; for each, among its candidate window vectors, keeps the one
+    of smallest distortion (first one on ties) whose cost fits what is left of the budget,
+    then charges its cost.  ``distortion_fn(layer, w, chosen_so_far)`` may depend on the
+    vectors chosen for the earlier layers; ``cost_fn(layer, w)`` is the layer's memory.
+    Returns (chosen vectors, chosen indices, total cost).  Raises ValueError when no candidate
+    of a layer fits (the page's pseudocode would carry ``None`` on)."""
+    policies, picks, remaining, total = [], [], budget, 0
+    for layer, feasible in enumerate(candidates):
+        best_w, best_i, min_distort = None, None, float("inf")
+        for i, w in enumerate(feasible):
+            d = distortion_fn(layer, list(w), [list(p) for p in policies])
+            c = cost_fn(layer, list(w))
+            if c <= remaining and d < min_distort:
+                best_w, best_i, min_distort = list(w), i, d
+        if best_w is None:
+            raise ValueError(f"no candidate of layer {layer} fits the remaining budget {remaining}")
+        policies.append(best_w)
+        picks.append(best_i)
+        cost = cost_fn(layer, best_w)
+        remaining -= cost
+        total += cost
+    return policies, picks, total
