@@ -174,10 +174,32 @@ def append_bytes(cfg) -> int:
     return 2 * cfg.batch * cfg.kv_heads * 2 * cfg.head_dim * cfg.elem_bytes
 
 
+def mean_step_bytes(cfg, first_step: int, steps: int) -> float:
+    """Algorithmic bytes of one decode step (all layers), averaged over the given steps."""
+    total = 0
+    for k in range(steps):
+        lens = [cfg.prefill[s] + first_step + k + 1 for s in range(cfg.batch)]
+        total += sum(attention_bytes(cfg, l, lens) for l in range(cfg.layers))
+    return total / steps + cfg.layers * append_bytes(cfg)
+
+
 def materialize_bytes(cfg, layer: int) -> int:
     w = np.asarray(cfg.windows[layer], dtype=np.int64)
     L = np.asarray(cfg.prefill, dtype=np.int64)
     return 2 * int(np.minimum(w[None, :], L[:, None]).sum()) * 2 * cfg.head_dim * cfg.elem_bytes
+
+
+def bench_config(cfg, args, world_size: int, step_bytes=None) -> dict:
+    """The ``config`` object of the JSON line; identical for both arms."""
+    c = {"workload": workload_desc(cfg), "global_batch": cfg.batch * world_size, "seq_len": max(cfg.prefill),
+         "parallelism": "replicas" if world_size > 1 else "single",
+         "path": args.path + (" (CUDA graph per step)" if args.graph else ""),
+         "kernel": ["auto", "tensor", "simt"][args.kernel],
+         "workers": args.workers or "auto", "split_tokens": args.split or "auto"}
+    if step_bytes is None:
+        step_bytes = mean_step_bytes(cfg, args.warmup, args.steps)
+    c["l2"] = f"inputs larger than L2: {step_bytes / 1e9:.2f} GB of resident KV read per step"
+    return c
 
 
 def workload_desc(cfg) -> str:
@@ -253,8 +275,7 @@ def run_reference(args, cfg):
         "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": ws,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": step_s * 1e3, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": workload_desc(cfg), "global_batch": cfg.batch, "seq_len": max(cfg.prefill),
-                   "parallelism": "replicas"},
+        "config": bench_config(cfg, args, ws),
         "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": threads, "kind": "oracle", "sample": sample},
         "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
@@ -376,11 +397,7 @@ def run_hwkv(args, cfg):
         raise RuntimeError(f"device error bits {bits:#x} in the timed region")
 
     # algorithmic bytes of the timed steps (resident K/V + q + out, plus the appends)
-    step_bytes = 0
-    for k in range(args.steps):
-        lens = [cfg.prefill[s] + args.warmup + k + 1 for s in range(cfg.batch)]
-        step_bytes += sum(attention_bytes(cfg, l, lens) for l in range(cfg.layers))
-    step_bytes = step_bytes / args.steps + cfg.layers * append_bytes(cfg)
+    step_bytes = mean_step_bytes(cfg, args.warmup, args.steps)
 
     # ---- dominant kernel, per launch: the same steps again with events around each launch
     # of the decode kernel (fused: the whole per-layer step; split: decode only) ----
@@ -470,12 +487,7 @@ def run_hwkv(args, cfg):
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": ws, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": max_ms / args.steps, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": cfg.dtype, "data": "synthetic",
-        "config": {"workload": workload_desc(cfg), "global_batch": cfg.batch * ws,
-                   "seq_len": max(cfg.prefill), "parallelism": "replicas" if ws > 1 else "single",
-                   "l2": f"inputs larger than L2: {step_bytes / 1e9:.2f} GB of resident KV read per step",
-                   "path": args.path + (" (CUDA graph per step)" if graph is not None else ""),
-                   "kernel": ["auto", "tensor", "simt"][args.kernel],
-                   "workers": args.workers or "auto", "split_tokens": args.split or "auto"},
+        "config": bench_config(cfg, args, ws, step_bytes),
         "resident_kv_gbs": step_bytes / (max_ms / args.steps / 1e3) / 1e9,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
                      "traffic": traffic, "peak_kind": peak_kind,
