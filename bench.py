@@ -507,6 +507,87 @@ def run_hwkv(args, cfg):
     print(json.dumps(line), flush=True)
 
 
+# --------------------------------------------------------------------------------------
+# chunked prefill (hwkv_prefill_attn): not the default line
+# --------------------------------------------------------------------------------------
+def prefill_flops(cfg, layer: int, pos0, n: int) -> int:
+    """Algorithmic FLOPs of one prefill launch: every query head of every chunk token does
+    2*D (QK) + 2*D (PV) per key of its window [max(0, p+1-w), p]."""
+    total = 0
+    G, D = cfg.group, cfg.head_dim
+    for s in range(cfg.batch):
+        for h in range(cfg.kv_heads):
+            w = int(cfg.windows[layer][h])
+            p = np.arange(int(pos0[s]), int(pos0[s]) + n, dtype=np.int64)
+            total += int(np.minimum(w, p + 1).sum()) * G * 4 * D
+    return total
+
+
+def run_prefill(args, cfg):
+    import torch
+    import workloads
+    import head_budgeted_kv_gb300 as hw
+    ws, rank, local = dist_env()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    hw.binding.load()
+    stream = torch.cuda.current_stream(dev)
+    wl = workloads.Workload(cfg, device=dev)
+    pool = hw.Pool(cfg.layers, cfg.kv_heads, cfg.head_dim, cfg.block_size, cfg.windows_array(), cfg.batch,
+                   cfg.torch_dtype, q_heads=cfg.q_heads, device=dev)
+    prefill = torch.tensor(cfg.prefill, dtype=torch.int32, device=dev)
+    for l in range(cfg.layers):
+        K, V = wl.prefill_layer(l, dev)
+        pool.materialize(l, K, V, prefill)
+        del K, V
+    n = args.chunk
+    nt = torch.full((cfg.batch,), n, dtype=torch.int32, device=dev)
+    chunks = [wl.chunk_inputs(l, 0, n, dev) for l in range(cfg.layers)]
+    outs = [torch.empty_like(c[0]) for c in chunks]
+    total = args.warmup + args.steps
+    pos = [(prefill + i * n).contiguous() for i in range(total)]
+    torch.cuda.synchronize()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    ms, flops = 0.0, 0
+    for i in range(total):
+        k = i - args.warmup
+        if k >= 0:
+            ev[k][0].record(stream)
+        for l in range(cfg.layers):
+            q, kk, vv = chunks[l]
+            pool.prefill(l, q, cfg.scale, kk, vv, pos[i], nt, out=outs[l])
+        if k >= 0:
+            ev[k][1].record(stream)
+            flops += sum(prefill_flops(cfg, l, [cfg.prefill[s] + i * n for s in range(cfg.batch)], n)
+                         for l in range(cfg.layers))
+    torch.cuda.synchronize()
+    for a, b in ev:
+        ms += a.elapsed_time(b)
+    bits = pool.check_device_errors()
+    if bits:
+        raise RuntimeError(f"device error bits {bits:#x}")
+    pool.close()
+    if rank != 0:
+        return
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            peak, kind = float(json.load(f)["bf16_tflops"]), "measured (burst, cuBLAS bf16)"
+    except (OSError, KeyError, ValueError):
+        peak, kind = 1900.0, "fallback"
+    tflops = flops / (ms / 1e3) / 1e12
+    tokens = cfg.batch * n * args.steps
+    line = {"metric": "chunked prefill tokens/s (windowed attention + ring append, all layers)",
+            "value": tokens / (ms / 1e3), "unit": "tokens/s", "n_gpus": ws, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms / args.steps, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": cfg.dtype, "data": "synthetic",
+            "config": {"workload": workload_desc(cfg) + f", chunk {n} tokens per sequence on top of the context",
+                       "global_batch": cfg.batch, "seq_len": max(cfg.prefill)},
+            "roofline": {"bound": "tensor", "achieved": tflops, "peak": peak, "unit": "TFLOP/s",
+                         "frac": tflops / peak, "traffic": None, "peak_kind": kind,
+                         "kernel": "prefill_kernel (mma.sync bf16) + chunk append, one pair per layer"}}
+    print(json.dumps(line), flush=True)
+
+
 def main(argv=None):
     p = argparse.ArgumentParser()
     p.add_argument("--gpus", type=int, default=1)
@@ -519,6 +600,8 @@ def main(argv=None):
     p.add_argument("--workers", type=int, default=0, help="tensor-core kernel: CTAs of the persistent grid")
     p.add_argument("--path", choices=["fused", "split"], default="fused")
     p.add_argument("--graph", action="store_true", help="replay each decode step as one captured CUDA graph")
+    p.add_argument("--mode", choices=["decode", "prefill"], default="decode")
+    p.add_argument("--chunk", type=int, default=2048, help="prefill mode: tokens per sequence per chunk")
     p.add_argument("--kernel", type=int, default=0)
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--cpu-budget", type=float, default=12.0)
@@ -531,6 +614,8 @@ def main(argv=None):
         cfg = cfg.with_layers(args.layers)
     if args.impl == "reference":
         run_reference(args, cfg)
+    elif args.mode == "prefill":
+        run_prefill(args, cfg)
     else:
         run_hwkv(args, cfg)
 

@@ -20,15 +20,16 @@ from .binding import (HWKV_BF16, HWKV_F32, HWKV_KERNEL_AUTO, HWKV_KERNEL_SIMT, H
                       hwkv_abi_version, hwkv_append, hwkv_append_decode_attn, hwkv_block_table,
                       hwkv_check_device_errors, hwkv_kernel_launches,
                       hwkv_decode_attn, hwkv_decode_workspace_bytes, hwkv_materialize, hwkv_pool_bytes,
-                      hwkv_pool_create, hwkv_pool_destroy, hwkv_pool_geometry, hwkv_set_block_table,
-                      hwkv_set_decode_config)
+                      hwkv_pool_create, hwkv_pool_destroy, hwkv_pool_geometry, hwkv_prefill_attn,
+                      hwkv_set_block_table, hwkv_set_decode_config)
 
 __all__ = [
     "Pool", "HwkvError", "binding", "HWKV_F32", "HWKV_BF16", "HWKV_KERNEL_AUTO", "HWKV_KERNEL_TENSOR",
     "HWKV_KERNEL_SIMT", "hwkv_abi_version", "hwkv_append", "hwkv_append_decode_attn", "hwkv_block_table",
     "hwkv_check_device_errors", "hwkv_kernel_launches",
     "hwkv_decode_attn", "hwkv_decode_workspace_bytes", "hwkv_materialize", "hwkv_pool_bytes", "hwkv_pool_create",
-    "hwkv_pool_destroy", "hwkv_pool_geometry", "hwkv_set_block_table", "hwkv_set_decode_config",
+    "hwkv_pool_destroy", "hwkv_pool_geometry", "hwkv_prefill_attn", "hwkv_set_block_table",
+    "hwkv_set_decode_config",
 ]
 
 
@@ -98,6 +99,13 @@ class Pool:
             self.q_heads = q.shape[1]
             self._size_workspace()
         hwkv_append_decode_attn(self.handle, layer, q, scale, k_new, v_new, pos, out, self.workspace, stream)
+        return out
+
+    def prefill(self, layer: int, q, scale: float, k_new, v_new, pos, n, out=None, stream=None):
+        """Chunked prefill: q [B][n_max][Hq][D], k_new/v_new [B][n_max][Hkv][D]; pos, n int32 [B]."""
+        if out is None:
+            out = torch.zeros_like(q)
+        hwkv_prefill_attn(self.handle, layer, q, scale, k_new, v_new, pos, n, out, stream)
         return out
 
     def check_device_errors(self, stream=None) -> int:

@@ -17,7 +17,7 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(BUILD, "libhwkv.so")
 
-SOURCES = ("hwkv_host.cpp", "hwkv_copy.cu", "hwkv_decode_simt.cu", "hwkv_decode_tc.cu", "hwkv_noalloc.cu")
+SOURCES = ("hwkv_host.cpp", "hwkv_copy.cu", "hwkv_decode_simt.cu", "hwkv_decode_tc.cu", "hwkv_noalloc.cu", "hwkv_prefill.cu")
 HEADERS = (os.path.join(CSRC, "hwkv_internal.h"), os.path.join(CSRC, "hwkv_device.cuh"), os.path.join(INCLUDE, "hwkv.h"))
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-I", INCLUDE, "-I", CSRC]

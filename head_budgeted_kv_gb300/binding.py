@@ -58,6 +58,7 @@ SIGNATURES = [
     ("hwkv_decode_attn", _i, [_vp, _i, _vp, _i, ctypes.c_float, _vp, _vp, _vp, _u64, _vp]),
     ("hwkv_append_decode_attn", _i, [_vp, _i, _vp, _i, ctypes.c_float, _vp, _vp, _vp, _vp, _vp, _u64, _vp]),
     ("hwkv_decode_attn_noalloc", _i, [_vp, _i, _vp, _i, ctypes.c_float, _vp, _vp, _vp]),
+    ("hwkv_prefill_attn", _i, [_vp, _i, _vp, _i, ctypes.c_float, _vp, _vp, _i, _vp, _vp, _vp, _vp]),
     ("hwkv_set_decode_config", _i, [_vp, _i, _i, _i]),
     ("hwkv_kernel_launches", _i, [_c_u64p]),
     ("hwkv_seqcalib", _i, [_i, _i, _i, _i, _i, _i, _i, _c_i32p, DISTORTION_FN, _vp, _u64, _c_i32p, _c_i32p, _c_u64p]),
@@ -242,6 +243,16 @@ def hwkv_decode_attn_noalloc(pool: int, layer: int, q: torch.Tensor, scale: floa
         raise ValueError("q and out must be contiguous")
     _check(load().hwkv_decode_attn_noalloc(pool, layer, _ptr(q), q.shape[1], float(scale), _ptr(lens), _ptr(out),
                                            _stream_ptr(stream)))
+
+
+def hwkv_prefill_attn(pool: int, layer: int, q: torch.Tensor, scale: float, k_new: torch.Tensor, v_new: torch.Tensor,
+                      pos: torch.Tensor, n: torch.Tensor, out: torch.Tensor, stream=None):
+    """q, out: [B][n_max][Hq][D]; k_new, v_new: [B][n_max][Hkv][D]; pos, n: int32 [B] on the device."""
+    for t in (q, k_new, v_new, out):
+        if not t.is_contiguous():
+            raise ValueError("prefill tensors must be contiguous")
+    _check(load().hwkv_prefill_attn(pool, layer, _ptr(q), q.shape[2], float(scale), _ptr(k_new), _ptr(v_new),
+                                    q.shape[1], _ptr(pos), _ptr(n), _ptr(out), _stream_ptr(stream)))
 
 
 def hwkv_set_decode_config(pool: int, split_tokens: int = 0, workers: int = 0, kernel: int = HWKV_KERNEL_AUTO):

@@ -641,6 +641,73 @@ int hwkv_append_decode_attn(hwkv_pool_t p, int layer, const void* q, int q_heads
   return decode_common(p, layer, q, q_heads, scale, pos_dev, 1, k_new, v_new, out, workspace, ws_bytes, stream);
 }
 
+int hwkv_prefill_attn(hwkv_pool_t p, int layer, const void* q, int q_heads, float scale, const void* k_new,
+                      const void* v_new, int n_max, const int32_t* pos_dev, const int32_t* n_dev, void* out,
+                      void* stream) {
+  if (!p) return fail(HWKV_ERR_INVALID_ARG, "pool is NULL");
+  const Geometry& g = p->g;
+  if (layer < 0 || layer >= g.layers) return fail(HWKV_ERR_INVALID_ARG, "layer %d out of range", layer);
+  if (!tc_eligible(p)) return fail(HWKV_ERR_UNSUPPORTED, "prefill needs a bf16 pool with block_size % 16 == 0");
+  if (q_heads < g.kv_heads || q_heads % g.kv_heads != 0)
+    return fail(HWKV_ERR_UNSUPPORTED, "q_heads must be a multiple of kv_heads");
+  const int G = q_heads / g.kv_heads;
+  if (G != 1 && G != 2 && G != 4 && G != 8) return fail(HWKV_ERR_UNSUPPORTED, "prefill supports GQA groups 1, 2, 4, 8");
+  if (!(scale == scale) || scale == std::numeric_limits<float>::infinity() ||
+      scale == -std::numeric_limits<float>::infinity())
+    return fail(HWKV_ERR_INVALID_ARG, "scale must be finite");
+  if (n_max < 1) return fail(HWKV_ERR_INVALID_ARG, "n_max must be >= 1");
+  if ((int64_t)g.num_seqs * n_max > kInt32Max) return fail(HWKV_ERR_UNSUPPORTED, "num_seqs * n_max must be below 2^31");
+  if (!q || !k_new || !v_new || !out || !pos_dev || !n_dev) return fail(HWKV_ERR_INVALID_ARG, "NULL tensor argument");
+  if (!aligned(q, 16) || !aligned(k_new, 16) || !aligned(v_new, 16) || !aligned(out, 16) || !aligned(pos_dev, 4) ||
+      !aligned(n_dev, 4))
+    return fail(HWKV_ERR_ALIGNMENT, "tensors must be 16-byte aligned, lengths 4-byte aligned");
+  int rc = check_device(p);
+  if (rc != HWKV_OK) return rc;
+  PFN_cuTensorMapEncodeTiled_v12000 encode = tensor_map_encoder();
+  if (!encode) return fail(HWKV_ERR_CUDA, "cuTensorMapEncodeTiled is unavailable");
+  // the chunk as a 3-D tensor (head_dim, kv_heads, seq * n_max + row): a box of 16 rows of one head
+  alignas(64) CUtensorMap kmap, vmap;
+  const cuuint64_t dims[3] = {(cuuint64_t)g.head_dim, (cuuint64_t)g.kv_heads, (cuuint64_t)g.num_seqs * n_max};
+  const cuuint64_t strides[2] = {(cuuint64_t)g.head_dim * 2, (cuuint64_t)g.kv_heads * g.head_dim * 2};
+  const cuuint32_t box[3] = {64, 1, 16};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  for (int kv = 0; kv < 2; ++kv) {
+    CUresult cr = encode(kv ? &vmap : &kmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(kv ? v_new : k_new),
+                         dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                         CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (cr != CUDA_SUCCESS) return fail(HWKV_ERR_CUDA, "tensor map of the chunk could not be encoded (%d)", (int)cr);
+  }
+  PrefillArgs a;
+  std::memset(&a, 0, sizeof a);
+  a.pv = pool_view(p);
+  a.g = layer_geom(p, layer);
+  a.q = q;
+  a.k_new = k_new;
+  a.v_new = v_new;
+  a.out = out;
+  a.pos0 = pos_dev;
+  a.nlen = n_dev;
+  a.n_max = n_max;
+  a.group = G;
+  const int qt = prefill_tokens_per_cta(G);
+  a.q_tiles = (n_max + qt - 1) / qt;
+  a.scale_log2 = scale * 1.4426950408889634f;
+  // longest windows first: their CTAs stream the most keys
+  std::vector<int> order(g.kv_heads);
+  for (int h = 0; h < g.kv_heads; ++h) order[h] = h;
+  std::stable_sort(order.begin(), order.end(), [&](int x, int y) { return a.g.window[x] > a.g.window[y]; });
+  int max_c = 0;
+  for (int h = 0; h < g.kv_heads; ++h) {
+    a.head_order[h] = order[h];
+    max_c = std::max(max_c, a.g.nblk_prefix[h + 1] - a.g.nblk_prefix[h]);
+  }
+  max_c *= g.block_size;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  HWKV_CUDA_TRY(launch_prefill(a, &p->tmap, &kmap, &vmap, st), "prefill launch");
+  HWKV_CUDA_TRY(launch_chunk_append(a, std::min(n_max, max_c), st), "chunk append launch");
+  return ok();
+}
+
 int hwkv_set_decode_config(hwkv_pool_t p, int split_tokens, int workers, int kernel) {
   if (!p) return fail(HWKV_ERR_INVALID_ARG, "pool is NULL");
   if (workers < 0 || workers > (1 << 20)) return fail(HWKV_ERR_INVALID_ARG, "workers must be in [0, 2^20]");

@@ -68,6 +68,22 @@ struct DecodeArgs {
   int32_t chunk_prefix[kMaxKvHeads + 1];  // CUDA-core kernel: prefix over heads of ceil(C_h / split)
 };
 
+struct PrefillArgs {
+  PoolView pv;
+  LayerGeom g;
+  const void* q;           // [B][n_max][Hq][D]
+  const void* k_new;       // [B][n_max][H][D] chunk keys / values
+  const void* v_new;
+  void* out;               // [B][n_max][Hq][D]
+  const int32_t* pos0;     // [B] lengths before the chunk
+  const int32_t* nlen;     // [B] chunk lengths (<= n_max)
+  int32_t n_max;
+  int32_t group;           // G = Hq / H
+  int32_t q_tiles;         // CTAs per (seq, head): ceil(n_max / tokens per CTA)
+  float scale_log2;
+  int32_t head_order[kMaxKvHeads];  // heads by decreasing window (work order)
+};
+
 // Counts every kernel launch the library makes (read by hwkv_kernel_launches).
 void count_launches(uint64_t n);
 
@@ -85,5 +101,10 @@ cudaError_t launch_decode_tc(const DecodeArgs& a, const CUtensorMap* tmap, int c
 int decode_tc_group_pad(int group);  // query-head columns the kernel instance holds (4 or 8)
 cudaError_t launch_decode_simt(const DecodeArgs& a, int dtype, int items, cudaStream_t st);
 cudaError_t launch_combine(const DecodeArgs& a, int dtype, cudaStream_t st);
+// chunked prefill (hwkv_prefill.cu): attention, then the chunk appended to the rings
+int prefill_tokens_per_cta(int group);
+cudaError_t launch_prefill(const PrefillArgs& a, const CUtensorMap* pool_map, const CUtensorMap* knew_map,
+                           const CUtensorMap* vnew_map, cudaStream_t st);
+cudaError_t launch_chunk_append(const PrefillArgs& a, int max_rows, cudaStream_t st);
 
 }  // namespace hwkv

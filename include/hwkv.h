@@ -198,6 +198,22 @@ int hwkv_append_decode_attn(hwkv_pool_t pool, int layer, const void* q, int q_he
 int hwkv_decode_attn_noalloc(hwkv_pool_t pool, int layer, const void* q, int q_heads, float scale,
                              const int32_t* lens_dev, void* out, void* stream);
 
+/* Chunked prefill of one layer ("Grouped-Cache Runtime": every head keeps only its window):
+ * for each sequence s, a chunk of n_s new tokens at positions pos_s .. pos_s + n_s - 1 attends
+ * causally, per KV head h, to the positions [max(0, p + 1 - w_h), p] of each token p -- the
+ * ones before the chunk read from the head's ring in the pool, the others from the chunk --
+ * and the chunk is then appended to the rings (slot p mod C; the last min(C, n_s) tokens are
+ * written).  The result equals appending the tokens one by one and decoding each.
+ *   q, out: device bf16 [num_seqs][n_max][q_heads][D]; k_new, v_new: [num_seqs][n_max][kv_heads][D];
+ *   all 16-byte aligned.  pos_dev / n_dev: device int32 [num_seqs], lengths before the chunk
+ *   and chunk lengths (0 <= n_s <= n_max, checked on the device; a bad sequence is skipped and
+ *   flagged HWKV_DEVERR_NEG_LENGTH).  Rows of out at or past n_s are left untouched.
+ * Needs a bf16 pool with block_size % 16 == 0 and q_heads / kv_heads in {1, 2, 4, 8}
+ * (HWKV_ERR_UNSUPPORTED otherwise).  Two kernels on `stream`; no workspace. */
+int hwkv_prefill_attn(hwkv_pool_t pool, int layer, const void* q, int q_heads, float scale, const void* k_new,
+                      const void* v_new, int n_max, const int32_t* pos_dev, const int32_t* n_dev, void* out,
+                      void* stream);
+
 /* Decode configuration.  kernel = HWKV_KERNEL_*.  split_tokens: tokens of one split-K chunk of
  * the CUDA-core kernel (0 = automatic; else a power of two in [16, 65536]).  workers: CTAs of
  * the tensor-core kernel's persistent grid (0 = automatic: every SM, as many CTAs as fit).

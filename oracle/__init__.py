@@ -9,7 +9,9 @@ Plain, slow CPU restatement of what the pages fix, written from
 * same page, section "Grouped-Cache Runtime" -- a paged block table gives each head
   ceil(window / block_size) blocks;
 * same page, section "SeqCalib" -- the layer-by-layer greedy choice of window vectors under
-  a memory budget (``seqcalib_greedy``).
+  a memory budget (``seqcalib_greedy``);
+* chunked prefill (``prefill_attention``): every new token attends to its own window of the
+  full history, exactly as if the chunk had been appended and decoded token by token.
 
 Where the pages are silent the oracle takes these readings:
 
@@ -302,3 +304,21 @@ def seqcalib_greedy(candidates, distortion_fn, budget: int, cost_fn):
         remaining -= cost
         total += cost
     return policies, picks, total
+
+
+# ------------------------------------------------------------------------------------
+# Chunked prefill: token p0 + i attends to [max(0, p0 + i + 1 - w), p0 + i + 1)
+# ------------------------------------------------------------------------------------
+def prefill_attention(q: np.ndarray, hist: dict, p0: int, windows_l, scale: float, threads=None) -> np.ndarray:
+    """fp64 windowed causal attention of a chunk of one sequence.
+
+    q    : [n][Hq][D] raw host array, token i at position p0 + i
+    hist : {kv_head: (p_lo, K rows, V rows)} covering every position the chunk's windows need
+    returns [n][Hq][D] float64
+    """
+    n = q.shape[0]
+    out = np.zeros(q.shape, dtype=np.float64)
+    for i in range(n):
+        per_tok = {(0, h): v for h, v in hist.items()}
+        out[i] = attention_jobs(q[i][None], per_tok, [p0 + i + 1], windows_l, scale, threads=threads)[0]
+    return out

@@ -47,6 +47,7 @@ POLICY_LAYER1 = (1024, 4096, 4096, 16384, 16384, 65536, 65536, 65536)
 
 # purposes folded into the seeds
 _P_PREFILL_K, _P_PREFILL_V, _P_Q, _P_KNEW, _P_VNEW, _P_SPIKE_PRE, _P_SPIKE_NEW = range(1, 8)
+_P_CHUNK_Q, _P_CHUNK_K, _P_CHUNK_V = 8, 9, 10
 
 
 @dataclasses.dataclass(frozen=True)
@@ -254,6 +255,18 @@ class Workload:
         kn = k32.to(cfg.torch_dtype)
         vn = _randn((L, B, H, D), _seed(cfg, _P_VNEW, 0, step), self.device, cfg.torch_dtype)
         return q.to(dev), kn.to(dev), vn.to(dev)
+
+    # ---- chunked prefill ----------------------------------------------------------
+    def chunk_inputs(self, layer: int, chunk: int, n_max: int, device=None):
+        """A prefill chunk of n_max token rows per sequence: (q [B][n_max][Hq][D],
+        k [B][n_max][Hkv][D], v [B][n_max][Hkv][D]), N(0, 1)."""
+        cfg = self.cfg
+        dev = torch.device(device) if device is not None else self.device
+        B, H, Hq, D = cfg.batch, cfg.kv_heads, cfg.q_heads, cfg.head_dim
+        q = _randn((B, n_max, Hq, D), _seed(cfg, _P_CHUNK_Q, layer, chunk), self.device, cfg.torch_dtype)
+        k = _randn((B, n_max, H, D), _seed(cfg, _P_CHUNK_K, layer, chunk), self.device, cfg.torch_dtype)
+        v = _randn((B, n_max, H, D), _seed(cfg, _P_CHUNK_V, layer, chunk), self.device, cfg.torch_dtype)
+        return q.to(dev), k.to(dev), v.to(dev)
 
     # ---- host copies for the oracle ------------------------------------------------
     def history(self, layer: int, s: int, h: int, p_lo: int, p_hi: int, prefill=None, steps=None):
