@@ -10,7 +10,8 @@
 // warp iteration, lanes splitting head_dim, and emits (m, l, acc[D]) per query head of the
 // GQA group: m = running max of scale*log2(e)*<q,k>, l = sum of 2^(score - m),
 // acc = sum of 2^(score - m) * v.  Heads whose ring is one chunk write the normalised
-// output directly; the others are merged by combine_kernel.
+// output directly; the others are merged by combine_kernel.  A CTA holds at most 8 query heads:
+// larger GQA groups are split over grid.y (each slice streams the chunk again).
 #include "hwkv_device.cuh"
 
 namespace hwkv {
@@ -38,13 +39,15 @@ __device__ __forceinline__ Item decode_item(const DecodeArgs& a, int item) {
 }
 
 constexpr int kSimtWarps = 4;
+constexpr int kSimtHeads = 8;  // query heads per CTA
 
 template <typename T, int D>
 __global__ void __launch_bounds__(kSimtWarps * 32) decode_simt_kernel(const __grid_constant__ DecodeArgs a) {
   constexpr int W = kSimtWarps;
   constexpr int PER = D / 32;
-  __shared__ float sm_m[W * 8], sm_l[W * 8];
-  __shared__ float sm_acc[W * 8 * D];
+  constexpr int GH = kSimtHeads;
+  __shared__ float sm_m[W * GH], sm_l[W * GH];
+  __shared__ float sm_acc[W * GH * D];
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int item = blockIdx.x;
@@ -63,17 +66,19 @@ __global__ void __launch_bounds__(kSimtWarps * 32) decode_simt_kernel(const __gr
   const int G = a.group;
   const int Hq = a.pv.kv_heads * G;
   const float sl2 = a.scale_log2;
+  const int g0 = blockIdx.y * GH;      // first query head of this CTA's slice
+  const int ng = min(GH, G - g0);      // query heads of the slice
 
-  float qv[kMaxGroup][PER];
-  float m[kMaxGroup], l[kMaxGroup], acc[kMaxGroup][PER];
-  const T* qbase = static_cast<const T*>(a.q) + ((int64_t)it.s * Hq + it.h * G) * D;
+  float qv[GH][PER];
+  float m[GH], l[GH], acc[GH][PER];
+  const T* qbase = static_cast<const T*>(a.q) + ((int64_t)it.s * Hq + it.h * G + g0) * D;
 #pragma unroll
-  for (int g = 0; g < kMaxGroup; ++g) {
+  for (int g = 0; g < GH; ++g) {
     m[g] = kNegInf;
     l[g] = 0.f;
 #pragma unroll
     for (int k = 0; k < PER; ++k) {
-      qv[g][k] = g < G ? load_in<T>(qbase + g * D + lane + 32 * k) : 0.f;
+      qv[g][k] = g < ng ? load_in<T>(qbase + g * D + lane + 32 * k) : 0.f;
       acc[g][k] = 0.f;
     }
   }
@@ -95,8 +100,8 @@ __global__ void __launch_bounds__(kSimtWarps * 32) decode_simt_kernel(const __gr
       vv[k] = load_in<T>(vrow + lane + 32 * k);
     }
 #pragma unroll
-    for (int g = 0; g < kMaxGroup; ++g) {
-      if (g < G) {
+    for (int g = 0; g < GH; ++g) {
+      if (g < ng) {
         float dot = 0.f;
 #pragma unroll
         for (int k = 0; k < PER; ++k) dot = fmaf(qv[g][k], kv[k], dot);
@@ -115,29 +120,30 @@ __global__ void __launch_bounds__(kSimtWarps * 32) decode_simt_kernel(const __gr
   }
 
 #pragma unroll
-  for (int g = 0; g < kMaxGroup; ++g) {
+  for (int g = 0; g < GH; ++g) {
     if (lane == 0) {
-      sm_m[warp * 8 + g] = m[g];
-      sm_l[warp * 8 + g] = l[g];
+      sm_m[warp * GH + g] = m[g];
+      sm_l[warp * GH + g] = l[g];
     }
 #pragma unroll
-    for (int k = 0; k < PER; ++k) sm_acc[(warp * 8 + g) * D + lane + 32 * k] = acc[g][k];
+    for (int k = 0; k < PER; ++k) sm_acc[(warp * GH + g) * D + lane + 32 * k] = acc[g][k];
   }
   __syncthreads();
 
   // merge the warps; single-chunk heads write the output, the others their partial
-  for (int e = threadIdx.x; e < G * D; e += W * 32) {
-    const int g = e / D, d = e - (e / D) * D;
+  for (int e = threadIdx.x; e < ng * D; e += W * 32) {
+    const int gl = e / D, d = e - (e / D) * D;
+    const int g = g0 + gl;
     float M = kNegInf;
 #pragma unroll
-    for (int w = 0; w < W; ++w) M = fmaxf(M, sm_m[w * 8 + g]);
+    for (int w = 0; w < W; ++w) M = fmaxf(M, sm_m[w * GH + gl]);
     float Ls = 0.f, A = 0.f;
     if (M != kNegInf) {
 #pragma unroll
       for (int w = 0; w < W; ++w) {
-        const float f = ex2(sm_m[w * 8 + g] - M);
-        Ls += sm_l[w * 8 + g] * f;
-        A += sm_acc[(w * 8 + g) * D + d] * f;
+        const float f = ex2(sm_m[w * GH + gl] - M);
+        Ls += sm_l[w * GH + gl] * f;
+        A += sm_acc[(w * GH + gl) * D + d] * f;
       }
     }
     if (it.nchunks == 1) {
@@ -184,10 +190,11 @@ __global__ void __launch_bounds__(256) combine_kernel(const __grid_constant__ De
 
 cudaError_t launch_decode_simt(const DecodeArgs& a, int dtype, int items, cudaStream_t st) {
   const int D = a.pv.head_dim;
-  if (dtype == HWKV_F32 && D == 64) decode_simt_kernel<float, 64><<<items, kSimtWarps * 32, 0, st>>>(a);
-  else if (dtype == HWKV_F32 && D == 128) decode_simt_kernel<float, 128><<<items, kSimtWarps * 32, 0, st>>>(a);
-  else if (dtype == HWKV_BF16 && D == 64) decode_simt_kernel<__nv_bfloat16, 64><<<items, kSimtWarps * 32, 0, st>>>(a);
-  else if (dtype == HWKV_BF16 && D == 128) decode_simt_kernel<__nv_bfloat16, 128><<<items, kSimtWarps * 32, 0, st>>>(a);
+  const dim3 grid((unsigned)items, (unsigned)((a.group + kSimtHeads - 1) / kSimtHeads));
+  if (dtype == HWKV_F32 && D == 64) decode_simt_kernel<float, 64><<<grid, kSimtWarps * 32, 0, st>>>(a);
+  else if (dtype == HWKV_F32 && D == 128) decode_simt_kernel<float, 128><<<grid, kSimtWarps * 32, 0, st>>>(a);
+  else if (dtype == HWKV_BF16 && D == 64) decode_simt_kernel<__nv_bfloat16, 64><<<grid, kSimtWarps * 32, 0, st>>>(a);
+  else if (dtype == HWKV_BF16 && D == 128) decode_simt_kernel<__nv_bfloat16, 128><<<grid, kSimtWarps * 32, 0, st>>>(a);
   else return cudaErrorInvalidValue;
   count_launches(1);
   return cudaGetLastError();

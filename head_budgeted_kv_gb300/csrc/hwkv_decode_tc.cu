@@ -17,12 +17,13 @@
 // the group's arrival counter, and the CTA that arrives last merges all partials of the group
 // and writes the output (no CTA ever waits for another).
 //
-// Per tile (16 tokens), per warp, with the GQA group (G <= 8 query heads, zero-padded to 8)
-// on the N side of mma.sync.m16n8k16 bf16 -> fp32:
-//   S[16 tok][8 q] = K_tile . Q^T over head_dim (K tile loaded with ldmatrix from the
-//   128-byte-swizzled TMA tile), masked to resident slots, online softmax in fp32 in the log2
-//   domain; P is moved from the accumulator layout to the operand layout with movmatrix.trans;
-//   O^T[D][8 q] = alpha * O^T + V_tile^T . P (V tile loaded with ldmatrix.trans).
+// Per tile (16 tokens), per warp, with the GQA group (G <= 16 query heads, zero-padded to one
+// or two 8-column n-tiles) on the N side of mma.sync.m16n8k16 bf16 -> fp32:
+//   S[16 tok][8 q] = K_tile . Q^T over head_dim per n-tile (K tile loaded once with ldmatrix
+//   from the 128-byte-swizzled TMA tile and shared by the n-tiles), masked to resident slots,
+//   online softmax in fp32 in the log2 domain; P is moved from the accumulator layout to the
+//   operand layout with movmatrix.trans; O^T[D][8 q] = alpha * O^T + V_tile^T . P (V tile
+//   loaded once with ldmatrix.trans).
 //
 // Waits are bounded (~2 s); a timeout records HWKV_DEVERR_WAIT_TIMEOUT and the warp stops.
 #include "hwkv_device.cuh"
@@ -193,12 +194,14 @@ __global__ void __launch_bounds__(kWarps * 32, 2) decode_sk_kernel(const __grid_
   constexpr int kStageBytes = 2 * kTileBytes;  // K tile + V tile
   constexpr int kSteps = D / 16;               // k-steps of QK, m-tiles of PV
   constexpr int kRowVecs = D * 2 / 16;         // 16-byte vectors per row
+  constexpr int NT = (GP + 7) / 8;             // 8-column n-tiles of query heads
+  constexpr int SG = GP < 8 ? GP : 8;          // query heads merged per pass in shared memory
 
   extern __shared__ uint8_t smem_dyn[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_dyn) + 1023) & ~uintptr_t(1023));
-  float* sc_acc = reinterpret_cast<float*>(smem + W * NS * kStageBytes);  // [W][GP][D]
+  float* sc_acc = reinterpret_cast<float*>(smem + W * NS * kStageBytes);  // [W][SG][D]
   __shared__ __align__(8) uint64_t bars[W * NS];
-  __shared__ float sc_m[W * GP], sc_l[W * GP];
+  __shared__ float sc_m[W * SG], sc_l[W * SG];
   __shared__ long long s_scan[W];
   __shared__ long long s_start[2];
   __shared__ int s_last;
@@ -320,22 +323,29 @@ __global__ void __launch_bounds__(kWarps * 32, 2) decode_sk_kernel(const __grid_
     const long long seg_begin = t_lo > spre ? t_lo : spre;
     const long long seg_end = t_hi < spre + sgr.tiles ? t_hi : spre + sgr.tiles;
 
-    // Q of this group as the B operand of S = K . Q^T: lane holds q[g][16i + 2*q4 + {0,1}]
-    // and the same +8, g = lane/4; rows g >= G are zero.
-    uint32_t qf[kSteps][2];
-    {
+    // Q of this group as the B operand of S = K . Q^T: in n-tile nt the lane holds
+    // q[g][16i + 2*q4 + {0,1}] and the same +8, g = 8*nt + lane/4; heads g >= G are zero.
+    uint32_t qf[NT][kSteps][2];
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) {
+      const int g = 8 * nt + gq;
       const __nv_bfloat16* qrow =
-          static_cast<const __nv_bfloat16*>(a.q) + ((int64_t)sgr.s * Hq + sgr.h * G + gq) * D;
+          static_cast<const __nv_bfloat16*>(a.q) + ((int64_t)sgr.s * Hq + sgr.h * G + g) * D;
 #pragma unroll
       for (int i = 0; i < kSteps; ++i) {
-        qf[i][0] = gq < G ? *reinterpret_cast<const uint32_t*>(qrow + 16 * i + 2 * q4) : 0u;
-        qf[i][1] = gq < G ? *reinterpret_cast<const uint32_t*>(qrow + 16 * i + 2 * q4 + 8) : 0u;
+        qf[nt][i][0] = g < G ? *reinterpret_cast<const uint32_t*>(qrow + 16 * i + 2 * q4) : 0u;
+        qf[nt][i][1] = g < G ? *reinterpret_cast<const uint32_t*>(qrow + 16 * i + 2 * q4 + 8) : 0u;
       }
     }
-    float acc[kSteps][4];
+    float acc[kSteps][NT][4];
 #pragma unroll
-    for (int j = 0; j < kSteps; ++j) acc[j][0] = acc[j][1] = acc[j][2] = acc[j][3] = 0.f;
-    float m0 = kNegInf, m1 = kNegInf, l0 = 0.f, l1 = 0.f;  // columns g = 2*q4, 2*q4 + 1
+    for (int j = 0; j < kSteps; ++j)
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt) acc[j][nt][0] = acc[j][nt][1] = acc[j][nt][2] = acc[j][nt][3] = 0.f;
+    // online-softmax state of columns g = 8*nt + 2*q4 + {0, 1}
+    float mx[NT][2], ls[NT][2];
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) mx[nt][0] = mx[nt][1] = kNegInf, ls[nt][0] = ls[nt][1] = 0.f;
     const int new_slot = (a.k_new != nullptr) ? (sgr.len - 1) % sgr.rs.C : -1;
 
     while (j_cons < seg_end) {
@@ -373,48 +383,64 @@ __global__ void __launch_bounds__(kWarps * 32, 2) decode_sk_kernel(const __grid_
           patched_stage = true;
         }
 
-        // S[16 tok][8 q] = K_tile . Q^T (two accumulation chains)
-        float sa[4] = {0.f, 0.f, 0.f, 0.f}, sb[4] = {0.f, 0.f, 0.f, 0.f};
+        // S[16 tok][8 q] = K_tile . Q^T per n-tile (two accumulation chains each)
+        float sa[NT][4], sb[NT][4];
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+          for (int e = 0; e < 4; ++e) sa[nt][e] = sb[nt][e] = 0.f;
 #pragma unroll
         for (int i = 0; i < kSteps; ++i) {
           uint32_t af[4];
           ldsm_x4(af, sK + swz(a_row, 16 * i + a_dof));
-          if (i & 1) mma_bf16(sb, af, qf[i][0], qf[i][1]);
-          else mma_bf16(sa, af, qf[i][0], qf[i][1]);
+#pragma unroll
+          for (int nt = 0; nt < NT; ++nt) {
+            if (i & 1) mma_bf16(sb[nt], af, qf[nt][i][0], qf[nt][i][1]);
+            else mma_bf16(sa[nt], af, qf[nt][i][0], qf[nt][i][1]);
+          }
         }
         const bool v0 = slot_valid(sgr.rs, t0 + gq), v1 = slot_valid(sgr.rs, t0 + gq + 8);
-        const float s0 = v0 ? sa[0] + sb[0] : kNegInf;
-        const float s1 = v0 ? sa[1] + sb[1] : kNegInf;
-        const float s2 = v1 ? sa[2] + sb[2] : kNegInf;
-        const float s3 = v1 ? sa[3] + sb[3] : kNegInf;
-        float mx0 = fmaxf(s0, s2), mx1 = fmaxf(s1, s3);
+        float al[NT][2];
+        uint32_t pb[NT][2];
 #pragma unroll
-        for (int off = 4; off < 32; off <<= 1) {
-          mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, off));
-          mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, off));
+        for (int nt = 0; nt < NT; ++nt) {
+          const float s0 = v0 ? sa[nt][0] + sb[nt][0] : kNegInf;
+          const float s1 = v0 ? sa[nt][1] + sb[nt][1] : kNegInf;
+          const float s2 = v1 ? sa[nt][2] + sb[nt][2] : kNegInf;
+          const float s3 = v1 ? sa[nt][3] + sb[nt][3] : kNegInf;
+          float mx0 = fmaxf(s0, s2), mx1 = fmaxf(s1, s3);
+#pragma unroll
+          for (int off = 4; off < 32; off <<= 1) {
+            mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, off));
+            mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, off));
+          }
+          const float n0 = fmaxf(mx[nt][0], mx0 * sl2), n1 = fmaxf(mx[nt][1], mx1 * sl2);
+          const float b0 = n0 == kNegInf ? 0.f : n0, b1 = n1 == kNegInf ? 0.f : n1;
+          al[nt][0] = ex2(mx[nt][0] - b0);
+          al[nt][1] = ex2(mx[nt][1] - b1);
+          const float p0 = ex2(fmaf(s0, sl2, -b0)), p1 = ex2(fmaf(s1, sl2, -b1));
+          const float p2 = ex2(fmaf(s2, sl2, -b0)), p3 = ex2(fmaf(s3, sl2, -b1));
+          ls[nt][0] = fmaf(ls[nt][0], al[nt][0], p0 + p2);
+          ls[nt][1] = fmaf(ls[nt][1], al[nt][1], p1 + p3);
+          mx[nt][0] = n0;
+          mx[nt][1] = n1;
+          pb[nt][0] = movmatrix_trans(pack_bf16(p0, p1));
+          pb[nt][1] = movmatrix_trans(pack_bf16(p2, p3));
         }
-        const float n0 = fmaxf(m0, mx0 * sl2), n1 = fmaxf(m1, mx1 * sl2);
-        const float b0 = n0 == kNegInf ? 0.f : n0, b1 = n1 == kNegInf ? 0.f : n1;
-        const float al0 = ex2(m0 - b0), al1 = ex2(m1 - b1);
-        const float p0 = ex2(fmaf(s0, sl2, -b0)), p1 = ex2(fmaf(s1, sl2, -b1));
-        const float p2 = ex2(fmaf(s2, sl2, -b0)), p3 = ex2(fmaf(s3, sl2, -b1));
-        l0 = fmaf(l0, al0, p0 + p2);
-        l1 = fmaf(l1, al1, p1 + p3);
-        m0 = n0;
-        m1 = n1;
-        const uint32_t pb0 = movmatrix_trans(pack_bf16(p0, p1));
-        const uint32_t pb1 = movmatrix_trans(pack_bf16(p2, p3));
 
-        // O^T[D][8 q] = alpha * O^T + V_tile^T . P
+        // O^T[D][8 q] = alpha * O^T + V_tile^T . P per n-tile
 #pragma unroll
         for (int j = 0; j < kSteps; ++j) {
-          acc[j][0] *= al0;
-          acc[j][1] *= al1;
-          acc[j][2] *= al0;
-          acc[j][3] *= al1;
           uint32_t af[4];
           ldsm_x4_trans(af, sV + swz(v_row, 16 * j + v_dof));
-          mma_bf16(acc[j], af, pb0, pb1);
+#pragma unroll
+          for (int nt = 0; nt < NT; ++nt) {
+            acc[j][nt][0] *= al[nt][0];
+            acc[j][nt][1] *= al[nt][1];
+            acc[j][nt][2] *= al[nt][0];
+            acc[j][nt][3] *= al[nt][1];
+            mma_bf16(acc[j][nt], af, pb[nt][0], pb[nt][1]);
+          }
         }
       }
       __syncwarp();
@@ -433,52 +459,62 @@ __global__ void __launch_bounds__(kWarps * 32, 2) decode_sk_kernel(const __grid_
     // ---- end of segment: merge the warps, then store output or partial -----------------
     if (seg_end >= t_hi) griddep_launch_dependents();  // this CTA reads no more tiles
 #pragma unroll
-    for (int off = 4; off < 32; off <<= 1) {
-      l0 += __shfl_xor_sync(0xffffffffu, l0, off);
-      l1 += __shfl_xor_sync(0xffffffffu, l1, off);
-    }
-    if (2 * q4 < GP) {
-      if (gq == 0) {
-        sc_m[warp * GP + 2 * q4] = m0;
-        sc_m[warp * GP + 2 * q4 + 1] = m1;
-        sc_l[warp * GP + 2 * q4] = l0;
-        sc_l[warp * GP + 2 * q4 + 1] = l1;
-      }
-      float* wacc = sc_acc + warp * GP * D;
+    for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
-      for (int j = 0; j < kSteps; ++j) {
-        const int d = 16 * j + gq;
-        wacc[(2 * q4) * D + d] = acc[j][0];
-        wacc[(2 * q4 + 1) * D + d] = acc[j][1];
-        wacc[(2 * q4) * D + d + 8] = acc[j][2];
-        wacc[(2 * q4 + 1) * D + d + 8] = acc[j][3];
+      for (int off = 4; off < 32; off <<= 1) {
+        ls[nt][0] += __shfl_xor_sync(0xffffffffu, ls[nt][0], off);
+        ls[nt][1] += __shfl_xor_sync(0xffffffffu, ls[nt][1], off);
       }
-    }
-    __syncthreads();
-
     const bool whole = seg_begin == spre && seg_end == spre + sgr.tiles;
     const long long slot = (long long)sg + cta;  // unique per (group, CTA) along the line
-    for (int e = threadIdx.x; e < G * D; e += W * 32) {
-      const int g = e / D, d = e - (e / D) * D;
-      float M = kNegInf;
+    // one pass per n-tile: the warps' states of query heads [8*nt, 8*nt + SG) meet in shared
+    // memory and are folded into the output or this CTA's partial
 #pragma unroll
-      for (int w = 0; w < W; ++w) M = fmaxf(M, sc_m[w * GP + g]);
-      float Ls = 0.f, A = 0.f;
-      if (M != kNegInf) {
+    for (int nt = 0; nt < NT; ++nt) {
+      if (nt > 0) __syncthreads();  // the previous pass has read the scratch
+      if (2 * q4 < SG) {
+        if (gq == 0) {
+          sc_m[warp * SG + 2 * q4] = mx[nt][0];
+          sc_m[warp * SG + 2 * q4 + 1] = mx[nt][1];
+          sc_l[warp * SG + 2 * q4] = ls[nt][0];
+          sc_l[warp * SG + 2 * q4 + 1] = ls[nt][1];
+        }
+        float* wacc = sc_acc + warp * SG * D;
 #pragma unroll
-        for (int w = 0; w < W; ++w) {
-          const float f = ex2(sc_m[w * GP + g] - M);
-          Ls += sc_l[w * GP + g] * f;
-          A += sc_acc[(w * GP + g) * D + d] * f;
+        for (int j = 0; j < kSteps; ++j) {
+          const int d = 16 * j + gq;
+          wacc[(2 * q4) * D + d] = acc[j][nt][0];
+          wacc[(2 * q4 + 1) * D + d] = acc[j][nt][1];
+          wacc[(2 * q4) * D + d + 8] = acc[j][nt][2];
+          wacc[(2 * q4 + 1) * D + d + 8] = acc[j][nt][3];
         }
       }
-      if (whole) {
-        out[((int64_t)sgr.s * Hq + sgr.h * G + g) * D + d] = __float2bfloat16_rn(Ls > 0.f ? A / Ls : 0.f);
-      } else {
-        a.part_acc[(slot * G + g) * D + d] = A;
-        if (d == 0) {
-          a.part_ml[(slot * G + g) * 2 + 0] = M;
-          a.part_ml[(slot * G + g) * 2 + 1] = Ls;
+      __syncthreads();
+      const int g0 = 8 * nt;
+      const int ng = min(SG, G - g0);  // real query heads of this pass
+      for (int e = threadIdx.x; e < ng * D; e += W * 32) {
+        const int gl = e / D, d = e - (e / D) * D;
+        const int g = g0 + gl;
+        float M = kNegInf;
+#pragma unroll
+        for (int w = 0; w < W; ++w) M = fmaxf(M, sc_m[w * SG + gl]);
+        float Ls = 0.f, A = 0.f;
+        if (M != kNegInf) {
+#pragma unroll
+          for (int w = 0; w < W; ++w) {
+            const float f = ex2(sc_m[w * SG + gl] - M);
+            Ls += sc_l[w * SG + gl] * f;
+            A += sc_acc[(w * SG + gl) * D + d] * f;
+          }
+        }
+        if (whole) {
+          out[((int64_t)sgr.s * Hq + sgr.h * G + g) * D + d] = __float2bfloat16_rn(Ls > 0.f ? A / Ls : 0.f);
+        } else {
+          a.part_acc[(slot * G + g) * D + d] = A;
+          if (d == 0) {
+            a.part_ml[(slot * G + g) * 2 + 0] = M;
+            a.part_ml[(slot * G + g) * 2 + 1] = Ls;
+          }
         }
       }
     }
@@ -538,7 +574,8 @@ __global__ void __launch_bounds__(kWarps * 32, 2) decode_sk_kernel(const __grid_
 
 template <int D, int GP, int NS>
 constexpr int sk_smem_bytes() {
-  return kWarps * NS * (2 * kTile * D * 2) + kWarps * GP * D * 4 + 1024;  // stages + merge scratch + align slack
+  // stages + merge scratch (at most 8 query heads per pass) + align slack
+  return kWarps * NS * (2 * kTile * D * 2) + kWarps * (GP < 8 ? GP : 8) * D * 4 + 1024;
 }
 
 // pipeline depth: 3 (head_dim 128) or 6 (head_dim 64) stages of 16 tokens per warp
@@ -579,25 +616,36 @@ cudaError_t launch_one(const DecodeArgs& a, const CUtensorMap* tmap, int ctas, c
 
 }  // namespace
 
-int decode_tc_group_pad(int group) { return group <= 4 ? 4 : 8; }
+int decode_tc_group_pad(int group) { return group <= 4 ? 4 : group <= 8 ? 8 : 16; }
 
-cudaError_t configure_decode_tc(int head_dim, int* ctas_per_sm_gp4, int* ctas_per_sm_gp8) {
+int decode_tc_pad_index(int group) { return group <= 4 ? 0 : group <= 8 ? 1 : 2; }
+
+template <int D>
+cudaError_t configure_dim(int ctas_per_sm[kGroupPads]) {
   cudaError_t e;
-  if (head_dim == 128) {
-    if ((e = configure_one<128, 4>(ctas_per_sm_gp4)) != cudaSuccess) return e;
-    return configure_one<128, 8>(ctas_per_sm_gp8);
-  }
-  if (head_dim == 64) {
-    if ((e = configure_one<64, 4>(ctas_per_sm_gp4)) != cudaSuccess) return e;
-    return configure_one<64, 8>(ctas_per_sm_gp8);
-  }
+  if ((e = configure_one<D, 4>(&ctas_per_sm[0])) != cudaSuccess) return e;
+  if ((e = configure_one<D, 8>(&ctas_per_sm[1])) != cudaSuccess) return e;
+  return configure_one<D, 16>(&ctas_per_sm[2]);
+}
+
+cudaError_t configure_decode_tc(int head_dim, int ctas_per_sm[kGroupPads]) {
+  if (head_dim == 128) return configure_dim<128>(ctas_per_sm);
+  if (head_dim == 64) return configure_dim<64>(ctas_per_sm);
   return cudaErrorInvalidValue;
 }
 
+template <int D>
+cudaError_t launch_dim(const DecodeArgs& a, const CUtensorMap* tmap, int ctas, cudaStream_t st) {
+  switch (decode_tc_group_pad(a.group)) {
+    case 4: return launch_one<D, 4>(a, tmap, ctas, st);
+    case 8: return launch_one<D, 8>(a, tmap, ctas, st);
+    default: return launch_one<D, 16>(a, tmap, ctas, st);
+  }
+}
+
 cudaError_t launch_decode_tc(const DecodeArgs& a, const CUtensorMap* tmap, int ctas, cudaStream_t st) {
-  const int gp = decode_tc_group_pad(a.group);
-  if (a.pv.head_dim == 128) return gp == 4 ? launch_one<128, 4>(a, tmap, ctas, st) : launch_one<128, 8>(a, tmap, ctas, st);
-  if (a.pv.head_dim == 64) return gp == 4 ? launch_one<64, 4>(a, tmap, ctas, st) : launch_one<64, 8>(a, tmap, ctas, st);
+  if (a.pv.head_dim == 128) return launch_dim<128>(a, tmap, ctas, st);
+  if (a.pv.head_dim == 64) return launch_dim<64>(a, tmap, ctas, st);
   return cudaErrorInvalidValue;
 }
 

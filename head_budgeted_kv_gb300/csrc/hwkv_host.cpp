@@ -153,7 +153,7 @@ struct hwkv_pool {
   std::vector<int32_t> h_tbl;
   int device = 0;
   int num_sms = 0;
-  int ctas_per_sm_gp4 = 0, ctas_per_sm_gp8 = 0;
+  int ctas_per_sm[kGroupPads] = {0, 0, 0};  // tensor-core decode instances, by group pad
   int split_override = 0;
   int workers_override = 0;
   int kernel_choice = HWKV_KERNEL_AUTO;
@@ -204,14 +204,14 @@ void plan_decode(hwkv_pool* p) {
 // persistent CTAs of the tensor-core kernel
 int tc_workers(const hwkv_pool* p, int group) {
   if (p->workers_override > 0) return p->workers_override;
-  const int per_sm = decode_tc_group_pad(group) == 4 ? p->ctas_per_sm_gp4 : p->ctas_per_sm_gp8;
+  const int per_sm = p->ctas_per_sm[decode_tc_pad_index(group)];
   return std::max(1, p->num_sms * std::max(1, per_sm));
 }
 
 // first-level merge blocks per head for a grid of `workers` CTAs
 int merge_blocks_for(int workers) { return (workers + kMergeBlock - 1) / kMergeBlock + 1; }
 
-int max_tc_workers(const hwkv_pool* p) { return std::max(tc_workers(p, 4), tc_workers(p, 8)); }
+int max_tc_workers(const hwkv_pool* p) { return std::max({tc_workers(p, 4), tc_workers(p, 8), tc_workers(p, 16)}); }
 
 // Workspace regions (each 256-byte aligned): partials [slots][G][D] floats, their (m, l)
 // [slots][G][2]; for the tensor-core kernel also the second-level partials and (m, l).
@@ -409,7 +409,7 @@ int hwkv_pool_create(int layers, int kv_heads, int head_dim, int block_size, con
     }
   }
   if (p->has_tmap) {
-    e = configure_decode_tc(p->g.head_dim, &p->ctas_per_sm_gp4, &p->ctas_per_sm_gp8);
+    e = configure_decode_tc(p->g.head_dim, p->ctas_per_sm);
     if (e != cudaSuccess) return cleanup_fail("cudaFuncSetAttribute", e);
   }
   plan_decode(p);
@@ -651,7 +651,7 @@ int hwkv_prefill_attn(hwkv_pool_t p, int layer, const void* q, int q_heads, floa
   if (q_heads < g.kv_heads || q_heads % g.kv_heads != 0)
     return fail(HWKV_ERR_UNSUPPORTED, "q_heads must be a multiple of kv_heads");
   const int G = q_heads / g.kv_heads;
-  if (G != 1 && G != 2 && G != 4 && G != 8) return fail(HWKV_ERR_UNSUPPORTED, "prefill supports GQA groups 1, 2, 4, 8");
+  if (G > kMaxGroup) return fail(HWKV_ERR_UNSUPPORTED, "q_heads must be G * kv_heads with 1 <= G <= %d", kMaxGroup);
   if (!(scale == scale) || scale == std::numeric_limits<float>::infinity() ||
       scale == -std::numeric_limits<float>::infinity())
     return fail(HWKV_ERR_INVALID_ARG, "scale must be finite");

@@ -10,7 +10,8 @@ namespace hwkv {
 
 constexpr int kMaxKvHeads = 32;
 constexpr int kMergeBlock = 16;  // CTAs whose partials one first-level merge folds
-constexpr int kMaxGroup = 8;
+constexpr int kMaxGroup = 16;  // query heads per KV head (GQA group)
+constexpr int kGroupPads = 3;   // tensor-core decode instances: 4, 8 or 16 query-head columns
 
 // Geometry of one layer, passed by value to every kernel of that layer.
 //   table entry of (seq s, kv head h, logical block j) = tbl[tbl_base + s*tbl_seq_stride
@@ -94,11 +95,13 @@ int set_error(int code, const char* fmt, ...);
 cudaError_t launch_append(const CopyArgs& a, int dtype, cudaStream_t st);
 // max_rows: the most positions any (seq, head) of the layer copies, min(max window, max_len)
 cudaError_t launch_materialize(const CopyArgs& a, int dtype, int max_rows, cudaStream_t st);
-// once per device before the first launch; returns resident CTAs per SM of both instances
-cudaError_t configure_decode_tc(int head_dim, int* ctas_per_sm_gp4, int* ctas_per_sm_gp8);
+// once per device before the first launch; returns resident CTAs per SM of the instances
+// for 4, 8 and 16 query-head columns
+cudaError_t configure_decode_tc(int head_dim, int ctas_per_sm[kGroupPads]);
 // tensor-core kernel: `ctas` persistent CTAs split the resident tiles of the layer evenly
 cudaError_t launch_decode_tc(const DecodeArgs& a, const CUtensorMap* tmap, int ctas, cudaStream_t st);
-int decode_tc_group_pad(int group);  // query-head columns the kernel instance holds (4 or 8)
+int decode_tc_group_pad(int group);  // query-head columns the kernel instance holds (4, 8 or 16)
+int decode_tc_pad_index(int group);  // 0, 1, 2 for 4, 8, 16 columns
 cudaError_t launch_decode_simt(const DecodeArgs& a, int dtype, int items, cudaStream_t st);
 cudaError_t launch_combine(const DecodeArgs& a, int dtype, cudaStream_t st);
 // chunked prefill (hwkv_prefill.cu): attention, then the chunk appended to the rings

@@ -9,8 +9,9 @@
 // K/V rows.  Appending the chunk then overwrites ring slots that earlier queries of the same
 // chunk still read, so the append is a second launch after the attention.
 //
-// prefill_kernel (bf16, block_size % 16 == 0, head_dim 64 or 128, G in {1, 2, 4, 8}):
-//   CTA = (seq, kv head, query tile of 64 rows = 64/G tokens x G query heads); 4 consumer
+// prefill_kernel (bf16, block_size % 16 == 0, head_dim 64 or 128, GQA group 1 <= G <= 16):
+//   CTA = (seq, kv head, query tile of 64 rows = floor(64/G) tokens x G query heads, the rows
+//   past the last whole token idle); 4 consumer
 //   warps own 16 rows each, a producer warp streams 16-token K/V tiles into a 4-stage ring of
 //   shared memory with TMA (pool tiles through the block table, chunk tiles through a tensor
 //   map of the chunk).  Per tile and warp: S[16 rows][16 keys] = Q K^T and O += P V with
@@ -56,7 +57,7 @@ struct PfTiles {
   int chunk_tiles;
 };
 
-template <int D, int G>
+template <int D>
 __global__ void __launch_bounds__(kPfThreads) prefill_kernel(const __grid_constant__ CUtensorMap pool_map,
                                                             const __grid_constant__ CUtensorMap knew_map,
                                                             const __grid_constant__ CUtensorMap vnew_map,
@@ -66,7 +67,6 @@ __global__ void __launch_bounds__(kPfThreads) prefill_kernel(const __grid_consta
   constexpr int kStageBytes = 2 * kTileBytes;
   constexpr int kSteps = D / 16;  // k-steps of QK
   constexpr int kDTiles = D / 8;  // n-tiles of PV
-  constexpr int QT = kPfRows / G; // tokens per CTA
 
   extern __shared__ uint8_t smem_dyn[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_dyn) + 1023) & ~uintptr_t(1023));
@@ -74,6 +74,8 @@ __global__ void __launch_bounds__(kPfThreads) prefill_kernel(const __grid_consta
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int H = a.pv.kv_heads;
+  const int G = a.group;
+  const int QT = kPfRows / G;  // tokens per CTA
   const int Hq = H * G;
   const int bs = a.pv.block_size;
 
@@ -175,11 +177,12 @@ __global__ void __launch_bounds__(kPfThreads) prefill_kernel(const __grid_consta
   const int row0 = warp * 16 + gq, row1 = row0 + 8;
   const int tok0 = qa + row0 / G, tok1 = qa + row1 / G;  // chunk rows of the lane's two rows
   const int pq0 = p0 + tok0, pq1 = p0 + tok1;            // their positions
+  // rows holding a real query: inside the CTA's whole tokens and the chunk
+  const bool ok0 = row0 < QT * G && tok0 < n, ok1 = row1 < QT * G && tok1 < n;
   // Q as the A operand: lane holds rows row0/row1, dims 16i + 2*q4 + {0,1} and +8
   uint32_t qf[kSteps][4];
   {
     const __nv_bfloat16* qbase = static_cast<const __nv_bfloat16*>(a.q);
-    const bool ok0 = tok0 < n, ok1 = tok1 < n;
     const __nv_bfloat16* q0 = qbase + (((int64_t)s * a.n_max + (ok0 ? tok0 : 0)) * Hq + h * G + row0 % G) * D;
     const __nv_bfloat16* q1 = qbase + (((int64_t)s * a.n_max + (ok1 ? tok1 : 0)) * Hq + h * G + row1 % G) * D;
 #pragma unroll
@@ -309,13 +312,13 @@ __global__ void __launch_bounds__(kPfThreads) prefill_kernel(const __grid_consta
   }
   const float i0 = l0 > 0.f ? 1.f / l0 : 0.f, i1 = l1 > 0.f ? 1.f / l1 : 0.f;
   __nv_bfloat16* obase = static_cast<__nv_bfloat16*>(a.out);
-  if (tok0 < n) {
+  if (ok0) {
     __nv_bfloat16* o0 = obase + (((int64_t)s * a.n_max + tok0) * Hq + h * G + row0 % G) * D;
 #pragma unroll
     for (int j = 0; j < kDTiles; ++j)
       *reinterpret_cast<uint32_t*>(o0 + 8 * j + 2 * q4) = pack_bf16(o[j][0] * i0, o[j][1] * i0);
   }
-  if (tok1 < n) {
+  if (ok1) {
     __nv_bfloat16* o1 = obase + (((int64_t)s * a.n_max + tok1) * Hq + h * G + row1 % G) * D;
 #pragma unroll
     for (int j = 0; j < kDTiles; ++j)
@@ -355,18 +358,17 @@ __global__ void __launch_bounds__(256) chunk_append_kernel(const __grid_constant
   }
 }
 
-template <int D, int G>
+template <int D>
 constexpr int pf_smem() {
   return kPfStages * 2 * kTile * D * 2 + 1024;
 }
 
-template <int D, int G>
+template <int D>
 cudaError_t launch_pf(const PrefillArgs& a, const CUtensorMap* pm, const CUtensorMap* km, const CUtensorMap* vm,
                       int items, cudaStream_t st) {
-  static_assert(kPfRows % G == 0, "G must divide the query rows of a CTA");
-  cudaError_t e = cudaFuncSetAttribute(prefill_kernel<D, G>, cudaFuncAttributeMaxDynamicSharedMemorySize, pf_smem<D, G>());
+  cudaError_t e = cudaFuncSetAttribute(prefill_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, pf_smem<D>());
   if (e != cudaSuccess) return e;
-  prefill_kernel<D, G><<<items, kPfThreads, pf_smem<D, G>(), st>>>(*pm, *km, *vm, a);
+  prefill_kernel<D><<<items, kPfThreads, pf_smem<D>(), st>>>(*pm, *km, *vm, a);
   count_launches(1);
   return cudaGetLastError();
 }
@@ -378,12 +380,9 @@ int prefill_tokens_per_cta(int group) { return kPfRows / group; }
 cudaError_t launch_prefill(const PrefillArgs& a, const CUtensorMap* pool_map, const CUtensorMap* knew_map,
                            const CUtensorMap* vnew_map, cudaStream_t st) {
   const int items = a.pv.kv_heads * a.pv.num_seqs * a.q_tiles;
-  const int D = a.pv.head_dim, G = a.group;
-#define HWKV_PF(DD, GG) \
-  if (D == DD && G == GG) return launch_pf<DD, GG>(a, pool_map, knew_map, vnew_map, items, st);
-  HWKV_PF(128, 1) HWKV_PF(128, 2) HWKV_PF(128, 4) HWKV_PF(128, 8)
-  HWKV_PF(64, 1) HWKV_PF(64, 2) HWKV_PF(64, 4) HWKV_PF(64, 8)
-#undef HWKV_PF
+  if (a.group < 1 || a.group > kMaxGroup) return cudaErrorInvalidValue;
+  if (a.pv.head_dim == 128) return launch_pf<128>(a, pool_map, knew_map, vnew_map, items, st);
+  if (a.pv.head_dim == 64) return launch_pf<64>(a, pool_map, knew_map, vnew_map, items, st);
   return cudaErrorInvalidValue;
 }
 

@@ -155,7 +155,8 @@ int hwkv_decode_workspace_bytes(hwkv_pool_t pool, int q_heads, uint64_t* out);
  * h = q / G and w = w[layer][h]:
  *     out[s][q] = sum_{p in [max(0,len_s-w), len_s)} softmax_p(scale * <q, k_p>) v_p
  * computed with fp32 accumulation and an online softmax; out has the pool's dtype.
- *   q, out: device [num_seqs][q_heads][D], 16-byte aligned; q_heads = G * kv_heads, G <= 8.
+ *   q, out: device [num_seqs][q_heads][D], 16-byte aligned; q_heads = G * kv_heads, G <= 16
+ *           (the tensor-core kernel pads the group to 4, 8 or 16 query-head columns).
  *   lens_dev: device int32 [num_seqs], lengths AFTER this step's append.  len 0 gives 0s.
  *   workspace: device scratch of >= hwkv_decode_workspace_bytes(), 16-byte aligned; its
  *              contents need no initialisation and are clobbered.  Launches that may run
@@ -208,7 +209,7 @@ int hwkv_decode_attn_noalloc(hwkv_pool_t pool, int layer, const void* q, int q_h
  *   all 16-byte aligned.  pos_dev / n_dev: device int32 [num_seqs], lengths before the chunk
  *   and chunk lengths (0 <= n_s <= n_max, checked on the device; a bad sequence is skipped and
  *   flagged HWKV_DEVERR_NEG_LENGTH).  Rows of out at or past n_s are left untouched.
- * Needs a bf16 pool with block_size % 16 == 0 and q_heads / kv_heads in {1, 2, 4, 8}
+ * Needs a bf16 pool with block_size % 16 == 0 and q_heads = G * kv_heads with G <= 16
  * (HWKV_ERR_UNSUPPORTED otherwise).  Two kernels on `stream`; no workspace. */
 int hwkv_prefill_attn(hwkv_pool_t pool, int layer, const void* q, int q_heads, float scale, const void* k_new,
                       const void* v_new, int n_max, const int32_t* pos_dev, const int32_t* n_dev, void* out,

@@ -86,6 +86,11 @@ EDGE = {
     "g1_d64": dict(kv_heads=4, group=1, head_dim=64, windows=((64, 128, 32, 512),), prefill=(700, 90)),
     "g2": dict(kv_heads=2, group=2, windows=((256, 96),), prefill=(1000, 1000)),
     "g8": dict(kv_heads=2, group=8, windows=((2048, 160),), prefill=(3000, 100)),
+    # groups past one 8-column n-tile (16, and 12 padded to 16), and padded small groups
+    "g16": dict(kv_heads=2, group=16, windows=((4096, 96),), prefill=(5000, 300)),
+    "g12_d64": dict(kv_heads=2, group=12, head_dim=64, windows=((512, 2048),), prefill=(1500, 2100)),
+    "g3": dict(kv_heads=3, group=3, windows=((256, 64, 1024),), prefill=(900, 40)),
+    "g6": dict(kv_heads=2, group=6, windows=((128, 700),), prefill=(800, 650)),
     # bigger block size, several layers
     "bs64_layers": dict(layers=3, kv_heads=2, block_size=64, windows=((128, 1024), (64, 256), (4096, 64)),
                         prefill=(5000, 700, 64)),
@@ -170,7 +175,7 @@ def test_tensor_core_partition_changes_rounding_only(workers):
     run.close()
 
 
-@pytest.mark.parametrize("name", ["clip", "ring_c_gt_w", "g8", "bs64_layers", "bs5", "f32"])
+@pytest.mark.parametrize("name", ["clip", "ring_c_gt_w", "g8", "g16", "bs64_layers", "bs5", "f32"])
 def test_fused_append_decode_equals_append_then_decode(name):
     """hwkv_append_decode_attn gives the same pool bytes and the same outputs as hwkv_append
     followed by hwkv_decode_attn, and matches the oracle."""
@@ -290,6 +295,10 @@ def test_host_side_argument_errors():
     with pytest.raises(hw.HwkvError) as e:
         hw.hwkv_decode_attn(run.pool.handle, 0, qmis, cfg.scale, lens, out, run.pool.workspace)
     assert e.value.status == hw.binding.HWKV_ERR_ALIGNMENT
+    q17 = torch.zeros(1, cfg.kv_heads * 17, cfg.head_dim, dtype=torch.bfloat16, device=run.dev)  # group 17
+    with pytest.raises(hw.HwkvError) as e:
+        hw.hwkv_decode_attn(run.pool.handle, 0, q17, cfg.scale, lens, torch.empty_like(q17), run.pool.workspace)
+    assert e.value.status == hw.binding.HWKV_ERR_UNSUPPORTED
     with pytest.raises(hw.HwkvError) as e:
         hw.hwkv_set_block_table(run.pool.handle, np.zeros(run.pool.geometry()[1], np.int32))
     assert e.value.status == hw.binding.HWKV_ERR_INVALID_ARG

@@ -136,6 +136,10 @@ CASES = {
     "g1_d64": dict(kv_heads=2, group=1, head_dim=64, windows=((128, 64),), prefill=(200, 10), chunks=[[75, 130]]),
     "g2": dict(kv_heads=2, group=2, windows=((1000, 160),), prefill=(1500, 300), chunks=[[40, 21]]),
     "g8": dict(kv_heads=1, group=8, windows=((256,),), prefill=(400, 5), chunks=[[20, 17]]),
+    # group 16: four tokens per 64-row tile; groups 3 and 12 leave idle rows (21 and 5 tokens)
+    "g16": dict(kv_heads=2, group=16, windows=((96, 512),), prefill=(600, 7), chunks=[[45, 9]]),
+    "g3": dict(kv_heads=2, group=3, windows=((80, 300),), prefill=(350, 0), chunks=[[50, 64]]),
+    "g12_d64": dict(kv_heads=1, group=12, head_dim=64, windows=((200,),), prefill=(260, 33), chunks=[[23, 18]]),
     "bs64": dict(kv_heads=2, block_size=64, windows=((128, 1000),), prefill=(900, 64), chunks=[[77, 129]]),
 }
 
@@ -175,7 +179,7 @@ def test_prefill_equals_token_by_token_decode():
 def test_prefill_rejects_unsupported_shapes():
     cfg = small_config(name="rej", cfg_id=93, kv_heads=2, group=3, windows=((64, 64),), prefill=(10,))
     pool = hw.Pool(1, 2, 128, 16, cfg.windows_array(), 1, torch.bfloat16, q_heads=6)
-    q = torch.zeros(1, 4, 6, 128, dtype=torch.bfloat16, device="cuda")
+    q = torch.zeros(1, 4, 34, 128, dtype=torch.bfloat16, device="cuda")  # group 17
     k = torch.zeros(1, 4, 2, 128, dtype=torch.bfloat16, device="cuda")
     pos = torch.zeros(1, dtype=torch.int32, device="cuda")
     with pytest.raises(hw.HwkvError) as e:
