@@ -584,7 +584,7 @@ def run_prefill(args, cfg):
                        "global_batch": cfg.batch, "seq_len": max(cfg.prefill)},
             "roofline": {"bound": "tensor", "achieved": tflops, "peak": peak, "unit": "TFLOP/s",
                          "frac": tflops / peak, "traffic": None, "peak_kind": kind,
-                         "kernel": "prefill_kernel (mma.sync bf16) + chunk append, one pair per layer"}}
+                         "kernel": "prefill_kernel (tcgen05 bf16, accumulators in tensor memory) + chunk append, one pair per layer"}}
     print(json.dumps(line), flush=True)
 
 

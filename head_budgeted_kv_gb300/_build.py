@@ -1,6 +1,6 @@
 """In-tree build of libhwkv.so for sm_103a with nvcc (no torch extension machinery).
 
-The three translation units compile in parallel, then link into
+The translation units compile in parallel, then link into
 ``head_budgeted_kv_gb300/_build/libhwkv.so`` with the CUDA runtime linked statically.
 """
 from __future__ import annotations
@@ -18,7 +18,8 @@ BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(BUILD, "libhwkv.so")
 
 SOURCES = ("hwkv_host.cpp", "hwkv_copy.cu", "hwkv_decode_simt.cu", "hwkv_decode_tc.cu", "hwkv_noalloc.cu", "hwkv_prefill.cu")
-HEADERS = (os.path.join(CSRC, "hwkv_internal.h"), os.path.join(CSRC, "hwkv_device.cuh"), os.path.join(INCLUDE, "hwkv.h"))
+HEADERS = (os.path.join(CSRC, "hwkv_internal.h"), os.path.join(CSRC, "hwkv_device.cuh"),
+           os.path.join(CSRC, "hwkv_tcgen05.cuh"), os.path.join(INCLUDE, "hwkv.h"))
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-I", INCLUDE, "-I", CSRC]
 

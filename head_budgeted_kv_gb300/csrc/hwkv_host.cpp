@@ -666,7 +666,7 @@ int hwkv_prefill_attn(hwkv_pool_t p, int layer, const void* q, int q_heads, floa
   PFN_cuTensorMapEncodeTiled_v12000 encode = tensor_map_encoder();
   if (!encode) return fail(HWKV_ERR_CUDA, "cuTensorMapEncodeTiled is unavailable");
   // the chunk as a 3-D tensor (head_dim, kv_heads, seq * n_max + row): a box of 16 rows of one head
-  alignas(64) CUtensorMap kmap, vmap;
+  alignas(64) CUtensorMap kmap, vmap, qmap;
   const cuuint64_t dims[3] = {(cuuint64_t)g.head_dim, (cuuint64_t)g.kv_heads, (cuuint64_t)g.num_seqs * n_max};
   const cuuint64_t strides[2] = {(cuuint64_t)g.head_dim * 2, (cuuint64_t)g.kv_heads * g.head_dim * 2};
   const cuuint32_t box[3] = {64, 1, 16};
@@ -676,6 +676,18 @@ int hwkv_prefill_attn(hwkv_pool_t p, int layer, const void* q, int q_heads, floa
                          dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (cr != CUDA_SUCCESS) return fail(HWKV_ERR_CUDA, "tensor map of the chunk could not be encoded (%d)", (int)cr);
+  }
+  {
+    // the queries as (head_dim, q_heads, seq * n_max + row): a box of the G heads of one KV head
+    // for the tokens of one 128-row query tile
+    const int tt = prefill_tile_tokens(G);
+    const cuuint64_t qdims[3] = {(cuuint64_t)g.head_dim, (cuuint64_t)q_heads, (cuuint64_t)g.num_seqs * n_max};
+    const cuuint64_t qstrides[2] = {(cuuint64_t)g.head_dim * 2, (cuuint64_t)q_heads * g.head_dim * 2};
+    const cuuint32_t qbox[3] = {64, (cuuint32_t)G, (cuuint32_t)tt};
+    CUresult cr = encode(&qmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(q), qdims, qstrides, qbox, estr,
+                         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (cr != CUDA_SUCCESS) return fail(HWKV_ERR_CUDA, "tensor map of the queries could not be encoded (%d)", (int)cr);
   }
   PrefillArgs a;
   std::memset(&a, 0, sizeof a);
@@ -703,7 +715,7 @@ int hwkv_prefill_attn(hwkv_pool_t p, int layer, const void* q, int q_heads, floa
   }
   max_c *= g.block_size;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  HWKV_CUDA_TRY(launch_prefill(a, &p->tmap, &kmap, &vmap, st), "prefill launch");
+  HWKV_CUDA_TRY(launch_prefill(a, &p->tmap, &kmap, &vmap, &qmap, st), "prefill launch");
   HWKV_CUDA_TRY(launch_chunk_append(a, std::min(n_max, max_c), st), "chunk append launch");
   return ok();
 }

@@ -80,7 +80,7 @@ struct PrefillArgs {
   const int32_t* nlen;     // [B] chunk lengths (<= n_max)
   int32_t n_max;
   int32_t group;           // G = Hq / H
-  int32_t q_tiles;         // CTAs per (seq, head): ceil(n_max / tokens per CTA)
+  int32_t q_tiles;         // CTAs per (seq, head): ceil(n_max / chunk tokens per CTA)
   float scale_log2;
   int32_t head_order[kMaxKvHeads];  // heads by decreasing window (work order)
 };
@@ -105,9 +105,10 @@ int decode_tc_pad_index(int group);  // 0, 1, 2 for 4, 8, 16 columns
 cudaError_t launch_decode_simt(const DecodeArgs& a, int dtype, int items, cudaStream_t st);
 cudaError_t launch_combine(const DecodeArgs& a, int dtype, cudaStream_t st);
 // chunked prefill (hwkv_prefill.cu): attention, then the chunk appended to the rings
-int prefill_tokens_per_cta(int group);
+int prefill_tokens_per_cta(int group);  // chunk tokens one CTA answers (two query tiles)
+int prefill_tile_tokens(int group);     // chunk tokens of one 128-row query tile
 cudaError_t launch_prefill(const PrefillArgs& a, const CUtensorMap* pool_map, const CUtensorMap* knew_map,
-                           const CUtensorMap* vnew_map, cudaStream_t st);
+                           const CUtensorMap* vnew_map, const CUtensorMap* q_map, cudaStream_t st);
 cudaError_t launch_chunk_append(const PrefillArgs& a, int max_rows, cudaStream_t st);
 
 }  // namespace hwkv

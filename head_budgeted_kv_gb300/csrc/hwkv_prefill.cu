@@ -1,5 +1,6 @@
 // Chunked prefill over the per-head paged rings: windowed causal attention for a chunk of new
-// tokens, then the chunk's K/V written into the rings.
+// tokens on the sm_100-family tensor cores (tcgen05, accumulators in tensor memory), then the
+// chunk's K/V written into the rings.
 //
 // "HeadWiseKV: Budgeted Per-Head Cache Residency for Hybrid Long-Context Language Models",
 // abstract and section "Grouped-Cache Runtime": each KV head keeps only a static window w of
@@ -9,26 +10,57 @@
 // K/V rows.  Appending the chunk then overwrites ring slots that earlier queries of the same
 // chunk still read, so the append is a second launch after the attention.
 //
-// prefill_kernel (bf16, block_size % 16 == 0, head_dim 64 or 128, GQA group 1 <= G <= 16):
-//   CTA = (seq, kv head, query tile of 64 rows = floor(64/G) tokens x G query heads, the rows
-//   past the last whole token idle); 4 consumer
-//   warps own 16 rows each, a producer warp streams 16-token K/V tiles into a 4-stage ring of
-//   shared memory with TMA (pool tiles through the block table, chunk tiles through a tensor
-//   map of the chunk).  Per tile and warp: S[16 rows][16 keys] = Q K^T and O += P V with
-//   mma.sync.m16n8k16 bf16 -> fp32 (FlashAttention-2 register reuse of P), causal + window
-//   mask per row, online softmax in fp32 (log2 domain).  Waits are bounded (~2 s).
-#include "hwkv_device.cuh"
+// prefill_kernel<D> (bf16, block_size % 16 == 0, head_dim 64 or 128, GQA group 1 <= G <= 16):
+//   CTA = (seq, kv head, two query tiles of 128 rows); a tile holds floor(128 / G) tokens x G
+//   query heads (row r = token r / G, head r % G; rows past the last whole token idle).  Keys
+//   stream in stages of 64 (four 16-token ring or chunk tiles) through a ring of shared-memory
+//   stages filled by TMA (pool tiles through the block table, chunk tiles through a tensor map
+//   of the chunk).  Warp roles:
+//     warp 0      TMA producer (one lane),
+//     warp 1      tensor-memory owner and MMA issuer (one lane): per stage and query tile
+//                 S = Q . K^T (M 128, N 64, K = D) into tensor memory, and O += P . V
+//                 (M 128, N = D, K 64; V read MN-major) accumulated in tensor memory,
+//     warps 4-7   softmax of query tile 0, warps 8-11 of tile 1: thread i owns row i, loads
+//                 its S row from tensor memory, masks it (causal, window, resident slots),
+//                 runs the online softmax in fp32 (log2 domain) and writes its P row as bf16
+//                 to shared memory in the 128-byte-swizzled K-major layout the MMA reads.
+//   The running maximum used for P is raised only when a row's maximum grows by more than
+//   2^8 (then the row of O in tensor memory and its sum are rescaled), so P stays <= 256 and
+//   O is rarely touched between stages.  Every wait is bounded (~2 s); a timeout records
+//   HWKV_DEVERR_WAIT_TIMEOUT and all roles stop.
+#include "hwkv_tcgen05.cuh"
 
 namespace hwkv {
 namespace {
 
-constexpr int kPfConsumers = 4;            // consumer warps (16 query rows each)
-constexpr int kPfThreads = (kPfConsumers + 1) * 32;
-constexpr int kPfStages = 4;
-constexpr int kPfRows = kPfConsumers * 16;  // query rows per CTA
+constexpr int kPfM = 128;                  // query rows per tile (MMA M)
+constexpr int kPfKeys = 64;                // keys per stage (MMA N of S, K of P . V)
+constexpr int kPfSub = kPfKeys / kTile;    // ring / chunk tiles per stage
+constexpr int kPfThreads = 12 * 32;
 
-__device__ __forceinline__ uint32_t swz(int row, int d) {
-  return (uint32_t)((d >> 6) * 2048 + row * 128 + ((((d & 63) >> 3) ^ (row & 7)) << 4) + (d & 7) * 2);
+template <int D>
+struct PfCfg {
+  static constexpr int kHalves = D / 64;              // 128-byte column blocks of a row
+  static constexpr int kQBytes = kPfM * D * 2;        // one query tile
+  static constexpr int kKBytes = kPfKeys * D * 2;     // K (or V) of one stage
+  static constexpr int kStageBytes = 2 * kKBytes;
+  static constexpr int kStages = D == 128 ? 4 : 6;
+  static constexpr int kPBytes = kPfM * kPfKeys * 2;  // P of one query tile
+  static constexpr int kQOff = 0;
+  static constexpr int kStageOff = 2 * kQBytes;
+  static constexpr int kPOff = kStageOff + kStages * kStageBytes;
+  static constexpr int kSmem = kPOff + 2 * kPBytes + 1024;
+  // tensor-memory columns: S of tiles 0 / 1 (64 each), O of tiles 0 / 1 (D each)
+  static constexpr uint32_t kCols = D == 128 ? 512 : 256;
+  static constexpr uint32_t kColS = 0, kColO = 2 * kPfKeys;
+};
+
+__device__ __forceinline__ void tma_load_2d_l2(uint32_t dst, const CUtensorMap* map, int x, int y, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(
+          dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_addr(bar))
+      : "memory");
 }
 
 __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map, int x, int y, int z, uint64_t* bar) {
@@ -43,57 +75,90 @@ __device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
   asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(bar)) : "memory");
 }
 
+// Waits for a phase; gives up when another role has given up (`abort`) or after ~2 s, which
+// it records and announces.
+__device__ __forceinline__ bool pf_wait(uint64_t* bar, uint32_t parity, volatile int* abort, int32_t* err) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = global_timer_ns();
+  for (uint32_t i = 1;; ++i) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((i & 63u) == 0) {
+      if (*abort) return false;
+      if (global_timer_ns() - t0 > 2000000000ull) {
+        *abort = 1;
+        atomicOr(err, HWKV_DEVERR_WAIT_TIMEOUT);
+        return false;
+      }
+    }
+  }
+}
+
 // The key tiles one CTA streams: first the ring tiles holding the prior context its queries
 // may see, then the chunk tiles up to its last query.
 struct PfTiles {
-  // prior part (ring of the head at length p0)
   Resident rs;        // resident positions before the chunk
   int prior_first;    // ring tile of the oldest prior position needed
   int prior_tiles;    // number of ring tiles (cyclic from prior_first)
   int C16;
   int p_oldest;       // position held by ring slot rs.first_slot
-  // chunk part: chunk rows [16 * chunk_first, ...)
-  int chunk_first;
+  int chunk_first;    // chunk rows [16 * chunk_first, ...)
   int chunk_tiles;
 };
 
-template <int D>
-__global__ void __launch_bounds__(kPfThreads) prefill_kernel(const __grid_constant__ CUtensorMap pool_map,
-                                                            const __grid_constant__ CUtensorMap knew_map,
-                                                            const __grid_constant__ CUtensorMap vnew_map,
-                                                            const __grid_constant__ PrefillArgs a) {
-  constexpr int kHalves = D / 64;
-  constexpr int kTileBytes = kTile * D * 2;
-  constexpr int kStageBytes = 2 * kTileBytes;
-  constexpr int kSteps = D / 16;  // k-steps of QK
-  constexpr int kDTiles = D / 8;  // n-tiles of PV
+// Where the keys of one 16-token tile of the stream come from.
+struct PfKeyTile {
+  int kind;  // 0 ring, 1 chunk, 2 padding (no keys)
+  int a;     // ring: ring distance of the tile's first slot from the oldest resident slot;
+             // chunk: chunk row of the tile's first key
+};
 
+__device__ __forceinline__ PfKeyTile key_tile(const PfTiles& tl, int t, int C) {
+  PfKeyTile k;
+  if (t < tl.prior_tiles) {
+    int tile = tl.prior_first + t;
+    if (tile >= tl.C16) tile -= tl.C16;
+    int d = (tile << 4) - tl.rs.first_slot;
+    if (d < 0) d += C;
+    k.kind = 0;
+    k.a = d;
+  } else if (t < tl.prior_tiles + tl.chunk_tiles) {
+    k.kind = 1;
+    k.a = (tl.chunk_first + t - tl.prior_tiles) << 4;
+  } else {
+    k.kind = 2;
+    k.a = 0;
+  }
+  return k;
+}
+
+template <int D>
+__global__ void __launch_bounds__(kPfThreads, 1) prefill_kernel(const __grid_constant__ CUtensorMap pool_map,
+                                                               const __grid_constant__ CUtensorMap knew_map,
+                                                               const __grid_constant__ CUtensorMap vnew_map,
+                                                               const __grid_constant__ CUtensorMap q_map,
+                                                               const __grid_constant__ PrefillArgs a) {
+  using Cfg = PfCfg<D>;
+  constexpr int NS = Cfg::kStages;
   extern __shared__ uint8_t smem_dyn[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_dyn) + 1023) & ~uintptr_t(1023));
-  __shared__ __align__(8) uint64_t full[kPfStages], empty[kPfStages];
+  __shared__ __align__(8) uint64_t kv_full[NS], kv_empty[NS];
+  __shared__ __align__(8) uint64_t q_full, s_full[2], s_free[2], p_full[2], o_done[2], drain;
+  __shared__ uint32_t s_tmem;
+  __shared__ int s_abort;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int H = a.pv.kv_heads;
   const int G = a.group;
-  const int QT = kPfRows / G;  // tokens per CTA
+  const int QT = kPfM / G;  // tokens per query tile
   const int Hq = H * G;
   const int bs = a.pv.block_size;
 
-  // work item: heads in the host's order (longest windows first), then sequences, query tiles
+  // work item: heads in the host's order (longest windows first), then sequences, tile pairs
   const int per_head = a.pv.num_seqs * a.q_tiles;
   const int h = a.head_order[blockIdx.x / per_head];
   const int rem = blockIdx.x % per_head;
   const int s = rem / a.q_tiles;
   const int qt = rem % a.q_tiles;
-
-  if (threadIdx.x == 0) {
-    for (int i = 0; i < kPfStages; ++i) {
-      mbar_init(&full[i], 1);
-      mbar_init(&empty[i], kPfConsumers);
-    }
-    fence_mbar_init();
-  }
-  __syncthreads();
 
   const int p0 = a.pos0[s];
   const int n = a.nlen[s];
@@ -101,14 +166,14 @@ __global__ void __launch_bounds__(kPfThreads) prefill_kernel(const __grid_consta
     if (threadIdx.x == 0 && h == a.head_order[0] && qt == 0) atomicOr(a.pv.err, HWKV_DEVERR_NEG_LENGTH);
     return;
   }
-  const int qa = qt * QT;  // first chunk row of this CTA
+  const int qa = qt * 2 * QT;  // first chunk row of this CTA
   if (qa >= n) return;
-  const int qb = min(n, qa + QT);  // one past the last chunk row
+  const int qb = min(n, qa + 2 * QT);  // one past the last chunk row
   const int w = a.g.window[h];
   const int C = (a.g.nblk_prefix[h + 1] - a.g.nblk_prefix[h]) * bs;
   const int32_t* tbl = a.pv.tbl + a.g.tbl_base + (int64_t)s * a.g.tbl_seq_stride + a.g.nblk_prefix[h];
 
-  // tiles: prior positions [lo, p0) with lo = max(0, p0 + qa + 1 - w), chunk rows [clo, qb)
+  // key tiles: prior positions [lo, p0) with lo = max(0, p0 + qa + 1 - w), chunk rows [clo, qb)
   PfTiles tl;
   tl.rs = resident(p0, w, C);
   tl.C16 = C >> 4;
@@ -130,199 +195,327 @@ __global__ void __launch_bounds__(kPfThreads) prefill_kernel(const __grid_consta
     tl.chunk_tiles = ((qb - 1) >> 4) - tl.chunk_first + 1;
   }
   const int ntiles = tl.prior_tiles + tl.chunk_tiles;
+  const int nst = (ntiles + kPfSub - 1) / kPfSub;
 
-  if (warp == kPfConsumers) {
-    // ---- producer: one lane streams the tiles -----------------------------------------
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < NS; ++i) {
+      mbar_init(&kv_full[i], 1);
+      mbar_init(&kv_empty[i], 1);
+    }
+    mbar_init(&q_full, 1);
+    for (int x = 0; x < 2; ++x) {
+      mbar_init(&s_full[x], 1);
+      mbar_init(&s_free[x], 4);
+      mbar_init(&p_full[x], 4);
+      mbar_init(&o_done[x], 1);
+    }
+    mbar_init(&drain, 1);
+    s_abort = 0;
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(&s_tmem, Cfg::kCols);
+    tmem_relinquish();
+  }
+  tc_fence_before_sync();
+  __syncthreads();
+  tc_fence_after_sync();
+  const uint32_t tmem = s_tmem;
+  const uint32_t sbase = smem_addr(smem);
+  volatile int* abort = &s_abort;
+
+  if (warp == 0) {
+    // ---- TMA producer -----------------------------------------------------------------
     if (lane == 0) {
-      const uint64_t policy = evict_first_policy();
-      for (int t = 0; t < ntiles; ++t) {
-        const int st = t % kPfStages;
-        if (t >= kPfStages && !mbar_wait_bounded(&empty[st], (uint32_t)((t / kPfStages) - 1) & 1u)) {
-          atomicOr(a.pv.err, HWKV_DEVERR_WAIT_TIMEOUT);
-          break;
-        }
-        const uint32_t dst = smem_addr(smem) + st * kStageBytes;
-        mbar_arrive_expect_tx(&full[st], kStageBytes);
-        if (t < tl.prior_tiles) {
-          int tile = tl.prior_first + t;
-          if (tile >= tl.C16) tile -= tl.C16;
-          const int t0 = tile << 4;
-          const int jb = t0 / bs;
-          int32_t blk = tbl[jb];
-          if (blk < 0 || (int64_t)blk >= a.pv.total_blocks) {
-            atomicOr(a.pv.err, HWKV_DEVERR_BAD_BLOCK);
-            blk = 0;
-          }
-          const int row_k = blk * 2 * bs + (t0 - jb * bs);
+      // both query tiles: box of G heads x QT tokens x 64 columns per column block
+      mbar_arrive_expect_tx(&q_full, 2 * Cfg::kHalves * QT * G * 128);
+      for (int x = 0; x < 2; ++x)
+        for (int hf = 0; hf < Cfg::kHalves; ++hf)
+          tma_load_3d(sbase + Cfg::kQOff + x * Cfg::kQBytes + hf * (kPfM * 128), &q_map, hf * 64, h * G,
+                      s * a.n_max + qa + x * QT, &q_full);
+      int issued = 0;
+      for (int j = 0; j < nst; ++j) {
+        const int st = j % NS;
+        // pool rows of the stage's ring tiles (looked up before waiting for the slot); chunk
+        // tiles are -1; padding tiles past the stream read pool row 0 (finite, masked)
+        int row[kPfSub];
 #pragma unroll
-          for (int hf = 0; hf < kHalves; ++hf) {
-            tma_load_2d(dst + hf * 2048, &pool_map, hf * 64, row_k, &full[st], policy);
-            tma_load_2d(dst + kTileBytes + hf * 2048, &pool_map, hf * 64, row_k + bs, &full[st], policy);
+        for (int u = 0; u < kPfSub; ++u) {
+          const int t = j * kPfSub + u;
+          row[u] = 0;
+          if (t < tl.prior_tiles) {
+            int tile = tl.prior_first + t;
+            if (tile >= tl.C16) tile -= tl.C16;
+            const int t0 = tile << 4;
+            const int jb = t0 / bs;
+            int32_t blk = tbl[jb];
+            if (blk < 0 || (int64_t)blk >= a.pv.total_blocks) {
+              atomicOr(a.pv.err, HWKV_DEVERR_BAD_BLOCK);
+              blk = 0;
+            }
+            row[u] = blk * 2 * bs + (t0 - jb * bs);
+          } else if (t < ntiles) {
+            row[u] = -1;
           }
+        }
+        if (j >= NS && !pf_wait(&kv_empty[st], (uint32_t)((j / NS) - 1) & 1u, abort, a.pv.err)) break;
+        const uint32_t kdst = sbase + Cfg::kStageOff + st * Cfg::kStageBytes;
+        const uint32_t vdst = kdst + Cfg::kKBytes;
+        mbar_arrive_expect_tx(&kv_full[st], Cfg::kStageBytes);
+#pragma unroll
+        for (int u = 0; u < kPfSub; ++u) {
+#pragma unroll
+          for (int hf = 0; hf < Cfg::kHalves; ++hf) {
+            const uint32_t off = hf * (kPfKeys * 128) + u * (kTile * 128);
+            if (row[u] < 0) {
+              const int z = s * a.n_max + ((tl.chunk_first + j * kPfSub + u - tl.prior_tiles) << 4);
+              tma_load_3d(kdst + off, &knew_map, hf * 64, h, z, &kv_full[st]);
+              tma_load_3d(vdst + off, &vnew_map, hf * 64, h, z, &kv_full[st]);
+            } else {
+              tma_load_2d_l2(kdst + off, &pool_map, hf * 64, row[u], &kv_full[st]);
+              tma_load_2d_l2(vdst + off, &pool_map, hf * 64, row[u] + bs, &kv_full[st]);
+            }
+          }
+        }
+        ++issued;
+      }
+      if (*abort) {  // let the copies in flight land before the shared memory is released
+        for (int j = max(0, issued - NS); j < issued; ++j)
+          if (!mbar_wait_bounded(&kv_full[j % NS], (uint32_t)(j / NS) & 1u)) break;
+      }
+    }
+  } else if (warp == 1) {
+    // ---- MMA issuer -------------------------------------------------------------------
+    if (lane == 0) {
+      constexpr uint32_t idS = umma_idesc_bf16(kPfM, kPfKeys, false, false);
+      constexpr uint32_t idO = umma_idesc_bf16(kPfM, D, false, true);
+      bool ok = pf_wait(&q_full, 0, abort, a.pv.err);
+      for (int j = 0; ok && j <= nst; ++j) {
+        if (j < nst) {
+          // S_x = Q_x . K^T for both query tiles, as soon as each softmax has read its last S
+          const int st = j % NS;
+          ok = pf_wait(&kv_full[st], (uint32_t)(j / NS) & 1u, abort, a.pv.err);
+          if (!ok) break;
+          tc_fence_after_sync();
+          const uint32_t kaddr = sbase + Cfg::kStageOff + st * Cfg::kStageBytes;
+          for (int x = 0; x < 2 && ok; ++x) {
+            if (j > 0) {
+              ok = pf_wait(&s_free[x], (uint32_t)(j - 1) & 1u, abort, a.pv.err);
+              if (!ok) break;
+              tc_fence_after_sync();
+            }
+            const uint32_t qaddr = sbase + Cfg::kQOff + x * Cfg::kQBytes;
+#pragma unroll
+            for (int i = 0; i < D / 16; ++i) {
+              const uint32_t qo = (i >> 2) * (kPfM * 128) + (i & 3) * 32;
+              const uint32_t ko = (i >> 2) * (kPfKeys * 128) + (i & 3) * 32;
+              umma_bf16(tmem + Cfg::kColS + x * kPfKeys, umma_desc_sw128(qaddr + qo, 16, 1024),
+                        umma_desc_sw128(kaddr + ko, 16, 1024), idS, i > 0 ? 1u : 0u);
+            }
+            umma_commit(&s_full[x]);
+          }
+          if (!ok) break;
+        }
+        if (j > 0) {
+          // O_x += P_x . V of the previous stage, once each softmax has written its P
+          const int jp = j - 1, stp = jp % NS;
+          const uint32_t vaddr = sbase + Cfg::kStageOff + stp * Cfg::kStageBytes + Cfg::kKBytes;
+          for (int x = 0; x < 2 && ok; ++x) {
+            ok = pf_wait(&p_full[x], (uint32_t)jp & 1u, abort, a.pv.err);
+            if (!ok) break;
+            tc_fence_after_sync();
+            const uint32_t paddr = sbase + Cfg::kPOff + x * Cfg::kPBytes;
+#pragma unroll
+            for (int i = 0; i < kPfKeys / 16; ++i)
+              umma_bf16(tmem + Cfg::kColO + x * D, umma_desc_sw128(paddr + i * 32, 16, 1024),
+                        umma_desc_sw128(vaddr + i * (16 * 128), kPfKeys * 128, 1024), idO,
+                        (jp > 0 || i > 0) ? 1u : 0u);
+            umma_commit(&o_done[x]);
+          }
+          if (!ok) break;
+          umma_commit(&kv_empty[stp]);
+        }
+      }
+      umma_commit(&drain);  // every MMA issued above completes before tensor memory is freed
+      mbar_wait_bounded(&drain, 0);
+    }
+  } else if (warp >= 4) {
+    // ---- softmax of query tile x: thread = row ----------------------------------------
+    const int x = (warp - 4) >> 2;
+    const int quarter = warp & 3;
+    const int r = quarter * 32 + lane;  // row of the tile = tensor-memory lane
+    const int tok = qa + x * QT + r / G;
+    const bool live = r < QT * G && tok < n;
+    const int pq = p0 + tok;
+    const int t_first = qa + x * QT, t_last = min(n, qa + (x + 1) * QT) - 1;  // live tokens of the tile
+    const int pq_lo = p0 + t_first, pq_hi = p0 + t_last;
+    const uint32_t lane_base = tmem + ((uint32_t)(quarter * 32) << 16);
+    const uint32_t colS = Cfg::kColS + x * kPfKeys, colO = Cfg::kColO + x * D;
+    const uint32_t prow = sbase + Cfg::kPOff + x * Cfg::kPBytes + r * 128;
+    const float sl2 = a.scale_log2;
+    float m_ref = kNegInf, l = 0.f;
+    bool ok = true;
+    for (int j = 0; j < nst; ++j) {
+      ok = __all_sync(0xffffffffu, pf_wait(&s_full[x], (uint32_t)j & 1u, abort, a.pv.err));
+      if (!ok) break;
+      tc_fence_after_sync();
+      float sv[kPfKeys];
+      tmem_ld32(lane_base + colS, sv);
+      tmem_ld32(lane_base + colS + 32, sv + 32);
+      tc_fence_before_sync();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&s_free[x]);
+
+      // where the stage's keys come from; a "clean" stage needs no mask for any live row
+      PfKeyTile kt[kPfSub];
+      bool clean = t_first <= t_last;
+#pragma unroll
+      for (int u = 0; u < kPfSub; ++u) {
+        kt[u] = key_tile(tl, j * kPfSub + u, C);
+        int k_lo = 0;
+        if (kt[u].kind == 0) {
+          clean = clean && kt[u].a + kTile - 1 < tl.rs.n;
+          k_lo = tl.p_oldest + kt[u].a;
+        } else if (kt[u].kind == 1) {
+          clean = clean && kt[u].a + kTile - 1 < n;
+          k_lo = p0 + kt[u].a;
         } else {
-          const int z = s * a.n_max + ((tl.chunk_first + t - tl.prior_tiles) << 4);
+          clean = false;
+        }
+        clean = clean && k_lo + kTile - 1 <= pq_lo && k_lo > pq_hi - w;
+      }
+      float mx = kNegInf;
+      if (clean) {
 #pragma unroll
-          for (int hf = 0; hf < kHalves; ++hf) {
-            tma_load_3d(dst + hf * 2048, &knew_map, hf * 64, h, z, &full[st]);
-            tma_load_3d(dst + kTileBytes + hf * 2048, &vnew_map, hf * 64, h, z, &full[st]);
+        for (int c = 0; c < kPfKeys; ++c) {
+          sv[c] *= sl2;
+          mx = fmaxf(mx, sv[c]);
+        }
+      } else {
+#pragma unroll
+        for (int c = 0; c < kPfKeys; ++c) {
+          const int u = c >> 4, i = c & 15;
+          bool okk = false;
+          int kp = 0;
+          if (kt[u].kind == 0) {
+            int d = kt[u].a + i;
+            if (d >= C) d -= C;
+            okk = d < tl.rs.n;
+            kp = tl.p_oldest + d;
+          } else if (kt[u].kind == 1) {
+            const int rr = kt[u].a + i;
+            okk = rr < n;
+            kp = p0 + rr;
+          }
+          okk = okk && live && kp <= pq && kp > pq - w;
+          sv[c] = okk ? sv[c] * sl2 : kNegInf;
+          mx = fmaxf(mx, sv[c]);
+        }
+      }
+      const float m_new = fmaxf(m_ref, mx);
+      const bool grow = m_new > m_ref + 8.f;
+      // P buffer and O are this tile's to touch once the previous P . V has completed
+      if (j > 0) {
+        ok = __all_sync(0xffffffffu, pf_wait(&o_done[x], (uint32_t)(j - 1) & 1u, abort, a.pv.err));
+        if (!ok) break;
+        tc_fence_after_sync();
+        if (__any_sync(0xffffffffu, grow)) {
+          const float f = grow ? ex2(m_ref - m_new) : 1.f;
+#pragma unroll 1
+          for (int c = 0; c < D; c += 32) {
+            float o[32];
+            tmem_ld32(lane_base + colO + c, o);
+#pragma unroll
+            for (int e = 0; e < 32; ++e) o[e] *= f;
+            tmem_st32(lane_base + colO + c, o);
+          }
+        }
+      }
+      if (grow) {
+        l *= ex2(m_ref - m_new);
+        m_ref = m_new;
+      }
+      const float b = m_ref == kNegInf ? 0.f : m_ref;
+
+      // V rows past the chunk are zeroed: their P is 0, but 0 times a non-finite value is not
+      if (x == 0) {
+        bool need = false;
+#pragma unroll
+        for (int u = 0; u < kPfSub; ++u) need = need || (kt[u].kind == 1 && kt[u].a + kTile > n);
+        if (need) {
+          ok = __all_sync(0xffffffffu, pf_wait(&kv_full[j % NS], (uint32_t)(j / NS) & 1u, abort, a.pv.err));
+          if (!ok) break;
+          const uint32_t vst = sbase + Cfg::kStageOff + (j % NS) * Cfg::kStageBytes + Cfg::kKBytes;
+#pragma unroll
+          for (int u = 0; u < kPfSub; ++u) {
+            if (kt[u].kind == 1 && kt[u].a + kTile > n) {
+              const int i0 = max(0, n - kt[u].a);
+              const int nvec = (kTile - i0) * Cfg::kHalves * 8;
+              for (int e = r; e < nvec; e += kPfM) {
+                const int rr = i0 + e / (Cfg::kHalves * 8);
+                const int rem2 = e % (Cfg::kHalves * 8);
+                const uint32_t adr = vst + (rem2 >> 3) * (kPfKeys * 128) + (u * kTile + rr) * 128 + (rem2 & 7) * 16;
+                asm volatile("st.shared.v4.u32 [%0], {%1, %1, %1, %1};" ::"r"(adr), "r"(0u) : "memory");
+              }
+            }
+          }
+        }
+      }
+
+      // P row (bf16) in the 128-byte-swizzled K-major layout
+      float ls = 0.f;
+#pragma unroll
+      for (int k = 0; k < kPfKeys / 8; ++k) {
+        uint32_t pk[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const float pa = ex2(sv[8 * k + 2 * e] - b), pb = ex2(sv[8 * k + 2 * e + 1] - b);
+          ls += pa + pb;
+          pk[e] = pack_bf16(pa, pb);
+        }
+        asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(prow + ((k ^ (r & 7)) << 4)), "r"(pk[0]),
+                     "r"(pk[1]), "r"(pk[2]), "r"(pk[3])
+                     : "memory");
+      }
+      l += ls;
+      fence_proxy_async_smem();
+      tc_fence_before_sync();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&p_full[x]);
+    }
+    if (ok) ok = __all_sync(0xffffffffu, pf_wait(&o_done[x], (uint32_t)(nst - 1) & 1u, abort, a.pv.err));
+    if (ok) {
+      // normalise and store the row
+      tc_fence_after_sync();
+      const float inv = l > 0.f ? 1.f / l : 0.f;
+      __nv_bfloat16* orow = static_cast<__nv_bfloat16*>(a.out) +
+                            (((int64_t)s * a.n_max + (live ? tok : 0)) * Hq + h * G + r % G) * D;
+#pragma unroll 1
+      for (int c = 0; c < D; c += 32) {
+        float o[32];
+        tmem_ld32(lane_base + colO + c, o);
+        if (live) {
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            uint4 v;
+            v.x = pack_bf16(o[8 * k + 0] * inv, o[8 * k + 1] * inv);
+            v.y = pack_bf16(o[8 * k + 2] * inv, o[8 * k + 3] * inv);
+            v.z = pack_bf16(o[8 * k + 4] * inv, o[8 * k + 5] * inv);
+            v.w = pack_bf16(o[8 * k + 6] * inv, o[8 * k + 7] * inv);
+            *reinterpret_cast<uint4*>(orow + c + 8 * k) = v;
           }
         }
       }
     }
-    return;
   }
 
-  // ---- consumers: 16 query rows per warp; row r -> token qa + r / G, head r % G ----------
-  const int gq = lane >> 2, q4 = lane & 3;
-  const int row0 = warp * 16 + gq, row1 = row0 + 8;
-  const int tok0 = qa + row0 / G, tok1 = qa + row1 / G;  // chunk rows of the lane's two rows
-  const int pq0 = p0 + tok0, pq1 = p0 + tok1;            // their positions
-  // rows holding a real query: inside the CTA's whole tokens and the chunk
-  const bool ok0 = row0 < QT * G && tok0 < n, ok1 = row1 < QT * G && tok1 < n;
-  // Q as the A operand: lane holds rows row0/row1, dims 16i + 2*q4 + {0,1} and +8
-  uint32_t qf[kSteps][4];
-  {
-    const __nv_bfloat16* qbase = static_cast<const __nv_bfloat16*>(a.q);
-    const __nv_bfloat16* q0 = qbase + (((int64_t)s * a.n_max + (ok0 ? tok0 : 0)) * Hq + h * G + row0 % G) * D;
-    const __nv_bfloat16* q1 = qbase + (((int64_t)s * a.n_max + (ok1 ? tok1 : 0)) * Hq + h * G + row1 % G) * D;
-#pragma unroll
-    for (int i = 0; i < kSteps; ++i) {
-      const int d = 16 * i + 2 * q4;
-      qf[i][0] = ok0 ? *reinterpret_cast<const uint32_t*>(q0 + d) : 0u;
-      qf[i][1] = ok1 ? *reinterpret_cast<const uint32_t*>(q1 + d) : 0u;
-      qf[i][2] = ok0 ? *reinterpret_cast<const uint32_t*>(q0 + d + 8) : 0u;
-      qf[i][3] = ok1 ? *reinterpret_cast<const uint32_t*>(q1 + d + 8) : 0u;
-    }
-  }
-  float o[kDTiles][4];
-#pragma unroll
-  for (int j = 0; j < kDTiles; ++j) o[j][0] = o[j][1] = o[j][2] = o[j][3] = 0.f;
-  float m0 = kNegInf, m1 = kNegInf, l0 = 0.f, l1 = 0.f;  // rows row0, row1
-  const float sl2 = a.scale_log2;
-  const int mi = lane >> 3, rr = lane & 7;
-  const int k_key = rr + ((mi >> 1) << 3), k_dof = (mi & 1) << 3;  // K (B operand, non-transposed)
-  const int v_key = rr + ((mi & 1) << 3), v_dof = (mi >> 1) << 3;  // V (B operand, transposed)
-
-  for (int t = 0; t < ntiles; ++t) {
-    const int st = t % kPfStages;
-    if (!mbar_wait_bounded(&full[st], (uint32_t)(t / kPfStages) & 1u)) {
-      if (lane == 0) atomicOr(a.pv.err, HWKV_DEVERR_WAIT_TIMEOUT);
-      break;
-    }
-    const uint32_t sK = smem_addr(smem) + st * kStageBytes;
-    const uint32_t sV = sK + kTileBytes;
-
-    // positions of the lane's four keys (columns 2*q4, 2*q4 + 1 of each 8-key half)
-    int kp[4];
-    bool kv_ok[4];
-    if (t < tl.prior_tiles) {
-      int tile = tl.prior_first + t;
-      if (tile >= tl.C16) tile -= tl.C16;
-#pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        const int slot = (tile << 4) + (c >> 1) * 8 + 2 * q4 + (c & 1);
-        int d = slot - tl.rs.first_slot;
-        if (d < 0) d += C;
-        kv_ok[c] = d < tl.rs.n;
-        kp[c] = tl.p_oldest + d;
-      }
-    } else {
-      const int r0 = (tl.chunk_first + t - tl.prior_tiles) << 4;
-#pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        const int r = r0 + (c >> 1) * 8 + 2 * q4 + (c & 1);
-        kv_ok[c] = r < n;
-        kp[c] = p0 + r;
-      }
-    }
-
-    // S[16 rows][16 keys] = Q . K^T
-    float sc[2][4];
-#pragma unroll
-    for (int nt = 0; nt < 2; ++nt) sc[nt][0] = sc[nt][1] = sc[nt][2] = sc[nt][3] = 0.f;
-#pragma unroll
-    for (int i = 0; i < kSteps; ++i) {
-      uint32_t b[4];
-      ldsm_x4(b, sK + swz(k_key, 16 * i + k_dof));
-      const uint32_t a4[4] = {qf[i][0], qf[i][1], qf[i][2], qf[i][3]};
-      mma_bf16(sc[0], a4, b[0], b[1]);
-      mma_bf16(sc[1], a4, b[2], b[3]);
-    }
-    // mask: key position in [pq - w + 1, pq] of its row, and holding a real token
-    float x[2][4];
-#pragma unroll
-    for (int nt = 0; nt < 2; ++nt) {
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const int c = nt * 2 + (e & 1);
-        const int pq = (e < 2) ? pq0 : pq1;
-        const bool ok = kv_ok[c] && kp[c] <= pq && kp[c] > pq - w;
-        x[nt][e] = ok ? sc[nt][e] : kNegInf;
-      }
-    }
-    float mx0 = fmaxf(fmaxf(x[0][0], x[0][1]), fmaxf(x[1][0], x[1][1]));
-    float mx1 = fmaxf(fmaxf(x[0][2], x[0][3]), fmaxf(x[1][2], x[1][3]));
-#pragma unroll
-    for (int off = 1; off < 4; off <<= 1) {
-      mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, off));
-      mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, off));
-    }
-    const float n0 = fmaxf(m0, mx0 * sl2), n1 = fmaxf(m1, mx1 * sl2);
-    const float b0 = n0 == kNegInf ? 0.f : n0, b1 = n1 == kNegInf ? 0.f : n1;
-    const float al0 = ex2(m0 - b0), al1 = ex2(m1 - b1);
-    float p[2][4];
-#pragma unroll
-    for (int nt = 0; nt < 2; ++nt) {
-      p[nt][0] = ex2(fmaf(x[nt][0], sl2, -b0));
-      p[nt][1] = ex2(fmaf(x[nt][1], sl2, -b0));
-      p[nt][2] = ex2(fmaf(x[nt][2], sl2, -b1));
-      p[nt][3] = ex2(fmaf(x[nt][3], sl2, -b1));
-    }
-    l0 = fmaf(l0, al0, p[0][0] + p[0][1] + p[1][0] + p[1][1]);
-    l1 = fmaf(l1, al1, p[0][2] + p[0][3] + p[1][2] + p[1][3]);
-    m0 = n0;
-    m1 = n1;
-    // P as the A operand of O += P . V (16 rows x 16 keys)
-    const uint32_t pa[4] = {pack_bf16(p[0][0], p[0][1]), pack_bf16(p[0][2], p[0][3]), pack_bf16(p[1][0], p[1][1]),
-                            pack_bf16(p[1][2], p[1][3])};
-#pragma unroll
-    for (int j = 0; j < kDTiles; j += 2) {
-      uint32_t b[4];
-      ldsm_x4_trans(b, sV + swz(v_key, 8 * j + v_dof));
-      o[j][0] *= al0;
-      o[j][1] *= al0;
-      o[j][2] *= al1;
-      o[j][3] *= al1;
-      o[j + 1][0] *= al0;
-      o[j + 1][1] *= al0;
-      o[j + 1][2] *= al1;
-      o[j + 1][3] *= al1;
-      mma_bf16(o[j], pa, b[0], b[1]);
-      mma_bf16(o[j + 1], pa, b[2], b[3]);
-    }
-    __syncwarp();
-    if (lane == 0) mbar_arrive(&empty[st]);
-  }
-
-  // normalise and store the lane's two rows (row sums over the 4 lanes of a row)
-#pragma unroll
-  for (int off = 1; off < 4; off <<= 1) {
-    l0 += __shfl_xor_sync(0xffffffffu, l0, off);
-    l1 += __shfl_xor_sync(0xffffffffu, l1, off);
-  }
-  const float i0 = l0 > 0.f ? 1.f / l0 : 0.f, i1 = l1 > 0.f ? 1.f / l1 : 0.f;
-  __nv_bfloat16* obase = static_cast<__nv_bfloat16*>(a.out);
-  if (ok0) {
-    __nv_bfloat16* o0 = obase + (((int64_t)s * a.n_max + tok0) * Hq + h * G + row0 % G) * D;
-#pragma unroll
-    for (int j = 0; j < kDTiles; ++j)
-      *reinterpret_cast<uint32_t*>(o0 + 8 * j + 2 * q4) = pack_bf16(o[j][0] * i0, o[j][1] * i0);
-  }
-  if (ok1) {
-    __nv_bfloat16* o1 = obase + (((int64_t)s * a.n_max + tok1) * Hq + h * G + row1 % G) * D;
-#pragma unroll
-    for (int j = 0; j < kDTiles; ++j)
-      *reinterpret_cast<uint32_t*>(o1 + 8 * j + 2 * q4) = pack_bf16(o[j][2] * i1, o[j][3] * i1);
+  // teardown: every tensor-memory access has completed (loads wait, the issuer drained)
+  __syncwarp();
+  tc_fence_before_sync();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after_sync();
+    tmem_dealloc(tmem, Cfg::kCols);
   }
 }
 
@@ -359,30 +552,27 @@ __global__ void __launch_bounds__(256) chunk_append_kernel(const __grid_constant
 }
 
 template <int D>
-constexpr int pf_smem() {
-  return kPfStages * 2 * kTile * D * 2 + 1024;
-}
-
-template <int D>
 cudaError_t launch_pf(const PrefillArgs& a, const CUtensorMap* pm, const CUtensorMap* km, const CUtensorMap* vm,
-                      int items, cudaStream_t st) {
-  cudaError_t e = cudaFuncSetAttribute(prefill_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, pf_smem<D>());
+                      const CUtensorMap* qm, int items, cudaStream_t st) {
+  cudaError_t e = cudaFuncSetAttribute(prefill_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, PfCfg<D>::kSmem);
   if (e != cudaSuccess) return e;
-  prefill_kernel<D><<<items, kPfThreads, pf_smem<D>(), st>>>(*pm, *km, *vm, a);
+  prefill_kernel<D><<<items, kPfThreads, PfCfg<D>::kSmem, st>>>(*pm, *km, *vm, *qm, a);
   count_launches(1);
   return cudaGetLastError();
 }
 
 }  // namespace
 
-int prefill_tokens_per_cta(int group) { return kPfRows / group; }
+int prefill_tokens_per_cta(int group) { return 2 * (kPfM / group); }
+
+int prefill_tile_tokens(int group) { return kPfM / group; }
 
 cudaError_t launch_prefill(const PrefillArgs& a, const CUtensorMap* pool_map, const CUtensorMap* knew_map,
-                           const CUtensorMap* vnew_map, cudaStream_t st) {
+                           const CUtensorMap* vnew_map, const CUtensorMap* q_map, cudaStream_t st) {
   const int items = a.pv.kv_heads * a.pv.num_seqs * a.q_tiles;
   if (a.group < 1 || a.group > kMaxGroup) return cudaErrorInvalidValue;
-  if (a.pv.head_dim == 128) return launch_pf<128>(a, pool_map, knew_map, vnew_map, items, st);
-  if (a.pv.head_dim == 64) return launch_pf<64>(a, pool_map, knew_map, vnew_map, items, st);
+  if (a.pv.head_dim == 128) return launch_pf<128>(a, pool_map, knew_map, vnew_map, q_map, items, st);
+  if (a.pv.head_dim == 64) return launch_pf<64>(a, pool_map, knew_map, vnew_map, q_map, items, st);
   return cudaErrorInvalidValue;
 }
 
