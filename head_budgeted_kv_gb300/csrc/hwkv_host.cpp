@@ -160,6 +160,10 @@ struct hwkv_pool {
   std::vector<LayerPlan> plans;
   bool has_tmap = false;
   alignas(64) CUtensorMap tmap;
+  // the pool as (head_dim, 2 * block_size rows, block): one box of stage_tb rows of 64 / stage_tb
+  // consecutive blocks is 64 keys (K or V) of a prefill stage
+  alignas(64) CUtensorMap stage_map;
+  int stage_tb = 0;
 };
 
 namespace {
@@ -405,7 +409,17 @@ int hwkv_pool_create(int layers, int kv_heads, int head_dim, int block_size, con
       CUresult cr = encode(&p->tmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, p->dev_pool, dims, strides, box, estr,
                            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-      p->has_tmap = cr == CUDA_SUCCESS;
+      const int bs = p->g.block_size;
+      const int tb = bs == 16 ? 16 : bs == 32 ? 32 : (bs % 64 == 0 ? 64 : 16);
+      cuuint64_t sdims[3] = {(cuuint64_t)p->g.head_dim, (cuuint64_t)(2 * bs), (cuuint64_t)p->g.total_blocks};
+      cuuint64_t sstrides[2] = {(cuuint64_t)p->g.head_dim * 2, (cuuint64_t)2 * bs * p->g.head_dim * 2};
+      cuuint32_t sbox[3] = {64, (cuuint32_t)tb, (cuuint32_t)(64 / tb)};
+      cuuint32_t sestr[3] = {1, 1, 1};
+      CUresult cr2 = encode(&p->stage_map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, p->dev_pool, sdims, sstrides, sbox, sestr,
+                            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+      p->stage_tb = (bs == 16 || bs == 32 || bs % 64 == 0) ? tb : 0;
+      p->has_tmap = cr == CUDA_SUCCESS && cr2 == CUDA_SUCCESS;
     }
   }
   if (p->has_tmap) {
@@ -665,15 +679,17 @@ int hwkv_prefill_attn(hwkv_pool_t p, int layer, const void* q, int q_heads, floa
   if (rc != HWKV_OK) return rc;
   PFN_cuTensorMapEncodeTiled_v12000 encode = tensor_map_encoder();
   if (!encode) return fail(HWKV_ERR_CUDA, "cuTensorMapEncodeTiled is unavailable");
-  // the chunk as a 3-D tensor (head_dim, kv_heads, seq * n_max + row): a box of 16 rows of one head
-  alignas(64) CUtensorMap kmap, vmap, qmap;
+  // the chunk as a 3-D tensor (head_dim, kv_heads, seq * n_max + row): boxes of 16 and of 64
+  // rows of one head
+  alignas(64) CUtensorMap kmap, vmap, kmap64, vmap64, qmap;
   const cuuint64_t dims[3] = {(cuuint64_t)g.head_dim, (cuuint64_t)g.kv_heads, (cuuint64_t)g.num_seqs * n_max};
   const cuuint64_t strides[2] = {(cuuint64_t)g.head_dim * 2, (cuuint64_t)g.kv_heads * g.head_dim * 2};
-  const cuuint32_t box[3] = {64, 1, 16};
+  const cuuint32_t box[3] = {64, 1, 16}, box64[3] = {64, 1, 64};
   const cuuint32_t estr[3] = {1, 1, 1};
-  for (int kv = 0; kv < 2; ++kv) {
-    CUresult cr = encode(kv ? &vmap : &kmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(kv ? v_new : k_new),
-                         dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+  for (int kv = 0; kv < 4; ++kv) {
+    CUtensorMap* m = kv == 0 ? &kmap : kv == 1 ? &vmap : kv == 2 ? &kmap64 : &vmap64;
+    CUresult cr = encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>((kv & 1) ? v_new : k_new), dims,
+                         strides, kv < 2 ? box : box64, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (cr != CUDA_SUCCESS) return fail(HWKV_ERR_CUDA, "tensor map of the chunk could not be encoded (%d)", (int)cr);
   }
@@ -704,6 +720,10 @@ int hwkv_prefill_attn(hwkv_pool_t p, int layer, const void* q, int q_heads, floa
   const int qt = prefill_tokens_per_cta(G);
   a.q_tiles = (n_max + qt - 1) / qt;
   a.scale_log2 = scale * 1.4426950408889634f;
+  a.bs_log2 = -1;
+  for (int b = 0; b < 31; ++b)
+    if ((1 << b) == g.block_size) a.bs_log2 = b;
+  a.stage_tb = p->stage_tb;
   // longest windows first: their CTAs stream the most keys
   std::vector<int> order(g.kv_heads);
   for (int h = 0; h < g.kv_heads; ++h) order[h] = h;
@@ -715,7 +735,8 @@ int hwkv_prefill_attn(hwkv_pool_t p, int layer, const void* q, int q_heads, floa
   }
   max_c *= g.block_size;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  HWKV_CUDA_TRY(launch_prefill(a, &p->tmap, &kmap, &vmap, &qmap, st), "prefill launch");
+  HWKV_CUDA_TRY(launch_prefill(a, &p->tmap, &p->stage_map, &kmap, &vmap, &kmap64, &vmap64, &qmap, st),
+                "prefill launch");
   HWKV_CUDA_TRY(launch_chunk_append(a, std::min(n_max, max_c), st), "chunk append launch");
   return ok();
 }

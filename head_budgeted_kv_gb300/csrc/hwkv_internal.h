@@ -82,6 +82,8 @@ struct PrefillArgs {
   int32_t group;           // G = Hq / H
   int32_t q_tiles;         // CTAs per (seq, head): ceil(n_max / chunk tokens per CTA)
   float scale_log2;
+  int32_t bs_log2;         // log2(block_size), or -1 when it is not a power of two
+  int32_t stage_tb;        // rows of one block in a 64-key pool copy (16, 32, 64), 0: per-tile copies only
   int32_t head_order[kMaxKvHeads];  // heads by decreasing window (work order)
 };
 
@@ -107,8 +109,11 @@ cudaError_t launch_combine(const DecodeArgs& a, int dtype, cudaStream_t st);
 // chunked prefill (hwkv_prefill.cu): attention, then the chunk appended to the rings
 int prefill_tokens_per_cta(int group);  // chunk tokens one CTA answers (two query tiles)
 int prefill_tile_tokens(int group);     // chunk tokens of one 128-row query tile
-cudaError_t launch_prefill(const PrefillArgs& a, const CUtensorMap* pool_map, const CUtensorMap* knew_map,
-                           const CUtensorMap* vnew_map, const CUtensorMap* q_map, cudaStream_t st);
+// pool_map: 16-row tiles of the pool; stage_map: 64 keys of consecutive blocks (see
+// hwkv_pool::stage_map); knew/vnew maps: 16-row and 64-row boxes of the chunk
+cudaError_t launch_prefill(const PrefillArgs& a, const CUtensorMap* pool_map, const CUtensorMap* stage_map,
+                           const CUtensorMap* knew_map, const CUtensorMap* vnew_map, const CUtensorMap* knew64_map,
+                           const CUtensorMap* vnew64_map, const CUtensorMap* q_map, cudaStream_t st);
 cudaError_t launch_chunk_append(const PrefillArgs& a, int max_rows, cudaStream_t st);
 
 }  // namespace hwkv

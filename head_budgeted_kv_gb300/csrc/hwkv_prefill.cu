@@ -18,12 +18,15 @@
 //   of the chunk).  Warp roles:
 //     warp 0      TMA producer (one lane),
 //     warp 1      tensor-memory owner and MMA issuer (one lane): per stage and query tile
-//                 S = Q . K^T (M 128, N 64, K = D) into tensor memory, and O += P . V
-//                 (M 128, N = D, K 64; V read MN-major) accumulated in tensor memory,
+//                 S = Q . K^T (M 128, N 64, K = D; both operands in shared memory) into
+//                 tensor memory, and O += P . V (M 128, N = D, K 64; P read from tensor
+//                 memory, V from shared memory MN-major) accumulated in tensor memory,
 //     warps 4-7   softmax of query tile 0, warps 8-11 of tile 1: thread i owns row i, loads
 //                 its S row from tensor memory, masks it (causal, window, resident slots),
 //                 runs the online softmax in fp32 (log2 domain) and writes its P row as bf16
-//                 to shared memory in the 128-byte-swizzled K-major layout the MMA reads.
+//                 back over the first half of the S columns it came from.
+//   S is double-buffered per tile: the S of stage j + 2 is issued after the P . V of stage j
+//   that reads the same columns, and the tensor pipe runs them in issue order.
 //   The running maximum used for P is raised only when a row's maximum grows by more than
 //   2^8 (then the row of O in tensor memory and its sum are rescaled), so P stays <= 256 and
 //   O is rarely touched between stages.  Every wait is bounded (~2 s); a timeout records
@@ -44,15 +47,15 @@ struct PfCfg {
   static constexpr int kQBytes = kPfM * D * 2;        // one query tile
   static constexpr int kKBytes = kPfKeys * D * 2;     // K (or V) of one stage
   static constexpr int kStageBytes = 2 * kKBytes;
-  static constexpr int kStages = D == 128 ? 4 : 6;
-  static constexpr int kPBytes = kPfM * kPfKeys * 2;  // P of one query tile
+  static constexpr int kStages = D == 128 ? 5 : 8;
   static constexpr int kQOff = 0;
   static constexpr int kStageOff = 2 * kQBytes;
-  static constexpr int kPOff = kStageOff + kStages * kStageBytes;
-  static constexpr int kSmem = kPOff + 2 * kPBytes + 1024;
-  // tensor-memory columns: S of tiles 0 / 1 (64 each), O of tiles 0 / 1 (D each)
-  static constexpr uint32_t kCols = D == 128 ? 512 : 256;
-  static constexpr uint32_t kColS = 0, kColO = 2 * kPfKeys;
+  static constexpr int kSmem = kStageOff + kStages * kStageBytes + 1024;
+  // tensor-memory columns: S (then P, in its first 32 columns) of query tile x in buffer b at
+  // (2x + b) * 64 (two buffers per tile, so the next stage's S is computed while the softmax
+  // works on this one), O of tile x at 256 + x * D
+  static constexpr uint32_t kCols = 512;
+  static constexpr uint32_t kColO = 4 * kPfKeys;
 };
 
 __device__ __forceinline__ void tma_load_2d_l2(uint32_t dst, const CUtensorMap* map, int x, int y, uint64_t* bar) {
@@ -131,10 +134,20 @@ __device__ __forceinline__ PfKeyTile key_tile(const PfTiles& tl, int t, int C) {
   return k;
 }
 
+// bits lo .. hi (inclusive, clamped to 0 .. 15) of a 16-key tile
+__device__ __forceinline__ uint32_t range_bits(int lo, int hi) {
+  lo = max(lo, 0);
+  hi = min(hi, 15);
+  return lo > hi ? 0u : ((0xFFFFu >> (15 - hi)) & (0xFFFFu << lo));
+}
+
 template <int D>
 __global__ void __launch_bounds__(kPfThreads, 1) prefill_kernel(const __grid_constant__ CUtensorMap pool_map,
+                                                               const __grid_constant__ CUtensorMap stage_map,
                                                                const __grid_constant__ CUtensorMap knew_map,
                                                                const __grid_constant__ CUtensorMap vnew_map,
+                                                               const __grid_constant__ CUtensorMap knew64_map,
+                                                               const __grid_constant__ CUtensorMap vnew64_map,
                                                                const __grid_constant__ CUtensorMap q_map,
                                                                const __grid_constant__ PrefillArgs a) {
   using Cfg = PfCfg<D>;
@@ -142,7 +155,9 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_kernel(const __grid_con
   extern __shared__ uint8_t smem_dyn[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_dyn) + 1023) & ~uintptr_t(1023));
   __shared__ __align__(8) uint64_t kv_full[NS], kv_empty[NS];
-  __shared__ __align__(8) uint64_t q_full, s_full[2], s_free[2], p_full[2], o_done[2], drain;
+  // per query tile x and stage parity b (a phase of each barrier is one stage of that parity,
+  // so no waiter can fall two phases behind, which a parity wait could not detect)
+  __shared__ __align__(8) uint64_t q_full, s_full[2][2], p_full[2][2], o_done[2][2], o_final[2], drain;
   __shared__ uint32_t s_tmem;
   __shared__ int s_abort;
 
@@ -204,10 +219,12 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_kernel(const __grid_con
     }
     mbar_init(&q_full, 1);
     for (int x = 0; x < 2; ++x) {
-      mbar_init(&s_full[x], 1);
-      mbar_init(&s_free[x], 4);
-      mbar_init(&p_full[x], 4);
-      mbar_init(&o_done[x], 1);
+      for (int b = 0; b < 2; ++b) {
+        mbar_init(&s_full[x][b], 1);
+        mbar_init(&p_full[x][b], 4);
+        mbar_init(&o_done[x][b], 1);
+      }
+      mbar_init(&o_final[x], 1);
     }
     mbar_init(&drain, 1);
     s_abort = 0;
@@ -233,47 +250,96 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_kernel(const __grid_con
         for (int hf = 0; hf < Cfg::kHalves; ++hf)
           tma_load_3d(sbase + Cfg::kQOff + x * Cfg::kQBytes + hf * (kPfM * 128), &q_map, hf * 64, h * G,
                       s * a.n_max + qa + x * QT, &q_full);
-      int issued = 0;
-      for (int j = 0; j < nst; ++j) {
-        const int st = j % NS;
-        // pool rows of the stage's ring tiles (looked up before waiting for the slot); chunk
-        // tiles are -1; padding tiles past the stream read pool row 0 (finite, masked)
-        int row[kPfSub];
+      // block-table entries of a stage's ring tiles, fetched one stage ahead so their latency
+      // hides behind the wait for the slot (kind 0 ring tile, 1 chunk tile, 2 padding)
+      int nxt_kind[kPfSub], nxt_blk[kPfSub], nxt_r0[kPfSub];
+      auto fetch = [&](int j) {
 #pragma unroll
         for (int u = 0; u < kPfSub; ++u) {
           const int t = j * kPfSub + u;
-          row[u] = 0;
+          nxt_kind[u] = t < tl.prior_tiles ? 0 : (t < ntiles ? 1 : 2);
+          nxt_blk[u] = 0;
+          nxt_r0[u] = 0;
           if (t < tl.prior_tiles) {
             int tile = tl.prior_first + t;
             if (tile >= tl.C16) tile -= tl.C16;
             const int t0 = tile << 4;
-            const int jb = t0 / bs;
-            int32_t blk = tbl[jb];
-            if (blk < 0 || (int64_t)blk >= a.pv.total_blocks) {
-              atomicOr(a.pv.err, HWKV_DEVERR_BAD_BLOCK);
-              blk = 0;
-            }
-            row[u] = blk * 2 * bs + (t0 - jb * bs);
-          } else if (t < ntiles) {
-            row[u] = -1;
+            const int jb = a.bs_log2 >= 0 ? t0 >> a.bs_log2 : t0 / bs;
+            nxt_blk[u] = __ldg(tbl + jb);
+            nxt_r0[u] = t0 - jb * bs;
           }
         }
+      };
+      fetch(0);
+      int issued = 0;
+      for (int j = 0; j < nst; ++j) {
+        const int st = j % NS;
+        int kind[kPfSub], blk[kPfSub], r0[kPfSub];
+#pragma unroll
+        for (int u = 0; u < kPfSub; ++u) {
+          kind[u] = nxt_kind[u];
+          blk[u] = nxt_blk[u];
+          r0[u] = nxt_r0[u];
+        }
+        if (j + 1 < nst) fetch(j + 1);
+        // pool rows of the ring tiles (-1 for chunk tiles); padding tiles read pool row 0
+        // (finite, masked)
+        int row[kPfSub];
+        bool blk_ok = true;
+#pragma unroll
+        for (int u = 0; u < kPfSub; ++u) {
+          row[u] = kind[u] == 1 ? -1 : 0;
+          if (kind[u] == 0) {
+            int32_t b = blk[u];
+            if (b < 0 || (int64_t)b >= a.pv.total_blocks) {
+              atomicOr(a.pv.err, HWKV_DEVERR_BAD_BLOCK);
+              b = 0;
+              blk_ok = false;
+            }
+            row[u] = b * 2 * bs + r0[u];
+          }
+        }
+        // one copy per 64 keys when the stage's ring tiles lie in consecutive blocks the way a
+        // stage_map box covers them (box row 16u of (stage_tb rows) x (64 / stage_tb blocks)),
+        // or when the stage is all chunk rows
+        const int tb = a.stage_tb;
+        bool ring_stage = tb > 0 && blk_ok && kind[0] == 0 && kind[kPfSub - 1] == 0 && r0[0] + tb <= bs;
+#pragma unroll
+        for (int u = 1; u < kPfSub; ++u)
+          ring_stage = ring_stage && kind[u] == 0 && r0[u] == r0[0] + ((kTile * u) & (tb - 1)) &&
+                       blk[u] == blk[0] + (kTile * u) / max(tb, 1);
+        const bool chunk_stage = kind[0] == 1 && kind[kPfSub - 1] == 1;
         if (j >= NS && !pf_wait(&kv_empty[st], (uint32_t)((j / NS) - 1) & 1u, abort, a.pv.err)) break;
         const uint32_t kdst = sbase + Cfg::kStageOff + st * Cfg::kStageBytes;
         const uint32_t vdst = kdst + Cfg::kKBytes;
         mbar_arrive_expect_tx(&kv_full[st], Cfg::kStageBytes);
-#pragma unroll
-        for (int u = 0; u < kPfSub; ++u) {
+        if (ring_stage) {
 #pragma unroll
           for (int hf = 0; hf < Cfg::kHalves; ++hf) {
-            const uint32_t off = hf * (kPfKeys * 128) + u * (kTile * 128);
-            if (row[u] < 0) {
-              const int z = s * a.n_max + ((tl.chunk_first + j * kPfSub + u - tl.prior_tiles) << 4);
-              tma_load_3d(kdst + off, &knew_map, hf * 64, h, z, &kv_full[st]);
-              tma_load_3d(vdst + off, &vnew_map, hf * 64, h, z, &kv_full[st]);
-            } else {
-              tma_load_2d_l2(kdst + off, &pool_map, hf * 64, row[u], &kv_full[st]);
-              tma_load_2d_l2(vdst + off, &pool_map, hf * 64, row[u] + bs, &kv_full[st]);
+            tma_load_3d(kdst + hf * (kPfKeys * 128), &stage_map, hf * 64, r0[0], blk[0], &kv_full[st]);
+            tma_load_3d(vdst + hf * (kPfKeys * 128), &stage_map, hf * 64, bs + r0[0], blk[0], &kv_full[st]);
+          }
+        } else if (chunk_stage) {
+          const int z = s * a.n_max + ((tl.chunk_first + j * kPfSub - tl.prior_tiles) << 4);
+#pragma unroll
+          for (int hf = 0; hf < Cfg::kHalves; ++hf) {
+            tma_load_3d(kdst + hf * (kPfKeys * 128), &knew64_map, hf * 64, h, z, &kv_full[st]);
+            tma_load_3d(vdst + hf * (kPfKeys * 128), &vnew64_map, hf * 64, h, z, &kv_full[st]);
+          }
+        } else {
+#pragma unroll
+          for (int u = 0; u < kPfSub; ++u) {
+#pragma unroll
+            for (int hf = 0; hf < Cfg::kHalves; ++hf) {
+              const uint32_t off = hf * (kPfKeys * 128) + u * (kTile * 128);
+              if (row[u] < 0) {
+                const int z = s * a.n_max + ((tl.chunk_first + j * kPfSub + u - tl.prior_tiles) << 4);
+                tma_load_3d(kdst + off, &knew_map, hf * 64, h, z, &kv_full[st]);
+                tma_load_3d(vdst + off, &vnew_map, hf * 64, h, z, &kv_full[st]);
+              } else {
+                tma_load_2d_l2(kdst + off, &pool_map, hf * 64, row[u], &kv_full[st]);
+                tma_load_2d_l2(vdst + off, &pool_map, hf * 64, row[u] + bs, &kv_full[st]);
+              }
             }
           }
         }
@@ -285,56 +351,55 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_kernel(const __grid_con
       }
     }
   } else if (warp == 1) {
-    // ---- MMA issuer -------------------------------------------------------------------
+    // ---- MMA issuer: S of stage j + 2 is issued right after P . V of stage j ---------
     if (lane == 0) {
       constexpr uint32_t idS = umma_idesc_bf16(kPfM, kPfKeys, false, false);
       constexpr uint32_t idO = umma_idesc_bf16(kPfM, D, false, true);
       bool ok = pf_wait(&q_full, 0, abort, a.pv.err);
-      for (int j = 0; ok && j <= nst; ++j) {
-        if (j < nst) {
-          // S_x = Q_x . K^T for both query tiles, as soon as each softmax has read its last S
-          const int st = j % NS;
-          ok = pf_wait(&kv_full[st], (uint32_t)(j / NS) & 1u, abort, a.pv.err);
-          if (!ok) break;
+      // S_x = Q_x . K^T of stage j into buffer j % 2 (issued after the P . V of stage j - 2,
+      // which read the P written there)
+      auto issue_s = [&](int j) {
+        const int st = j % NS, b = j & 1;
+        ok = pf_wait(&kv_full[st], (uint32_t)(j / NS) & 1u, abort, a.pv.err);
+        if (!ok) return;
+        tc_fence_after_sync();
+        const uint32_t kaddr = sbase + Cfg::kStageOff + st * Cfg::kStageBytes;
+        for (int x = 0; x < 2; ++x) {
+          const uint32_t qaddr = sbase + Cfg::kQOff + x * Cfg::kQBytes;
+#pragma unroll
+          for (int i = 0; i < D / 16; ++i) {
+            const uint32_t qo = (i >> 2) * (kPfM * 128) + (i & 3) * 32;
+            const uint32_t ko = (i >> 2) * (kPfKeys * 128) + (i & 3) * 32;
+            umma_bf16(tmem + (2 * x + b) * kPfKeys, umma_desc_sw128(qaddr + qo, 16, 1024),
+                      umma_desc_sw128(kaddr + ko, 16, 1024), idS, i > 0 ? 1u : 0u);
+          }
+          umma_commit(&s_full[x][b]);
+        }
+      };
+      // O_x += P_x . V of stage j, once the softmax has written P_x into tensor memory
+      auto issue_pv = [&](int j) {
+        const int st = j % NS, b = j & 1;
+        const uint32_t vaddr = sbase + Cfg::kStageOff + st * Cfg::kStageBytes + Cfg::kKBytes;
+        for (int x = 0; x < 2; ++x) {
+          ok = pf_wait(&p_full[x][b], (uint32_t)(j >> 1) & 1u, abort, a.pv.err);
+          if (!ok) return;
           tc_fence_after_sync();
-          const uint32_t kaddr = sbase + Cfg::kStageOff + st * Cfg::kStageBytes;
-          for (int x = 0; x < 2 && ok; ++x) {
-            if (j > 0) {
-              ok = pf_wait(&s_free[x], (uint32_t)(j - 1) & 1u, abort, a.pv.err);
-              if (!ok) break;
-              tc_fence_after_sync();
-            }
-            const uint32_t qaddr = sbase + Cfg::kQOff + x * Cfg::kQBytes;
+          const uint32_t pcol = tmem + (2 * x + b) * kPfKeys;
 #pragma unroll
-            for (int i = 0; i < D / 16; ++i) {
-              const uint32_t qo = (i >> 2) * (kPfM * 128) + (i & 3) * 32;
-              const uint32_t ko = (i >> 2) * (kPfKeys * 128) + (i & 3) * 32;
-              umma_bf16(tmem + Cfg::kColS + x * kPfKeys, umma_desc_sw128(qaddr + qo, 16, 1024),
-                        umma_desc_sw128(kaddr + ko, 16, 1024), idS, i > 0 ? 1u : 0u);
-            }
-            umma_commit(&s_full[x]);
-          }
-          if (!ok) break;
+          for (int i = 0; i < kPfKeys / 16; ++i)
+            umma_bf16_tmem_a(tmem + Cfg::kColO + x * D, pcol + i * 8,
+                             umma_desc_sw128(vaddr + i * (16 * 128), kPfKeys * 128, 1024), idO,
+                             (j > 0 || i > 0) ? 1u : 0u);
+          umma_commit(&o_done[x][b]);
+          if (j == nst - 1) umma_commit(&o_final[x]);
         }
-        if (j > 0) {
-          // O_x += P_x . V of the previous stage, once each softmax has written its P
-          const int jp = j - 1, stp = jp % NS;
-          const uint32_t vaddr = sbase + Cfg::kStageOff + stp * Cfg::kStageBytes + Cfg::kKBytes;
-          for (int x = 0; x < 2 && ok; ++x) {
-            ok = pf_wait(&p_full[x], (uint32_t)jp & 1u, abort, a.pv.err);
-            if (!ok) break;
-            tc_fence_after_sync();
-            const uint32_t paddr = sbase + Cfg::kPOff + x * Cfg::kPBytes;
-#pragma unroll
-            for (int i = 0; i < kPfKeys / 16; ++i)
-              umma_bf16(tmem + Cfg::kColO + x * D, umma_desc_sw128(paddr + i * 32, 16, 1024),
-                        umma_desc_sw128(vaddr + i * (16 * 128), kPfKeys * 128, 1024), idO,
-                        (jp > 0 || i > 0) ? 1u : 0u);
-            umma_commit(&o_done[x]);
-          }
-          if (!ok) break;
-          umma_commit(&kv_empty[stp]);
-        }
+        umma_commit(&kv_empty[st]);
+      };
+      if (ok) issue_s(0);
+      if (ok && nst > 1) issue_s(1);
+      for (int j = 0; ok && j < nst; ++j) {
+        issue_pv(j);
+        if (ok && j + 2 < nst) issue_s(j + 2);
       }
       umma_commit(&drain);  // every MMA issued above completes before tensor memory is freed
       mbar_wait_bounded(&drain, 0);
@@ -350,21 +415,21 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_kernel(const __grid_con
     const int t_first = qa + x * QT, t_last = min(n, qa + (x + 1) * QT) - 1;  // live tokens of the tile
     const int pq_lo = p0 + t_first, pq_hi = p0 + t_last;
     const uint32_t lane_base = tmem + ((uint32_t)(quarter * 32) << 16);
-    const uint32_t colS = Cfg::kColS + x * kPfKeys, colO = Cfg::kColO + x * D;
-    const uint32_t prow = sbase + Cfg::kPOff + x * Cfg::kPBytes + r * 128;
+    const uint32_t colO = Cfg::kColO + x * D;
     const float sl2 = a.scale_log2;
+    // with a positive scale the row maximum is taken on raw scores and scale-and-subtract is
+    // one packed FMA; masked scores become -inf before scaling (+inf for a negative scale)
+    const bool pos_scale = sl2 > 0.f;
+    const float masked = pos_scale ? kNegInf : -kNegInf;
     float m_ref = kNegInf, l = 0.f;
     bool ok = true;
     for (int j = 0; j < nst; ++j) {
-      ok = __all_sync(0xffffffffu, pf_wait(&s_full[x], (uint32_t)j & 1u, abort, a.pv.err));
+      const int b = j & 1;
+      ok = __all_sync(0xffffffffu, pf_wait(&s_full[x][b], (uint32_t)(j >> 1) & 1u, abort, a.pv.err));
       if (!ok) break;
       tc_fence_after_sync();
       float sv[kPfKeys];
-      tmem_ld32(lane_base + colS, sv);
-      tmem_ld32(lane_base + colS + 32, sv + 32);
-      tc_fence_before_sync();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&s_free[x]);
+      tmem_ld64(lane_base + (2 * x + b) * kPfKeys, sv);
 
       // where the stage's keys come from; a "clean" stage needs no mask for any live row
       PfKeyTile kt[kPfSub];
@@ -384,42 +449,58 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_kernel(const __grid_con
         }
         clean = clean && k_lo + kTile - 1 <= pq_lo && k_lo > pq_hi - w;
       }
-      float mx = kNegInf;
-      if (clean) {
+      if (!clean) {
+        // visible keys of this row per 16-key tile: position in (pq - w, pq], resident or in
+        // the chunk, as intervals of the tile's key index
 #pragma unroll
-        for (int c = 0; c < kPfKeys; ++c) {
-          sv[c] *= sl2;
-          mx = fmaxf(mx, sv[c]);
-        }
-      } else {
-#pragma unroll
-        for (int c = 0; c < kPfKeys; ++c) {
-          const int u = c >> 4, i = c & 15;
-          bool okk = false;
-          int kp = 0;
+        for (int u = 0; u < kPfSub; ++u) {
+          uint32_t vis = 0;
+          const int ka = kt[u].a;
           if (kt[u].kind == 0) {
-            int d = kt[u].a + i;
-            if (d >= C) d -= C;
-            okk = d < tl.rs.n;
-            kp = tl.p_oldest + d;
+            // ring distance d = ka + i (wrapping at C) holds position p_oldest + d
+            const int dlo = max(0, pq - w + 1 - tl.p_oldest), dhi = min(tl.rs.n - 1, pq - tl.p_oldest);
+            vis = range_bits(dlo - ka, min(dhi - ka, C - 1 - ka));
+            if (ka + kTile > C) vis |= range_bits(max(dlo - ka + C, C - ka), dhi - ka + C);
           } else if (kt[u].kind == 1) {
-            const int rr = kt[u].a + i;
-            okk = rr < n;
-            kp = p0 + rr;
+            vis = range_bits(pq - w + 1 - p0 - ka, min(n - 1 - ka, pq - p0 - ka));
           }
-          okk = okk && live && kp <= pq && kp > pq - w;
-          sv[c] = okk ? sv[c] * sl2 : kNegInf;
+          if (!live) vis = 0;
+#pragma unroll
+          for (int i = 0; i < kTile; ++i) sv[u * kTile + i] = (vis >> i) & 1u ? sv[u * kTile + i] : masked;
+        }
+      }
+      // row maximum in log2 units
+      float mx;
+      if (pos_scale) {
+        // a tree of three-input maxima (64 -> 22 -> 8 -> 3 -> 1), not a dependent chain
+        float t1[22], t2[8], t3[3];
+#pragma unroll
+        for (int i = 0; i < 21; ++i) t1[i] = fmax3(sv[3 * i], sv[3 * i + 1], sv[3 * i + 2]);
+        t1[21] = sv[63];
+#pragma unroll
+        for (int i = 0; i < 7; ++i) t2[i] = fmax3(t1[3 * i], t1[3 * i + 1], t1[3 * i + 2]);
+        t2[7] = t1[21];
+        t3[0] = fmax3(t2[0], t2[1], t2[2]);
+        t3[1] = fmax3(t2[3], t2[4], t2[5]);
+        t3[2] = fmaxf(t2[6], t2[7]);
+        const float m3 = fmax3(t3[0], t3[1], t3[2]);
+        mx = m3 == kNegInf ? kNegInf : m3 * sl2;
+      } else {
+        mx = kNegInf;
+#pragma unroll
+        for (int c = 0; c < kPfKeys; ++c) {
+          sv[c] = sv[c] == -kNegInf ? kNegInf : sv[c] * sl2;
           mx = fmaxf(mx, sv[c]);
         }
       }
       const float m_new = fmaxf(m_ref, mx);
       const bool grow = m_new > m_ref + 8.f;
-      // P buffer and O are this tile's to touch once the previous P . V has completed
-      if (j > 0) {
-        ok = __all_sync(0xffffffffu, pf_wait(&o_done[x], (uint32_t)(j - 1) & 1u, abort, a.pv.err));
+      // O may be rescaled once the previous P . V into it has completed
+      if (j > 0 && __any_sync(0xffffffffu, grow)) {
+        ok = __all_sync(0xffffffffu, pf_wait(&o_done[x][(j - 1) & 1], (uint32_t)((j - 1) >> 1) & 1u, abort, a.pv.err));
         if (!ok) break;
         tc_fence_after_sync();
-        if (__any_sync(0xffffffffu, grow)) {
+        {
           const float f = grow ? ex2(m_ref - m_new) : 1.f;
 #pragma unroll 1
           for (int c = 0; c < D; c += 32) {
@@ -435,7 +516,7 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_kernel(const __grid_con
         l *= ex2(m_ref - m_new);
         m_ref = m_new;
       }
-      const float b = m_ref == kNegInf ? 0.f : m_ref;
+      const float bm = m_ref == kNegInf ? 0.f : m_ref;
 
       // V rows past the chunk are zeroed: their P is 0, but 0 times a non-finite value is not
       if (x == 0) {
@@ -459,31 +540,30 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_kernel(const __grid_con
               }
             }
           }
+          fence_proxy_async_smem();  // before the P . V reads the stage
         }
       }
 
-      // P row (bf16) in the 128-byte-swizzled K-major layout
-      float ls = 0.f;
+      // P row (bf16 pairs) over the S columns it came from: p = 2^(s * scale_log2 - m_ref)
+      const float2 sl2v = make_float2(pos_scale ? sl2 : 1.f, pos_scale ? sl2 : 1.f);
+      const float2 nb = make_float2(-bm, -bm);
+      float2 ls[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
+      float pk[kPfKeys / 2];
 #pragma unroll
-      for (int k = 0; k < kPfKeys / 8; ++k) {
-        uint32_t pk[4];
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const float pa = ex2(sv[8 * k + 2 * e] - b), pb = ex2(sv[8 * k + 2 * e + 1] - b);
-          ls += pa + pb;
-          pk[e] = pack_bf16(pa, pb);
-        }
-        asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(prow + ((k ^ (r & 7)) << 4)), "r"(pk[0]),
-                     "r"(pk[1]), "r"(pk[2]), "r"(pk[3])
-                     : "memory");
+      for (int c = 0; c < kPfKeys / 2; ++c) {
+        const float2 t = ffma2(make_float2(sv[2 * c], sv[2 * c + 1]), sl2v, nb);
+        const float2 pp = make_float2(ex2(t.x), ex2(t.y));
+        ls[c & 3] = fadd2(ls[c & 3], pp);
+        pk[c] = __uint_as_float(pack_bf16(pp.x, pp.y));
       }
-      l += ls;
-      fence_proxy_async_smem();
+      l += ((ls[0].x + ls[0].y) + (ls[1].x + ls[1].y)) + ((ls[2].x + ls[2].y) + (ls[3].x + ls[3].y));
+      tmem_st32(lane_base + (2 * x + b) * kPfKeys, pk);
       tc_fence_before_sync();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&p_full[x]);
+      if (lane == 0) mbar_arrive(&p_full[x][b]);
     }
-    if (ok) ok = __all_sync(0xffffffffu, pf_wait(&o_done[x], (uint32_t)(nst - 1) & 1u, abort, a.pv.err));
+    // the last P . V into O
+    if (ok) ok = __all_sync(0xffffffffu, pf_wait(&o_final[x], 0u, abort, a.pv.err));
     if (ok) {
       // normalise and store the row
       tc_fence_after_sync();
@@ -552,11 +632,12 @@ __global__ void __launch_bounds__(256) chunk_append_kernel(const __grid_constant
 }
 
 template <int D>
-cudaError_t launch_pf(const PrefillArgs& a, const CUtensorMap* pm, const CUtensorMap* km, const CUtensorMap* vm,
-                      const CUtensorMap* qm, int items, cudaStream_t st) {
+cudaError_t launch_pf(const PrefillArgs& a, const CUtensorMap* pm, const CUtensorMap* sm, const CUtensorMap* km,
+                      const CUtensorMap* vm, const CUtensorMap* km64, const CUtensorMap* vm64, const CUtensorMap* qm,
+                      int items, cudaStream_t st) {
   cudaError_t e = cudaFuncSetAttribute(prefill_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, PfCfg<D>::kSmem);
   if (e != cudaSuccess) return e;
-  prefill_kernel<D><<<items, kPfThreads, PfCfg<D>::kSmem, st>>>(*pm, *km, *vm, *qm, a);
+  prefill_kernel<D><<<items, kPfThreads, PfCfg<D>::kSmem, st>>>(*pm, *sm, *km, *vm, *km64, *vm64, *qm, a);
   count_launches(1);
   return cudaGetLastError();
 }
@@ -567,12 +648,15 @@ int prefill_tokens_per_cta(int group) { return 2 * (kPfM / group); }
 
 int prefill_tile_tokens(int group) { return kPfM / group; }
 
-cudaError_t launch_prefill(const PrefillArgs& a, const CUtensorMap* pool_map, const CUtensorMap* knew_map,
-                           const CUtensorMap* vnew_map, const CUtensorMap* q_map, cudaStream_t st) {
+cudaError_t launch_prefill(const PrefillArgs& a, const CUtensorMap* pool_map, const CUtensorMap* stage_map,
+                           const CUtensorMap* knew_map, const CUtensorMap* vnew_map, const CUtensorMap* knew64_map,
+                           const CUtensorMap* vnew64_map, const CUtensorMap* q_map, cudaStream_t st) {
   const int items = a.pv.kv_heads * a.pv.num_seqs * a.q_tiles;
   if (a.group < 1 || a.group > kMaxGroup) return cudaErrorInvalidValue;
-  if (a.pv.head_dim == 128) return launch_pf<128>(a, pool_map, knew_map, vnew_map, q_map, items, st);
-  if (a.pv.head_dim == 64) return launch_pf<64>(a, pool_map, knew_map, vnew_map, q_map, items, st);
+  if (a.pv.head_dim == 128)
+    return launch_pf<128>(a, pool_map, stage_map, knew_map, vnew_map, knew64_map, vnew64_map, q_map, items, st);
+  if (a.pv.head_dim == 64)
+    return launch_pf<64>(a, pool_map, stage_map, knew_map, vnew_map, knew64_map, vnew64_map, q_map, items, st);
   return cudaErrorInvalidValue;
 }
 

@@ -141,6 +141,9 @@ CASES = {
     "g3": dict(kv_heads=2, group=3, windows=((80, 300),), prefill=(350, 0), chunks=[[50, 64]]),
     "g12_d64": dict(kv_heads=1, group=12, head_dim=64, windows=((200,),), prefill=(260, 33), chunks=[[23, 18]]),
     "bs64": dict(kv_heads=2, block_size=64, windows=((128, 1000),), prefill=(900, 64), chunks=[[77, 129]]),
+    # long key streams (about 130 stages of 64 keys per CTA), so the kernel's pipeline barriers
+    # run through many phases
+    "deep": dict(kv_heads=2, windows=((8192, 2048),), prefill=(9000, 2100), chunks=[[160, 70]]),
 }
 
 
