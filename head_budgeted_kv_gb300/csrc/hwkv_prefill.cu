@@ -356,6 +356,13 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_kernel(const __grid_con
       constexpr uint32_t idS = umma_idesc_bf16(kPfM, kPfKeys, false, false);
       constexpr uint32_t idO = umma_idesc_bf16(kPfM, D, false, true);
       bool ok = pf_wait(&q_full, 0, abort, a.pv.err);
+      // Descriptors are built once; an operand's start address moves by adding its offset in
+      // 16-byte units to the low field (shared addresses stay below 2^18 bytes, so the
+      // 14-bit field does not carry).  One thread issues every MMA, so this arithmetic is on
+      // the tensor pipe's critical path.
+      const uint64_t dq = umma_desc_sw128(sbase + Cfg::kQOff, 16, 1024);
+      const uint64_t dk = umma_desc_sw128(sbase + Cfg::kStageOff, 16, 1024);
+      const uint64_t dv = umma_desc_sw128(sbase + Cfg::kStageOff + Cfg::kKBytes, kPfKeys * 128, 1024);
       // S_x = Q_x . K^T of stage j into buffer j % 2 (issued after the P . V of stage j - 2,
       // which read the P written there)
       auto issue_s = [&](int j) {
@@ -363,15 +370,15 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_kernel(const __grid_con
         ok = pf_wait(&kv_full[st], (uint32_t)(j / NS) & 1u, abort, a.pv.err);
         if (!ok) return;
         tc_fence_after_sync();
-        const uint32_t kaddr = sbase + Cfg::kStageOff + st * Cfg::kStageBytes;
+        const uint64_t dks = dk + (uint64_t)((st * Cfg::kStageBytes) >> 4);
+#pragma unroll
         for (int x = 0; x < 2; ++x) {
-          const uint32_t qaddr = sbase + Cfg::kQOff + x * Cfg::kQBytes;
 #pragma unroll
           for (int i = 0; i < D / 16; ++i) {
-            const uint32_t qo = (i >> 2) * (kPfM * 128) + (i & 3) * 32;
-            const uint32_t ko = (i >> 2) * (kPfKeys * 128) + (i & 3) * 32;
-            umma_bf16(tmem + (2 * x + b) * kPfKeys, umma_desc_sw128(qaddr + qo, 16, 1024),
-                      umma_desc_sw128(kaddr + ko, 16, 1024), idS, i > 0 ? 1u : 0u);
+            constexpr int kQRow = kPfM * 128, kKRow = kPfKeys * 128;
+            umma_bf16(tmem + (2 * x + b) * kPfKeys,
+                      dq + (uint64_t)((x * Cfg::kQBytes + (i >> 2) * kQRow + (i & 3) * 32) >> 4),
+                      dks + (uint64_t)(((i >> 2) * kKRow + (i & 3) * 32) >> 4), idS, i > 0 ? 1u : 0u);
           }
           umma_commit(&s_full[x][b]);
         }
@@ -379,7 +386,8 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_kernel(const __grid_con
       // O_x += P_x . V of stage j, once the softmax has written P_x into tensor memory
       auto issue_pv = [&](int j) {
         const int st = j % NS, b = j & 1;
-        const uint32_t vaddr = sbase + Cfg::kStageOff + st * Cfg::kStageBytes + Cfg::kKBytes;
+        const uint64_t dvs = dv + (uint64_t)((st * Cfg::kStageBytes) >> 4);
+#pragma unroll
         for (int x = 0; x < 2; ++x) {
           ok = pf_wait(&p_full[x][b], (uint32_t)(j >> 1) & 1u, abort, a.pv.err);
           if (!ok) return;
@@ -387,8 +395,7 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_kernel(const __grid_con
           const uint32_t pcol = tmem + (2 * x + b) * kPfKeys;
 #pragma unroll
           for (int i = 0; i < kPfKeys / 16; ++i)
-            umma_bf16_tmem_a(tmem + Cfg::kColO + x * D, pcol + i * 8,
-                             umma_desc_sw128(vaddr + i * (16 * 128), kPfKeys * 128, 1024), idO,
+            umma_bf16_tmem_a(tmem + Cfg::kColO + x * D, pcol + i * 8, dvs + (uint64_t)((i * 16 * 128) >> 4), idO,
                              (j > 0 || i > 0) ? 1u : 0u);
           umma_commit(&o_done[x][b]);
           if (j == nst - 1) umma_commit(&o_final[x]);

@@ -189,3 +189,40 @@ def test_prefill_rejects_unsupported_shapes():
         pool.prefill(0, q, 0.1, k, k, pos, pos)
     assert e.value.status == hw.binding.HWKV_ERR_UNSUPPORTED
     pool.close()
+
+
+@pytest.mark.slow
+@pytest.mark.parametrize("name", ["full", "long"])
+def test_prefill_full_size_sampled(name):
+    """One layer of the full-size geometry in the configuration bench.py's prefill mode times
+    (a chunk of 2048 tokens per sequence on top of the context): sampled tokens of every
+    sequence, all query heads, against the oracle; device error word clear."""
+    cfg = workloads.config(name).with_layers(1)
+    dev = torch.device("cuda")
+    wl = workloads.Workload(cfg, device=dev)
+    pool = hw.Pool(cfg.layers, cfg.kv_heads, cfg.head_dim, cfg.block_size, cfg.windows_array(), cfg.batch,
+                   torch.bfloat16, q_heads=cfg.q_heads)
+    pre = torch.tensor(cfg.prefill, dtype=torch.int32, device=dev)
+    K, V = wl.prefill_layer(0, dev)
+    pool.materialize(0, K, V, pre)
+    n = 2048
+    q, k, v = wl.chunk_inputs(0, 0, n, dev)
+    out = pool.prefill(0, q, cfg.scale, k, v, pre, torch.full((cfg.batch,), n, dtype=torch.int32, device=dev))
+    torch.cuda.synchronize()
+    assert pool.check_device_errors() == 0
+    toks = [0, 1, 63, 64, 127, 1000, 2047]
+    for s in range(cfg.batch):
+        L = int(cfg.prefill[s])
+        for t in toks:
+            p = L + t
+            spans = {}
+            for h in range(cfg.kv_heads):
+                lo = max(0, p + 1 - int(cfg.windows[0][h]))  # first position of the window
+                c0 = max(0, lo - L)                           # first chunk row in it
+                kh = np.concatenate([_raw(K[s, h, lo:L]), _raw(k[s, c0:t + 1, h])])
+                vh = np.concatenate([_raw(V[s, h, lo:L]), _raw(v[s, c0:t + 1, h])])
+                spans[(0, h)] = (lo, kh, vh)
+            ref = oracle.attention_jobs(_raw(q[s, t])[None], spans, [p + 1], cfg.windows[0], cfg.scale)[0]
+            got = out[s, t].float().cpu().double().numpy()
+            assert_close(got, ref, cfg, f"{name} seq {s} token {t}")
+    pool.close()
