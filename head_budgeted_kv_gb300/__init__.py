@@ -21,15 +21,16 @@ from .binding import (HWKV_BF16, HWKV_F32, HWKV_KERNEL_AUTO, HWKV_KERNEL_SIMT, H
                       hwkv_check_device_errors, hwkv_kernel_launches,
                       hwkv_decode_attn, hwkv_decode_workspace_bytes, hwkv_materialize, hwkv_pool_bytes,
                       hwkv_pool_create, hwkv_pool_destroy, hwkv_pool_geometry, hwkv_prefill_attn,
-                      hwkv_set_block_table, hwkv_set_decode_config)
+                      hwkv_prefill_workspace_bytes, hwkv_set_block_table, hwkv_set_decode_config,
+                      hwkv_set_prefill_config)
 
 __all__ = [
     "Pool", "HwkvError", "binding", "HWKV_F32", "HWKV_BF16", "HWKV_KERNEL_AUTO", "HWKV_KERNEL_TENSOR",
     "HWKV_KERNEL_SIMT", "hwkv_abi_version", "hwkv_append", "hwkv_append_decode_attn", "hwkv_block_table",
     "hwkv_check_device_errors", "hwkv_kernel_launches",
     "hwkv_decode_attn", "hwkv_decode_workspace_bytes", "hwkv_materialize", "hwkv_pool_bytes", "hwkv_pool_create",
-    "hwkv_pool_destroy", "hwkv_pool_geometry", "hwkv_prefill_attn", "hwkv_set_block_table",
-    "hwkv_set_decode_config",
+    "hwkv_pool_destroy", "hwkv_pool_geometry", "hwkv_prefill_attn", "hwkv_prefill_workspace_bytes",
+    "hwkv_set_block_table", "hwkv_set_decode_config", "hwkv_set_prefill_config",
 ]
 
 
@@ -51,6 +52,7 @@ class Pool:
         self.handle = hwkv_pool_create(layers, kv_heads, head_dim, block_size, windows, num_seqs, dtype,
                                        self.buffer, stream)
         self.workspace = None
+        self.prefill_workspace = None
         self._size_workspace()
 
     def _size_workspace(self):
@@ -102,11 +104,19 @@ class Pool:
         return out
 
     def prefill(self, layer: int, q, scale: float, k_new, v_new, pos, n, out=None, stream=None):
-        """Chunked prefill: q [B][n_max][Hq][D], k_new/v_new [B][n_max][Hkv][D]; pos, n int32 [B]."""
+        """Chunked prefill: q [B][n_max][Hq][D], k_new/v_new [B][n_max][Hkv][D]; pos, n int32 [B].
+        Keeps a workspace for the split of long key streams, grown on demand."""
         if out is None:
             out = torch.zeros_like(q)
-        hwkv_prefill_attn(self.handle, layer, q, scale, k_new, v_new, pos, n, out, stream)
+        need = hwkv_prefill_workspace_bytes(self.handle, layer, q.shape[2], q.shape[1])
+        if need and (self.prefill_workspace is None or self.prefill_workspace.numel() < need):
+            self.prefill_workspace = torch.empty(need, dtype=torch.uint8, device=self.buffer.device)
+        hwkv_prefill_attn(self.handle, layer, q, scale, k_new, v_new, pos, n, out,
+                          self.prefill_workspace if need else None, stream)
         return out
+
+    def set_prefill_config(self, max_stages: int = 0):
+        hwkv_set_prefill_config(self.handle, max_stages)
 
     def check_device_errors(self, stream=None) -> int:
         return hwkv_check_device_errors(self.handle, stream)

@@ -58,7 +58,9 @@ SIGNATURES = [
     ("hwkv_decode_attn", _i, [_vp, _i, _vp, _i, ctypes.c_float, _vp, _vp, _vp, _u64, _vp]),
     ("hwkv_append_decode_attn", _i, [_vp, _i, _vp, _i, ctypes.c_float, _vp, _vp, _vp, _vp, _vp, _u64, _vp]),
     ("hwkv_decode_attn_noalloc", _i, [_vp, _i, _vp, _i, ctypes.c_float, _vp, _vp, _vp]),
-    ("hwkv_prefill_attn", _i, [_vp, _i, _vp, _i, ctypes.c_float, _vp, _vp, _i, _vp, _vp, _vp, _vp]),
+    ("hwkv_prefill_attn", _i, [_vp, _i, _vp, _i, ctypes.c_float, _vp, _vp, _i, _vp, _vp, _vp, _vp, _u64, _vp]),
+    ("hwkv_prefill_workspace_bytes", _i, [_vp, _i, _i, _i, ctypes.POINTER(_u64)]),
+    ("hwkv_set_prefill_config", _i, [_vp, _i]),
     ("hwkv_set_decode_config", _i, [_vp, _i, _i, _i]),
     ("hwkv_kernel_launches", _i, [_c_u64p]),
     ("hwkv_seqcalib", _i, [_i, _i, _i, _i, _i, _i, _i, _c_i32p, DISTORTION_FN, _vp, _u64, _c_i32p, _c_i32p, _c_u64p]),
@@ -93,7 +95,7 @@ def load(build_if_missing: bool = True):
         fn = getattr(lib, name)
         fn.restype = res
         fn.argtypes = args
-    if lib.hwkv_abi_version() != 1:
+    if lib.hwkv_abi_version() != 2:
         raise RuntimeError("libhwkv.so ABI version mismatch")
     _lib = lib
     return lib
@@ -246,13 +248,25 @@ def hwkv_decode_attn_noalloc(pool: int, layer: int, q: torch.Tensor, scale: floa
 
 
 def hwkv_prefill_attn(pool: int, layer: int, q: torch.Tensor, scale: float, k_new: torch.Tensor, v_new: torch.Tensor,
-                      pos: torch.Tensor, n: torch.Tensor, out: torch.Tensor, stream=None):
-    """q, out: [B][n_max][Hq][D]; k_new, v_new: [B][n_max][Hkv][D]; pos, n: int32 [B] on the device."""
+                      pos: torch.Tensor, n: torch.Tensor, out: torch.Tensor, workspace=None, stream=None):
+    """q, out: [B][n_max][Hq][D]; k_new, v_new: [B][n_max][Hkv][D]; pos, n: int32 [B] on the device;
+    workspace: optional device tensor of hwkv_prefill_workspace_bytes() bytes."""
     for t in (q, k_new, v_new, out):
         if not t.is_contiguous():
             raise ValueError("prefill tensors must be contiguous")
+    ws, ws_bytes = (None, 0) if workspace is None else (_ptr(workspace), workspace.numel() * workspace.element_size())
     _check(load().hwkv_prefill_attn(pool, layer, _ptr(q), q.shape[2], float(scale), _ptr(k_new), _ptr(v_new),
-                                    q.shape[1], _ptr(pos), _ptr(n), _ptr(out), _stream_ptr(stream)))
+                                    q.shape[1], _ptr(pos), _ptr(n), _ptr(out), ws, ws_bytes, _stream_ptr(stream)))
+
+
+def hwkv_prefill_workspace_bytes(pool: int, layer: int, q_heads: int, n_max: int) -> int:
+    out = _u64(0)
+    _check(load().hwkv_prefill_workspace_bytes(pool, layer, q_heads, n_max, ctypes.byref(out)))
+    return out.value
+
+
+def hwkv_set_prefill_config(pool: int, max_stages: int = 0):
+    _check(load().hwkv_set_prefill_config(pool, max_stages))
 
 
 def hwkv_set_decode_config(pool: int, split_tokens: int = 0, workers: int = 0, kernel: int = HWKV_KERNEL_AUTO):

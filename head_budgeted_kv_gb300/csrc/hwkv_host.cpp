@@ -164,6 +164,7 @@ struct hwkv_pool {
   // consecutive blocks is 64 keys (K or V) of a prefill stage
   alignas(64) CUtensorMap stage_map;
   int stage_tb = 0;
+  int prefill_max_stages = 0;  // cap on a prefill CTA's key stages (0 = automatic)
 };
 
 namespace {
@@ -203,6 +204,49 @@ void plan_decode(hwkv_pool* p) {
     }
     lp.items = lp.chunk_prefix[g.kv_heads] * g.num_seqs;
   }
+}
+
+// Work plan of one prefill launch: heads by decreasing window; a head whose key stream (upper
+// bound over lengths) is much longer than an even share of the work is split over several CTAs
+// per (seq, query-tile pair), whose fp32 partials a combine kernel merges.  Returns the
+// workspace bytes the split needs (0 when nothing is split).  allow_split = false plans one
+// CTA per stream.
+uint64_t plan_prefill(const hwkv_pool* p, int layer, int G, int n_max, bool allow_split, PrefillArgs& a) {
+  const Geometry& g = p->g;
+  const int H = g.kv_heads;
+  std::vector<int> order(H);
+  for (int h = 0; h < H; ++h) order[h] = h;
+  const int* win = &g.windows[(size_t)layer * H];
+  std::stable_sort(order.begin(), order.end(), [&](int x, int y) { return win[x] > win[y]; });
+  const int per_pair = prefill_tokens_per_cta(G);
+  const int pairs = (n_max + per_pair - 1) / per_pair;
+  const int64_t items = (int64_t)g.num_seqs * pairs;
+  std::vector<int> maxst(H);
+  int64_t work = 0;
+  for (int i = 0; i < H; ++i) {
+    const int h = order[i];
+    const int C = g.nblk[(size_t)layer * H + h] * g.block_size;
+    maxst[i] = prefill_max_stages(win[h], C, G, n_max);
+    work += items * maxst[i];
+  }
+  // about three waves of one CTA per SM
+  int64_t target = p->prefill_max_stages > 0 ? p->prefill_max_stages
+                                            : std::max<int64_t>(16, (work + 3LL * p->num_sms - 1) / (3LL * p->num_sms));
+  int64_t ctas = 0;
+  bool any = false;
+  for (int i = 0; i < H; ++i) {
+    int sp = 1;
+    if (allow_split && maxst[i] > target) sp = (int)std::min<int64_t>(64, (maxst[i] + target - 1) / target);
+    a.head_order[i] = order[i];
+    a.splits[i] = sp;
+    a.split_stages[i] = (maxst[i] + sp - 1) / sp;
+    a.head_ctas[i] = (int32_t)ctas;
+    ctas += items * sp;
+    any = any || sp > 1;
+  }
+  a.head_ctas[H] = (int32_t)ctas;
+  a.q_tiles = pairs;
+  return any ? (uint64_t)ctas * 2 * 128 * ((uint64_t)g.head_dim + 2) * sizeof(float) : 0;
 }
 
 // persistent CTAs of the tensor-core kernel
@@ -655,9 +699,29 @@ int hwkv_append_decode_attn(hwkv_pool_t p, int layer, const void* q, int q_heads
   return decode_common(p, layer, q, q_heads, scale, pos_dev, 1, k_new, v_new, out, workspace, ws_bytes, stream);
 }
 
+int hwkv_prefill_workspace_bytes(hwkv_pool_t p, int layer, int q_heads, int n_max, uint64_t* out) {
+  if (!p || !out) return fail(HWKV_ERR_INVALID_ARG, "NULL argument");
+  const Geometry& g = p->g;
+  if (layer < 0 || layer >= g.layers) return fail(HWKV_ERR_INVALID_ARG, "layer %d out of range", layer);
+  if (q_heads < g.kv_heads || q_heads % g.kv_heads != 0 || q_heads / g.kv_heads > kMaxGroup)
+    return fail(HWKV_ERR_UNSUPPORTED, "q_heads must be G * kv_heads with 1 <= G <= %d", kMaxGroup);
+  if (n_max < 1) return fail(HWKV_ERR_INVALID_ARG, "n_max must be >= 1");
+  PrefillArgs a;
+  std::memset(&a, 0, sizeof a);
+  *out = plan_prefill(p, layer, q_heads / g.kv_heads, n_max, true, a);
+  return ok();
+}
+
+int hwkv_set_prefill_config(hwkv_pool_t p, int max_stages) {
+  if (!p) return fail(HWKV_ERR_INVALID_ARG, "pool is NULL");
+  if (max_stages < 0) return fail(HWKV_ERR_INVALID_ARG, "max_stages must be >= 0");
+  p->prefill_max_stages = max_stages;
+  return ok();
+}
+
 int hwkv_prefill_attn(hwkv_pool_t p, int layer, const void* q, int q_heads, float scale, const void* k_new,
                       const void* v_new, int n_max, const int32_t* pos_dev, const int32_t* n_dev, void* out,
-                      void* stream) {
+                      void* workspace, uint64_t workspace_bytes, void* stream) {
   if (!p) return fail(HWKV_ERR_INVALID_ARG, "pool is NULL");
   const Geometry& g = p->g;
   if (layer < 0 || layer >= g.layers) return fail(HWKV_ERR_INVALID_ARG, "layer %d out of range", layer);
@@ -673,8 +737,8 @@ int hwkv_prefill_attn(hwkv_pool_t p, int layer, const void* q, int q_heads, floa
   if ((int64_t)g.num_seqs * n_max > kInt32Max) return fail(HWKV_ERR_UNSUPPORTED, "num_seqs * n_max must be below 2^31");
   if (!q || !k_new || !v_new || !out || !pos_dev || !n_dev) return fail(HWKV_ERR_INVALID_ARG, "NULL tensor argument");
   if (!aligned(q, 16) || !aligned(k_new, 16) || !aligned(v_new, 16) || !aligned(out, 16) || !aligned(pos_dev, 4) ||
-      !aligned(n_dev, 4))
-    return fail(HWKV_ERR_ALIGNMENT, "tensors must be 16-byte aligned, lengths 4-byte aligned");
+      !aligned(n_dev, 4) || !aligned(workspace, 16))
+    return fail(HWKV_ERR_ALIGNMENT, "tensors and workspace must be 16-byte aligned, lengths 4-byte aligned");
   int rc = check_device(p);
   if (rc != HWKV_OK) return rc;
   PFN_cuTensorMapEncodeTiled_v12000 encode = tensor_map_encoder();
@@ -717,26 +781,25 @@ int hwkv_prefill_attn(hwkv_pool_t p, int layer, const void* q, int q_heads, floa
   a.nlen = n_dev;
   a.n_max = n_max;
   a.group = G;
-  const int qt = prefill_tokens_per_cta(G);
-  a.q_tiles = (n_max + qt - 1) / qt;
+  // split long key streams when the workspace holds their partials, else one CTA per stream
+  uint64_t need = plan_prefill(p, layer, G, n_max, true, a);
+  if (need > 0 && (workspace == nullptr || workspace_bytes < need)) need = plan_prefill(p, layer, G, n_max, false, a);
+  if (need > 0) {
+    a.part_o = static_cast<float*>(workspace);
+    a.part_ml = a.part_o + (size_t)a.head_ctas[g.kv_heads] * 2 * 128 * g.head_dim;
+  }
   a.scale_log2 = scale * 1.4426950408889634f;
   a.bs_log2 = -1;
   for (int b = 0; b < 31; ++b)
     if ((1 << b) == g.block_size) a.bs_log2 = b;
   a.stage_tb = p->stage_tb;
-  // longest windows first: their CTAs stream the most keys
-  std::vector<int> order(g.kv_heads);
-  for (int h = 0; h < g.kv_heads; ++h) order[h] = h;
-  std::stable_sort(order.begin(), order.end(), [&](int x, int y) { return a.g.window[x] > a.g.window[y]; });
   int max_c = 0;
-  for (int h = 0; h < g.kv_heads; ++h) {
-    a.head_order[h] = order[h];
-    max_c = std::max(max_c, a.g.nblk_prefix[h + 1] - a.g.nblk_prefix[h]);
-  }
+  for (int h = 0; h < g.kv_heads; ++h) max_c = std::max(max_c, a.g.nblk_prefix[h + 1] - a.g.nblk_prefix[h]);
   max_c *= g.block_size;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   HWKV_CUDA_TRY(launch_prefill(a, &p->tmap, &p->stage_map, &kmap, &vmap, &kmap64, &vmap64, &qmap, st),
                 "prefill launch");
+  if (need > 0) HWKV_CUDA_TRY(launch_prefill_combine(a, st), "prefill combine launch");
   HWKV_CUDA_TRY(launch_chunk_append(a, std::min(n_max, max_c), st), "chunk append launch");
   return ok();
 }

@@ -80,11 +80,18 @@ struct PrefillArgs {
   const int32_t* nlen;     // [B] chunk lengths (<= n_max)
   int32_t n_max;
   int32_t group;           // G = Hq / H
-  int32_t q_tiles;         // CTAs per (seq, head): ceil(n_max / chunk tokens per CTA)
+  int32_t q_tiles;         // query-tile pairs per (seq, head): ceil(n_max / chunk tokens per pair)
   float scale_log2;
   int32_t bs_log2;         // log2(block_size), or -1 when it is not a power of two
   int32_t stage_tb;        // rows of one block in a 64-key pool copy (16, 32, 64), 0: per-tile copies only
   int32_t head_order[kMaxKvHeads];  // heads by decreasing window (work order)
+  // split of long key streams: head order position i has splits[i] CTAs per (seq, tile pair),
+  // each streaming split_stages[i] stages; its CTAs are [head_ctas[i], head_ctas[i + 1])
+  int32_t splits[kMaxKvHeads];
+  int32_t split_stages[kMaxKvHeads];
+  int32_t head_ctas[kMaxKvHeads + 1];
+  float* part_o;           // [CTA][256 rows][D] unnormalised partial outputs of split streams
+  float* part_ml;          // [CTA][256 rows][2] (reference maximum in log2 units, sum)
 };
 
 // Counts every kernel launch the library makes (read by hwkv_kernel_launches).
@@ -115,5 +122,9 @@ cudaError_t launch_prefill(const PrefillArgs& a, const CUtensorMap* pool_map, co
                            const CUtensorMap* knew_map, const CUtensorMap* vnew_map, const CUtensorMap* knew64_map,
                            const CUtensorMap* vnew64_map, const CUtensorMap* q_map, cudaStream_t st);
 cudaError_t launch_chunk_append(const PrefillArgs& a, int max_rows, cudaStream_t st);
+// merge of the partials of split key streams (after launch_prefill)
+cudaError_t launch_prefill_combine(const PrefillArgs& a, cudaStream_t st);
+// upper bound on the 64-key stages of one prefill CTA's key stream for a head
+int prefill_max_stages(int window, int ring_capacity, int group, int n_max);
 
 }  // namespace hwkv

@@ -31,6 +31,8 @@
 //   2^8 (then the row of O in tensor memory and its sum are rescaled), so P stays <= 256 and
 //   O is rarely touched between stages.  Every wait is bounded (~2 s); a timeout records
 //   HWKV_DEVERR_WAIT_TIMEOUT and all roles stop.
+#include <algorithm>
+
 #include "hwkv_tcgen05.cuh"
 
 namespace hwkv {
@@ -168,12 +170,16 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_kernel(const __grid_con
   const int Hq = H * G;
   const int bs = a.pv.block_size;
 
-  // work item: heads in the host's order (longest windows first), then sequences, tile pairs
-  const int per_head = a.pv.num_seqs * a.q_tiles;
-  const int h = a.head_order[blockIdx.x / per_head];
-  const int rem = blockIdx.x % per_head;
-  const int s = rem / a.q_tiles;
-  const int qt = rem % a.q_tiles;
+  // work item: heads in the host's order (longest windows first), then sequences, tile pairs,
+  // then the splits of the pair's key stream
+  int hi = 0;
+  while (hi + 1 < H && (int)blockIdx.x >= a.head_ctas[hi + 1]) ++hi;
+  const int h = a.head_order[hi];
+  const int sp = a.splits[hi];
+  const int item = ((int)blockIdx.x - a.head_ctas[hi]) / sp;
+  const int piece = ((int)blockIdx.x - a.head_ctas[hi]) - item * sp;
+  const int s = item / a.q_tiles;
+  const int qt = item - s * a.q_tiles;
 
   const int p0 = a.pos0[s];
   const int n = a.nlen[s];
@@ -211,6 +217,15 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_kernel(const __grid_con
   }
   const int ntiles = tl.prior_tiles + tl.chunk_tiles;
   const int nst = (ntiles + kPfSub - 1) / kPfSub;
+  // this CTA's stages [j0, j0 + nloc) of the stream; a split stream leaves a partial per CTA
+  const bool split = sp > 1;
+  const int j0 = split ? piece * a.split_stages[hi] : 0;
+  const int nloc = split ? min(nst, j0 + a.split_stages[hi]) - j0 : nst;
+  if (nloc <= 0) {  // nothing of the stream left for this split: an empty partial
+    float2* ml = reinterpret_cast<float2*>(a.part_ml) + (size_t)blockIdx.x * 2 * kPfM;
+    for (int r = threadIdx.x; r < 2 * kPfM; r += blockDim.x) ml[r] = make_float2(kNegInf, 0.f);
+    return;
+  }
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < NS; ++i) {
@@ -270,10 +285,11 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_kernel(const __grid_con
           }
         }
       };
-      fetch(0);
+      fetch(j0);
       int issued = 0;
-      for (int j = 0; j < nst; ++j) {
-        const int st = j % NS;
+      for (int jj = 0; jj < nloc; ++jj) {
+        const int j = j0 + jj;  // stage of the stream (key tiles 4j ..); jj indexes the ring
+        const int st = jj % NS;
         int kind[kPfSub], blk[kPfSub], r0[kPfSub];
 #pragma unroll
         for (int u = 0; u < kPfSub; ++u) {
@@ -281,7 +297,7 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_kernel(const __grid_con
           blk[u] = nxt_blk[u];
           r0[u] = nxt_r0[u];
         }
-        if (j + 1 < nst) fetch(j + 1);
+        if (jj + 1 < nloc) fetch(j + 1);
         // pool rows of the ring tiles (-1 for chunk tiles); padding tiles read pool row 0
         // (finite, masked)
         int row[kPfSub];
@@ -309,7 +325,7 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_kernel(const __grid_con
           ring_stage = ring_stage && kind[u] == 0 && r0[u] == r0[0] + ((kTile * u) & (tb - 1)) &&
                        blk[u] == blk[0] + (kTile * u) / max(tb, 1);
         const bool chunk_stage = kind[0] == 1 && kind[kPfSub - 1] == 1;
-        if (j >= NS && !pf_wait(&kv_empty[st], (uint32_t)((j / NS) - 1) & 1u, abort, a.pv.err)) break;
+        if (jj >= NS && !pf_wait(&kv_empty[st], (uint32_t)((jj / NS) - 1) & 1u, abort, a.pv.err)) break;
         const uint32_t kdst = sbase + Cfg::kStageOff + st * Cfg::kStageBytes;
         const uint32_t vdst = kdst + Cfg::kKBytes;
         mbar_arrive_expect_tx(&kv_full[st], Cfg::kStageBytes);
@@ -398,15 +414,15 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_kernel(const __grid_con
             umma_bf16_tmem_a(tmem + Cfg::kColO + x * D, pcol + i * 8, dvs + (uint64_t)((i * 16 * 128) >> 4), idO,
                              (j > 0 || i > 0) ? 1u : 0u);
           umma_commit(&o_done[x][b]);
-          if (j == nst - 1) umma_commit(&o_final[x]);
+          if (j == nloc - 1) umma_commit(&o_final[x]);
         }
         umma_commit(&kv_empty[st]);
       };
       if (ok) issue_s(0);
-      if (ok && nst > 1) issue_s(1);
-      for (int j = 0; ok && j < nst; ++j) {
+      if (ok && nloc > 1) issue_s(1);
+      for (int j = 0; ok && j < nloc; ++j) {
         issue_pv(j);
-        if (ok && j + 2 < nst) issue_s(j + 2);
+        if (ok && j + 2 < nloc) issue_s(j + 2);
       }
       umma_commit(&drain);  // every MMA issued above completes before tensor memory is freed
       mbar_wait_bounded(&drain, 0);
@@ -430,9 +446,10 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_kernel(const __grid_con
     const float masked = pos_scale ? kNegInf : -kNegInf;
     float m_ref = kNegInf, l = 0.f;
     bool ok = true;
-    for (int j = 0; j < nst; ++j) {
-      const int b = j & 1;
-      ok = __all_sync(0xffffffffu, pf_wait(&s_full[x][b], (uint32_t)(j >> 1) & 1u, abort, a.pv.err));
+    for (int jj = 0; jj < nloc; ++jj) {
+      const int j = j0 + jj;  // stage of the stream; jj counts this CTA's stages (barrier phases)
+      const int b = jj & 1;
+      ok = __all_sync(0xffffffffu, pf_wait(&s_full[x][b], (uint32_t)(jj >> 1) & 1u, abort, a.pv.err));
       if (!ok) break;
       tc_fence_after_sync();
       float sv[kPfKeys];
@@ -503,8 +520,8 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_kernel(const __grid_con
       const float m_new = fmaxf(m_ref, mx);
       const bool grow = m_new > m_ref + 8.f;
       // O may be rescaled once the previous P . V into it has completed
-      if (j > 0 && __any_sync(0xffffffffu, grow)) {
-        ok = __all_sync(0xffffffffu, pf_wait(&o_done[x][(j - 1) & 1], (uint32_t)((j - 1) >> 1) & 1u, abort, a.pv.err));
+      if (jj > 0 && __any_sync(0xffffffffu, grow)) {
+        ok = __all_sync(0xffffffffu, pf_wait(&o_done[x][(jj - 1) & 1], (uint32_t)((jj - 1) >> 1) & 1u, abort, a.pv.err));
         if (!ok) break;
         tc_fence_after_sync();
         {
@@ -531,9 +548,9 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_kernel(const __grid_con
 #pragma unroll
         for (int u = 0; u < kPfSub; ++u) need = need || (kt[u].kind == 1 && kt[u].a + kTile > n);
         if (need) {
-          ok = __all_sync(0xffffffffu, pf_wait(&kv_full[j % NS], (uint32_t)(j / NS) & 1u, abort, a.pv.err));
+          ok = __all_sync(0xffffffffu, pf_wait(&kv_full[jj % NS], (uint32_t)(jj / NS) & 1u, abort, a.pv.err));
           if (!ok) break;
-          const uint32_t vst = sbase + Cfg::kStageOff + (j % NS) * Cfg::kStageBytes + Cfg::kKBytes;
+          const uint32_t vst = sbase + Cfg::kStageOff + (jj % NS) * Cfg::kStageBytes + Cfg::kKBytes;
 #pragma unroll
           for (int u = 0; u < kPfSub; ++u) {
             if (kt[u].kind == 1 && kt[u].a + kTile > n) {
@@ -571,7 +588,23 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_kernel(const __grid_con
     }
     // the last P . V into O
     if (ok) ok = __all_sync(0xffffffffu, pf_wait(&o_final[x], 0u, abort, a.pv.err));
-    if (ok) {
+    if (ok && split) {
+      // partial of a split stream: O not normalised, with the row's reference maximum and sum
+      tc_fence_after_sync();
+      const size_t prow = (size_t)blockIdx.x * 2 * kPfM + x * kPfM + r;
+      float* po = a.part_o + prow * D;
+#pragma unroll 1
+      for (int c = 0; c < D; c += 32) {
+        float o[32];
+        tmem_ld32(lane_base + colO + c, o);
+        if (live) {
+#pragma unroll
+          for (int k = 0; k < 8; ++k)
+            *reinterpret_cast<float4*>(po + c + 4 * k) = make_float4(o[4 * k], o[4 * k + 1], o[4 * k + 2], o[4 * k + 3]);
+        }
+      }
+      if (live) reinterpret_cast<float2*>(a.part_ml)[prow] = make_float2(m_ref, l);
+    } else if (ok) {
       // normalise and store the row
       tc_fence_after_sync();
       const float inv = l > 0.f ? 1.f / l : 0.f;
@@ -638,6 +671,56 @@ __global__ void __launch_bounds__(256) chunk_append_kernel(const __grid_constant
   }
 }
 
+// Merges the partials of split key streams: per (seq, head, tile pair) whose stream was split,
+// each live row's output is the online-softmax merge of its splits' (O, reference maximum m,
+// sum l): out = sum_i O_i 2^(m_i - M) / sum_i l_i 2^(m_i - M), M = max_i m_i.  One warp per row,
+// lanes over head_dim.
+template <int D>
+__global__ void __launch_bounds__(256) prefill_combine_kernel(const __grid_constant__ PrefillArgs a) {
+  constexpr int kC = D / 32;  // columns per lane
+  const int per_head = a.pv.num_seqs * a.q_tiles;
+  const int hi = blockIdx.x / per_head;
+  const int item = blockIdx.x - hi * per_head;
+  const int sp = a.splits[hi];
+  if (sp <= 1) return;
+  const int h = a.head_order[hi];
+  const int s = item / a.q_tiles, qt = item - (item / a.q_tiles) * a.q_tiles;
+  const int p0 = a.pos0[s], n = a.nlen[s];
+  if (p0 < 0 || n < 0 || n > a.n_max) return;
+  const int G = a.group, QT = kPfM / G, Hq = a.pv.kv_heads * G;
+  const int qa = qt * 2 * QT;
+  if (qa >= n) return;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const size_t slot0 = (size_t)a.head_ctas[hi] + (size_t)item * sp;
+  for (int row = warp; row < 2 * kPfM; row += 8) {
+    const int x = row / kPfM, r = row - x * kPfM;
+    const int tok = qa + x * QT + r / G;
+    if (r >= QT * G || tok >= n) continue;
+    float M = kNegInf;
+    for (int i = 0; i < sp; ++i) M = fmaxf(M, reinterpret_cast<const float2*>(a.part_ml)[(slot0 + i) * 2 * kPfM + row].x);
+    float L = 0.f, acc[kC];
+#pragma unroll
+    for (int c = 0; c < kC; ++c) acc[c] = 0.f;
+    if (M != kNegInf) {
+      for (int i = 0; i < sp; ++i) {
+        const size_t pr = (slot0 + i) * 2 * kPfM + row;
+        const float2 ml = reinterpret_cast<const float2*>(a.part_ml)[pr];
+        if (ml.x == kNegInf) continue;
+        const float f = ex2(ml.x - M);
+        L = fmaf(ml.y, f, L);
+        const float* po = a.part_o + pr * D + lane * kC;
+#pragma unroll
+        for (int c = 0; c < kC; ++c) acc[c] = fmaf(po[c], f, acc[c]);
+      }
+    }
+    const float inv = L > 0.f ? 1.f / L : 0.f;
+    __nv_bfloat16* orow = static_cast<__nv_bfloat16*>(a.out) + (((int64_t)s * a.n_max + tok) * Hq + h * G + r % G) * D;
+#pragma unroll
+    for (int c = 0; c < kC; c += 2)
+      *reinterpret_cast<uint32_t*>(orow + lane * kC + c) = pack_bf16(acc[c] * inv, acc[c + 1] * inv);
+  }
+}
+
 template <int D>
 cudaError_t launch_pf(const PrefillArgs& a, const CUtensorMap* pm, const CUtensorMap* sm, const CUtensorMap* km,
                       const CUtensorMap* vm, const CUtensorMap* km64, const CUtensorMap* vm64, const CUtensorMap* qm,
@@ -653,18 +736,36 @@ cudaError_t launch_pf(const PrefillArgs& a, const CUtensorMap* pm, const CUtenso
 
 int prefill_tokens_per_cta(int group) { return 2 * (kPfM / group); }
 
+int prefill_max_stages(int window, int ring_capacity, int group, int n_max) {
+  // ring tiles: at most the window's (or the ring's) 16-token tiles plus one for alignment;
+  // chunk tiles: the pair's tokens plus the window reaching back into the chunk
+  const int qt2 = 2 * (kPfM / group);
+  const int64_t prior = std::min<int64_t>(ring_capacity / 16, (window + 15) / 16 + 1);
+  const int64_t chunk = std::min<int64_t>((n_max + 15) / 16 + 1, (qt2 + (int64_t)window + 15) / 16 + 1);
+  return (int)((prior + chunk + kPfSub - 1) / kPfSub);
+}
+
 int prefill_tile_tokens(int group) { return kPfM / group; }
 
 cudaError_t launch_prefill(const PrefillArgs& a, const CUtensorMap* pool_map, const CUtensorMap* stage_map,
                            const CUtensorMap* knew_map, const CUtensorMap* vnew_map, const CUtensorMap* knew64_map,
                            const CUtensorMap* vnew64_map, const CUtensorMap* q_map, cudaStream_t st) {
-  const int items = a.pv.kv_heads * a.pv.num_seqs * a.q_tiles;
+  const int items = a.head_ctas[a.pv.kv_heads];
   if (a.group < 1 || a.group > kMaxGroup) return cudaErrorInvalidValue;
   if (a.pv.head_dim == 128)
     return launch_pf<128>(a, pool_map, stage_map, knew_map, vnew_map, knew64_map, vnew64_map, q_map, items, st);
   if (a.pv.head_dim == 64)
     return launch_pf<64>(a, pool_map, stage_map, knew_map, vnew_map, knew64_map, vnew64_map, q_map, items, st);
   return cudaErrorInvalidValue;
+}
+
+cudaError_t launch_prefill_combine(const PrefillArgs& a, cudaStream_t st) {
+  const int blocks = a.pv.kv_heads * a.pv.num_seqs * a.q_tiles;
+  if (a.pv.head_dim == 128) prefill_combine_kernel<128><<<blocks, 256, 0, st>>>(a);
+  else if (a.pv.head_dim == 64) prefill_combine_kernel<64><<<blocks, 256, 0, st>>>(a);
+  else return cudaErrorInvalidValue;
+  count_launches(1);
+  return cudaGetLastError();
 }
 
 cudaError_t launch_chunk_append(const PrefillArgs& a, int max_rows, cudaStream_t st) {

@@ -43,7 +43,7 @@
 extern "C" {
 #endif
 
-#define HWKV_ABI_VERSION 1
+#define HWKV_ABI_VERSION 2
 
 /* status codes */
 #define HWKV_OK 0
@@ -209,11 +209,25 @@ int hwkv_decode_attn_noalloc(hwkv_pool_t pool, int layer, const void* q, int q_h
  *   all 16-byte aligned.  pos_dev / n_dev: device int32 [num_seqs], lengths before the chunk
  *   and chunk lengths (0 <= n_s <= n_max, checked on the device; a bad sequence is skipped and
  *   flagged HWKV_DEVERR_NEG_LENGTH).  Rows of out at or past n_s are left untouched.
+ *   workspace: device scratch of hwkv_prefill_workspace_bytes() bytes (16-byte aligned) that lets
+ *   the library split long key streams over several CTAs and merge their fp32 partials; NULL or
+ *   a smaller size runs one CTA per stream (same results up to rounding, slower for long windows
+ *   at small batch).  Contents need no initialisation and are clobbered.
  * Needs a bf16 pool with block_size % 16 == 0 and q_heads = G * kv_heads with G <= 16
- * (HWKV_ERR_UNSUPPORTED otherwise).  Two kernels on `stream`; no workspace. */
+ * (HWKV_ERR_UNSUPPORTED otherwise).  Two or three kernels on `stream` (attention, the merge of
+ * split streams, the append). */
 int hwkv_prefill_attn(hwkv_pool_t pool, int layer, const void* q, int q_heads, float scale, const void* k_new,
                       const void* v_new, int n_max, const int32_t* pos_dev, const int32_t* n_dev, void* out,
-                      void* stream);
+                      void* workspace, uint64_t workspace_bytes, void* stream);
+
+/* Bytes of workspace hwkv_prefill_attn uses to split the key streams of `layer` for chunks of up
+ * to n_max tokens and q_heads query heads (0 when nothing would be split).  Host only; depends on
+ * the geometry, the GPU's SM count and hwkv_set_prefill_config. */
+int hwkv_prefill_workspace_bytes(hwkv_pool_t pool, int layer, int q_heads, int n_max, uint64_t* out);
+
+/* Prefill configuration: max_stages caps the 64-key stages one CTA streams before its stream is
+ * split (0 = automatic: about three waves of one CTA per SM).  Results differ only by rounding. */
+int hwkv_set_prefill_config(hwkv_pool_t pool, int max_stages);
 
 /* Decode configuration.  kernel = HWKV_KERNEL_*.  split_tokens: tokens of one split-K chunk of
  * the CUDA-core kernel (0 = automatic; else a power of two in [16, 65536]).  workers: CTAs of

@@ -43,13 +43,15 @@ class History:
         return lo, self.k[(l, s, h)][lo:hi], self.v[(l, s, h)][lo:hi]
 
 
-def _run(cfg, chunks, seed_decode_steps=2, check_every_token=True):
+def _run(cfg, chunks, seed_decode_steps=2, check_every_token=True, max_stages=0):
     """Materialise cfg.prefill, then prefill the given chunk lengths [[n_s per seq] per chunk],
-    then decode a few steps; compare everything with the oracle."""
+    then decode a few steps; compare everything with the oracle.  max_stages > 0 splits every
+    key stream longer than that many 64-key stages over several CTAs."""
     dev = torch.device("cuda")
     wl = workloads.Workload(cfg, device=dev)
     pool = hw.Pool(cfg.layers, cfg.kv_heads, cfg.head_dim, cfg.block_size, cfg.windows_array(), cfg.batch,
                    torch.bfloat16, q_heads=cfg.q_heads)
+    pool.set_prefill_config(max_stages)
     hist = History(cfg)
     lens = np.asarray(cfg.prefill, dtype=np.int64)
     pre = torch.tensor(cfg.prefill, dtype=torch.int32, device=dev)
@@ -144,6 +146,12 @@ CASES = {
     # long key streams (about 130 stages of 64 keys per CTA), so the kernel's pipeline barriers
     # run through many phases
     "deep": dict(kv_heads=2, windows=((8192, 2048),), prefill=(9000, 2100), chunks=[[160, 70]]),
+    # key streams split over several CTAs and merged (forced by a small stage cap): long and
+    # short streams, empty splits past short contexts, a zero-length chunk, group 16, two layers
+    "split_deep": dict(kv_heads=2, windows=((8192, 2048),), prefill=(9000, 2100), chunks=[[160, 70]], max_stages=9),
+    "split_ragged": dict(layers=2, kv_heads=3, windows=((64, 1024, 16), (256, 48, 500)), prefill=(700, 20, 130),
+                         chunks=[[33, 0, 90]], max_stages=2),
+    "split_g16": dict(kv_heads=2, group=16, windows=((900, 512),), prefill=(600, 7), chunks=[[45, 9]], max_stages=3),
 }
 
 
@@ -151,8 +159,37 @@ CASES = {
 def test_prefill_against_oracle(name):
     spec = dict(CASES[name])
     chunks = spec.pop("chunks")
+    max_stages = spec.pop("max_stages", 0)
     cfg = small_config(name=name, cfg_id=91, steps=2, **spec)
-    _run(cfg, chunks)
+    _run(cfg, chunks, max_stages=max_stages)
+
+
+def test_split_streams_change_rounding_only():
+    """The same chunk with and without the split of its key streams: outputs within rounding,
+    rings bit-identical."""
+    cfg = small_config(name="splitcmp", cfg_id=94, kv_heads=2, windows=((4096, 300),), prefill=(5000, 40))
+    dev = torch.device("cuda")
+    wl = workloads.Workload(cfg, device=dev)
+    pre = torch.tensor(cfg.prefill, dtype=torch.int32, device=dev)
+    K, V = wl.prefill_layer(0, dev)
+    q, k, v = wl.chunk_inputs(0, 0, 200, dev)
+    nt = torch.tensor([200, 130], dtype=torch.int32, device=dev)
+    outs, pools = [], []
+    for cap in (0, 4):
+        pool = hw.Pool(1, 2, 128, 16, cfg.windows_array(), 2, torch.bfloat16, q_heads=cfg.q_heads)
+        pool.set_prefill_config(cap)
+        pool.materialize(0, K, V, pre)
+        outs.append(pool.prefill(0, q, cfg.scale, k, v, pre, nt))
+        pools.append(pool)
+    torch.cuda.synchronize()
+    assert hw.hwkv_prefill_workspace_bytes(pools[1].handle, 0, cfg.q_heads, 200) > 0
+    for s, n in enumerate((200, 130)):
+        assert_close(outs[1][s, :n].float().cpu().double().numpy(), outs[0][s, :n].float().cpu().double().numpy(),
+                     cfg, f"seq {s}")
+    assert torch.equal(pools[0].buffer, pools[1].buffer)
+    for p in pools:
+        assert p.check_device_errors() == 0
+        p.close()
 
 
 def test_prefill_equals_token_by_token_decode():
