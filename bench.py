@@ -535,6 +535,7 @@ def run_prefill(args, cfg):
     wl = workloads.Workload(cfg, device=dev)
     pool = hw.Pool(cfg.layers, cfg.kv_heads, cfg.head_dim, cfg.block_size, cfg.windows_array(), cfg.batch,
                    cfg.torch_dtype, q_heads=cfg.q_heads, device=dev)
+    pool.set_prefill_config(args.prefill_max_stages)
     prefill = torch.tensor(cfg.prefill, dtype=torch.int32, device=dev)
     for l in range(cfg.layers):
         K, V = wl.prefill_layer(l, dev)
@@ -602,6 +603,8 @@ def main(argv=None):
     p.add_argument("--graph", action="store_true", help="replay each decode step as one captured CUDA graph")
     p.add_argument("--mode", choices=["decode", "prefill"], default="decode")
     p.add_argument("--chunk", type=int, default=2048, help="prefill mode: tokens per sequence per chunk")
+    p.add_argument("--prefill-max-stages", type=int, default=0,
+                   help="prefill mode: split key streams longer than this many 64-key stages (0 = automatic)")
     p.add_argument("--kernel", type=int, default=0)
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--cpu-budget", type=float, default=12.0)
