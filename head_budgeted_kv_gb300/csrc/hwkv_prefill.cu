@@ -17,16 +17,17 @@
 //   stages filled by TMA (pool tiles through the block table, chunk tiles through a tensor map
 //   of the chunk).  Warp roles:
 //     warp 0      TMA producer (one lane),
-//     warp 1      tensor-memory owner and MMA issuer (one lane): per stage and query tile
-//                 S = Q . K^T (M 128, N 64, K = D; both operands in shared memory) into
-//                 tensor memory, and O += P . V (M 128, N = D, K 64; P read from tensor
-//                 memory, V from shared memory MN-major) accumulated in tensor memory,
+//     warp 1      tensor-memory owner; one lane issues S = Q . K^T per stage and query tile
+//                 (M 128, N 64, K = D; both operands in shared memory) into tensor memory,
+//     warp 2      one lane issues O += P . V (M 128, N = D, K 64; P read from tensor memory,
+//                 V from shared memory MN-major), O accumulated in tensor memory (two issuers,
+//                 so one's waits for P or for data are covered by the other's queued work),
 //     warps 4-7   softmax of query tile 0, warps 8-11 of tile 1: thread i owns row i, loads
 //                 its S row from tensor memory, masks it (causal, window, resident slots),
 //                 runs the online softmax in fp32 (log2 domain) and writes its P row as bf16
 //                 back over the first half of the S columns it came from.
-//   S is double-buffered per tile: the S of stage j + 2 is issued after the P . V of stage j
-//   that reads the same columns, and the tensor pipe runs them in issue order.
+//   S is double-buffered per tile: the S of stage j + 2 is issued once the P . V of stage j,
+//   which reads the same columns, has completed.
 //   The running maximum used for P is raised only when a row's maximum grows by more than
 //   2^8 (then the row of O in tensor memory and its sum are rescaled), so P stays <= 256 and
 //   O is rarely touched between stages.  Every wait is bounded (~2 s); a timeout records
@@ -159,7 +160,7 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_kernel(const __grid_con
   __shared__ __align__(8) uint64_t kv_full[NS], kv_empty[NS];
   // per query tile x and stage parity b (a phase of each barrier is one stage of that parity,
   // so no waiter can fall two phases behind, which a parity wait could not detect)
-  __shared__ __align__(8) uint64_t q_full, s_full[2][2], p_full[2][2], o_done[2][2], o_final[2], drain;
+  __shared__ __align__(8) uint64_t q_full, s_full[2][2], p_full[2][2], o_done[2][2], o_final[2], drain[2];
   __shared__ uint32_t s_tmem;
   __shared__ int s_abort;
 
@@ -241,7 +242,8 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_kernel(const __grid_con
       }
       mbar_init(&o_final[x], 1);
     }
-    mbar_init(&drain, 1);
+    mbar_init(&drain[0], 1);
+    mbar_init(&drain[1], 1);
     s_abort = 0;
     fence_mbar_init();
   }
@@ -366,66 +368,70 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_kernel(const __grid_con
           if (!mbar_wait_bounded(&kv_full[j % NS], (uint32_t)(j / NS) & 1u)) break;
       }
     }
-  } else if (warp == 1) {
-    // ---- MMA issuer: S of stage j + 2 is issued right after P . V of stage j ---------
+  } else if (warp == 1 || warp == 2) {
+    // ---- MMA issuers: warp 1 the S of every stage, warp 2 the P . V of every stage ------
     if (lane == 0) {
       constexpr uint32_t idS = umma_idesc_bf16(kPfM, kPfKeys, false, false);
       constexpr uint32_t idO = umma_idesc_bf16(kPfM, D, false, true);
-      bool ok = pf_wait(&q_full, 0, abort, a.pv.err);
       // Descriptors are built once; an operand's start address moves by adding its offset in
       // 16-byte units to the low field (shared addresses stay below 2^18 bytes, so the
-      // 14-bit field does not carry).  One thread issues every MMA, so this arithmetic is on
-      // the tensor pipe's critical path.
+      // 14-bit field does not carry).
       const uint64_t dq = umma_desc_sw128(sbase + Cfg::kQOff, 16, 1024);
       const uint64_t dk = umma_desc_sw128(sbase + Cfg::kStageOff, 16, 1024);
       const uint64_t dv = umma_desc_sw128(sbase + Cfg::kStageOff + Cfg::kKBytes, kPfKeys * 128, 1024);
-      // S_x = Q_x . K^T of stage j into buffer j % 2 (issued after the P . V of stage j - 2,
-      // which read the P written there)
-      auto issue_s = [&](int j) {
-        const int st = j % NS, b = j & 1;
-        ok = pf_wait(&kv_full[st], (uint32_t)(j / NS) & 1u, abort, a.pv.err);
-        if (!ok) return;
-        tc_fence_after_sync();
-        const uint64_t dks = dk + (uint64_t)((st * Cfg::kStageBytes) >> 4);
-#pragma unroll
-        for (int x = 0; x < 2; ++x) {
-#pragma unroll
-          for (int i = 0; i < D / 16; ++i) {
-            constexpr int kQRow = kPfM * 128, kKRow = kPfKeys * 128;
-            umma_bf16(tmem + (2 * x + b) * kPfKeys,
-                      dq + (uint64_t)((x * Cfg::kQBytes + (i >> 2) * kQRow + (i & 3) * 32) >> 4),
-                      dks + (uint64_t)(((i >> 2) * kKRow + (i & 3) * 32) >> 4), idS, i > 0 ? 1u : 0u);
-          }
-          umma_commit(&s_full[x][b]);
-        }
-      };
-      // O_x += P_x . V of stage j, once the softmax has written P_x into tensor memory
-      auto issue_pv = [&](int j) {
-        const int st = j % NS, b = j & 1;
-        const uint64_t dvs = dv + (uint64_t)((st * Cfg::kStageBytes) >> 4);
-#pragma unroll
-        for (int x = 0; x < 2; ++x) {
-          ok = pf_wait(&p_full[x][b], (uint32_t)(j >> 1) & 1u, abort, a.pv.err);
-          if (!ok) return;
+      bool ok = true;
+      if (warp == 1) {
+        // S_x = Q_x . K^T of stage j into buffer j % 2, once the P . V of stage j - 2 (which
+        // read the P written there) has completed
+        ok = pf_wait(&q_full, 0, abort, a.pv.err);
+        for (int j = 0; ok && j < nloc; ++j) {
+          const int st = j % NS, b = j & 1;
+          ok = pf_wait(&kv_full[st], (uint32_t)(j / NS) & 1u, abort, a.pv.err);
+          if (!ok) break;
           tc_fence_after_sync();
-          const uint32_t pcol = tmem + (2 * x + b) * kPfKeys;
+          const uint64_t dks = dk + (uint64_t)((st * Cfg::kStageBytes) >> 4);
 #pragma unroll
-          for (int i = 0; i < kPfKeys / 16; ++i)
-            umma_bf16_tmem_a(tmem + Cfg::kColO + x * D, pcol + i * 8, dvs + (uint64_t)((i * 16 * 128) >> 4), idO,
-                             (j > 0 || i > 0) ? 1u : 0u);
-          umma_commit(&o_done[x][b]);
-          if (j == nloc - 1) umma_commit(&o_final[x]);
+          for (int x = 0; x < 2; ++x) {
+            if (j >= 2) {
+              ok = pf_wait(&o_done[x][b], (uint32_t)((j - 2) >> 1) & 1u, abort, a.pv.err);
+              if (!ok) break;
+              tc_fence_after_sync();
+            }
+#pragma unroll
+            for (int i = 0; i < D / 16; ++i) {
+              constexpr int kQRow = kPfM * 128, kKRow = kPfKeys * 128;
+              umma_bf16(tmem + (2 * x + b) * kPfKeys,
+                        dq + (uint64_t)((x * Cfg::kQBytes + (i >> 2) * kQRow + (i & 3) * 32) >> 4),
+                        dks + (uint64_t)(((i >> 2) * kKRow + (i & 3) * 32) >> 4), idS, i > 0 ? 1u : 0u);
+            }
+            umma_commit(&s_full[x][b]);
+          }
         }
-        umma_commit(&kv_empty[st]);
-      };
-      if (ok) issue_s(0);
-      if (ok && nloc > 1) issue_s(1);
-      for (int j = 0; ok && j < nloc; ++j) {
-        issue_pv(j);
-        if (ok && j + 2 < nloc) issue_s(j + 2);
+      } else {
+        // O_x += P_x . V of stage j, once the softmax has written P_x into tensor memory; the
+        // stage is free once this completes (its S was complete before P was written)
+        for (int j = 0; ok && j < nloc; ++j) {
+          const int st = j % NS, b = j & 1;
+          const uint64_t dvs = dv + (uint64_t)((st * Cfg::kStageBytes) >> 4);
+#pragma unroll
+          for (int x = 0; x < 2; ++x) {
+            ok = pf_wait(&p_full[x][b], (uint32_t)(j >> 1) & 1u, abort, a.pv.err);
+            if (!ok) break;
+            tc_fence_after_sync();
+            const uint32_t pcol = tmem + (2 * x + b) * kPfKeys;
+#pragma unroll
+            for (int i = 0; i < kPfKeys / 16; ++i)
+              umma_bf16_tmem_a(tmem + Cfg::kColO + x * D, pcol + i * 8, dvs + (uint64_t)((i * 16 * 128) >> 4), idO,
+                               (j > 0 || i > 0) ? 1u : 0u);
+            umma_commit(&o_done[x][b]);
+            if (j == nloc - 1) umma_commit(&o_final[x]);
+          }
+          if (!ok) break;
+          umma_commit(&kv_empty[st]);
+        }
       }
-      umma_commit(&drain);  // every MMA issued above completes before tensor memory is freed
-      mbar_wait_bounded(&drain, 0);
+      umma_commit(&drain[warp - 1]);  // every MMA this lane issued completes before tensor memory is freed
+      mbar_wait_bounded(&drain[warp - 1], 0);
     }
   } else if (warp >= 4) {
     // ---- softmax of query tile x: thread = row ----------------------------------------
