@@ -111,6 +111,13 @@ struct PfTiles {
   int chunk_tiles;
 };
 
+// How the producer copies one stage (see the producer).
+struct PfCopy {
+  int mode;          // 0 one pool box, 1 one chunk box, 2 per tile
+  int a, b;          // mode 0: row in block, first block; mode 1: first chunk row
+  int row[4];        // mode 2: pool row of tile u, or -1 - chunk row
+};
+
 // Where the keys of one 16-token tile of the stream come from.
 struct PfKeyTile {
   int kind;  // 0 ring, 1 chunk, 2 padding (no keys)
@@ -163,6 +170,7 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_kernel(const __grid_con
   __shared__ __align__(8) uint64_t q_full, s_full[2][2], p_full[2][2], o_done[2][2], o_final[2], drain[2];
   __shared__ uint32_t s_tmem;
   __shared__ int s_abort;
+  __shared__ PfCopy s_copy[32];  // copy plan of the producer's next 32 stages
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int H = a.pv.kv_heads;
@@ -259,111 +267,121 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_kernel(const __grid_con
   volatile int* abort = &s_abort;
 
   if (warp == 0) {
-    // ---- TMA producer -----------------------------------------------------------------
-    if (lane == 0) {
-      // both query tiles: box of G heads x QT tokens x 64 columns per column block
-      mbar_arrive_expect_tx(&q_full, 2 * Cfg::kHalves * QT * G * 128);
-      for (int x = 0; x < 2; ++x)
-        for (int hf = 0; hf < Cfg::kHalves; ++hf)
-          tma_load_3d(sbase + Cfg::kQOff + x * Cfg::kQBytes + hf * (kPfM * 128), &q_map, hf * 64, h * G,
-                      s * a.n_max + qa + x * QT, &q_full);
-      // block-table entries of a stage's ring tiles, fetched one stage ahead so their latency
-      // hides behind the wait for the slot (kind 0 ring tile, 1 chunk tile, 2 padding)
-      int nxt_kind[kPfSub], nxt_blk[kPfSub], nxt_r0[kPfSub];
-      auto fetch = [&](int j) {
-#pragma unroll
-        for (int u = 0; u < kPfSub; ++u) {
-          const int t = j * kPfSub + u;
-          nxt_kind[u] = t < tl.prior_tiles ? 0 : (t < ntiles ? 1 : 2);
-          nxt_blk[u] = 0;
-          nxt_r0[u] = 0;
-          if (t < tl.prior_tiles) {
-            int tile = tl.prior_first + t;
-            if (tile >= tl.C16) tile -= tl.C16;
-            const int t0 = tile << 4;
-            const int jb = a.bs_log2 >= 0 ? t0 >> a.bs_log2 : t0 / bs;
-            nxt_blk[u] = __ldg(tbl + jb);
-            nxt_r0[u] = t0 - jb * bs;
-          }
-        }
-      };
-      fetch(j0);
+    // ---- TMA producer (whole warp) ----------------------------------------------------
+    {
+      if (lane == 0) {
+        // both query tiles: box of G heads x QT tokens x 64 columns per column block
+        mbar_arrive_expect_tx(&q_full, 2 * Cfg::kHalves * QT * G * 128);
+        for (int x = 0; x < 2; ++x)
+          for (int hf = 0; hf < Cfg::kHalves; ++hf)
+            tma_load_3d(sbase + Cfg::kQOff + x * Cfg::kQBytes + hf * (kPfM * 128), &q_map, hf * 64, h * G,
+                        s * a.n_max + qa + x * QT, &q_full);
+      }
       int issued = 0;
-      for (int jj = 0; jj < nloc; ++jj) {
-        const int j = j0 + jj;  // stage of the stream (key tiles 4j ..); jj indexes the ring
-        const int st = jj % NS;
-        int kind[kPfSub], blk[kPfSub], r0[kPfSub];
+      // Copy plan of 32 stages at a time, one stage per lane (table lookups and index math in
+      // parallel), then lane 0 issues the copies.  mode 0: one 64-key box of the pool per K / V
+      // and column block (the ring tiles lie in consecutive blocks as a stage_map box covers
+      // them); 1: one 64-row box of the chunk; 2: per 16-row tile (rows: pool row, or -1 - chunk
+      // row for a chunk tile).
+      for (int c0 = 0; c0 < nloc; c0 += 32) {
+        if (__shfl_sync(0xffffffffu, (int)*abort, 0)) break;  // the same decision in every lane
+        {
+          const int jj = c0 + lane;
+          if (jj < nloc) {
+            const int j = j0 + jj;
+            int kind[kPfSub], blk[kPfSub], r0[kPfSub], row[kPfSub];
+            bool blk_ok = true;
 #pragma unroll
-        for (int u = 0; u < kPfSub; ++u) {
-          kind[u] = nxt_kind[u];
-          blk[u] = nxt_blk[u];
-          r0[u] = nxt_r0[u];
-        }
-        if (jj + 1 < nloc) fetch(j + 1);
-        // pool rows of the ring tiles (-1 for chunk tiles); padding tiles read pool row 0
-        // (finite, masked)
-        int row[kPfSub];
-        bool blk_ok = true;
-#pragma unroll
-        for (int u = 0; u < kPfSub; ++u) {
-          row[u] = kind[u] == 1 ? -1 : 0;
-          if (kind[u] == 0) {
-            int32_t b = blk[u];
-            if (b < 0 || (int64_t)b >= a.pv.total_blocks) {
-              atomicOr(a.pv.err, HWKV_DEVERR_BAD_BLOCK);
-              b = 0;
-              blk_ok = false;
-            }
-            row[u] = b * 2 * bs + r0[u];
-          }
-        }
-        // one copy per 64 keys when the stage's ring tiles lie in consecutive blocks the way a
-        // stage_map box covers them (box row 16u of (stage_tb rows) x (64 / stage_tb blocks)),
-        // or when the stage is all chunk rows
-        const int tb = a.stage_tb;
-        bool ring_stage = tb > 0 && blk_ok && kind[0] == 0 && kind[kPfSub - 1] == 0 && r0[0] + tb <= bs;
-#pragma unroll
-        for (int u = 1; u < kPfSub; ++u)
-          ring_stage = ring_stage && kind[u] == 0 && r0[u] == r0[0] + ((kTile * u) & (tb - 1)) &&
-                       blk[u] == blk[0] + (kTile * u) / max(tb, 1);
-        const bool chunk_stage = kind[0] == 1 && kind[kPfSub - 1] == 1;
-        if (jj >= NS && !pf_wait(&kv_empty[st], (uint32_t)((jj / NS) - 1) & 1u, abort, a.pv.err)) break;
-        const uint32_t kdst = sbase + Cfg::kStageOff + st * Cfg::kStageBytes;
-        const uint32_t vdst = kdst + Cfg::kKBytes;
-        mbar_arrive_expect_tx(&kv_full[st], Cfg::kStageBytes);
-        if (ring_stage) {
-#pragma unroll
-          for (int hf = 0; hf < Cfg::kHalves; ++hf) {
-            tma_load_3d(kdst + hf * (kPfKeys * 128), &stage_map, hf * 64, r0[0], blk[0], &kv_full[st]);
-            tma_load_3d(vdst + hf * (kPfKeys * 128), &stage_map, hf * 64, bs + r0[0], blk[0], &kv_full[st]);
-          }
-        } else if (chunk_stage) {
-          const int z = s * a.n_max + ((tl.chunk_first + j * kPfSub - tl.prior_tiles) << 4);
-#pragma unroll
-          for (int hf = 0; hf < Cfg::kHalves; ++hf) {
-            tma_load_3d(kdst + hf * (kPfKeys * 128), &knew64_map, hf * 64, h, z, &kv_full[st]);
-            tma_load_3d(vdst + hf * (kPfKeys * 128), &vnew64_map, hf * 64, h, z, &kv_full[st]);
-          }
-        } else {
-#pragma unroll
-          for (int u = 0; u < kPfSub; ++u) {
-#pragma unroll
-            for (int hf = 0; hf < Cfg::kHalves; ++hf) {
-              const uint32_t off = hf * (kPfKeys * 128) + u * (kTile * 128);
-              if (row[u] < 0) {
-                const int z = s * a.n_max + ((tl.chunk_first + j * kPfSub + u - tl.prior_tiles) << 4);
-                tma_load_3d(kdst + off, &knew_map, hf * 64, h, z, &kv_full[st]);
-                tma_load_3d(vdst + off, &vnew_map, hf * 64, h, z, &kv_full[st]);
-              } else {
-                tma_load_2d_l2(kdst + off, &pool_map, hf * 64, row[u], &kv_full[st]);
-                tma_load_2d_l2(vdst + off, &pool_map, hf * 64, row[u] + bs, &kv_full[st]);
+            for (int u = 0; u < kPfSub; ++u) {
+              const int t = j * kPfSub + u;
+              kind[u] = t < tl.prior_tiles ? 0 : (t < ntiles ? 1 : 2);
+              blk[u] = 0;
+              r0[u] = 0;
+              if (kind[u] == 0) {
+                int tile = tl.prior_first + t;
+                if (tile >= tl.C16) tile -= tl.C16;
+                const int t0 = tile << 4;
+                const int jb = a.bs_log2 >= 0 ? t0 >> a.bs_log2 : t0 / bs;
+                blk[u] = __ldg(tbl + jb);
+                r0[u] = t0 - jb * bs;
               }
             }
+#pragma unroll
+            for (int u = 0; u < kPfSub; ++u) {
+              if (kind[u] == 0) {
+                if (blk[u] < 0 || (int64_t)blk[u] >= a.pv.total_blocks) {
+                  atomicOr(a.pv.err, HWKV_DEVERR_BAD_BLOCK);
+                  blk[u] = 0;  // keep the barrier accounting intact; the result is flagged
+                  blk_ok = false;
+                }
+                row[u] = blk[u] * 2 * bs + r0[u];
+              } else if (kind[u] == 1) {
+                row[u] = -1 - ((tl.chunk_first + j * kPfSub + u - tl.prior_tiles) << 4);
+              } else {
+                row[u] = 0;  // padding: pool row 0 (finite, masked)
+              }
+            }
+            const int tb = a.stage_tb;
+            bool ring_stage = tb > 0 && blk_ok && kind[0] == 0 && kind[kPfSub - 1] == 0 && r0[0] + tb <= bs;
+#pragma unroll
+            for (int u = 1; u < kPfSub; ++u)
+              ring_stage = ring_stage && kind[u] == 0 && r0[u] == r0[0] + ((kTile * u) & (tb - 1)) &&
+                           blk[u] == blk[0] + (kTile * u) / max(tb, 1);
+            const bool chunk_stage = kind[0] == 1 && kind[kPfSub - 1] == 1;
+            PfCopy& cp = s_copy[lane];
+            cp.mode = ring_stage ? 0 : (chunk_stage ? 1 : 2);
+            cp.a = ring_stage ? r0[0] : (chunk_stage ? -1 - row[0] : 0);
+            cp.b = ring_stage ? blk[0] : 0;
+#pragma unroll
+            for (int u = 0; u < kPfSub; ++u) cp.row[u] = row[u];
           }
         }
-        ++issued;
+        __syncwarp();
+        if (lane == 0) {
+          for (int l = 0; l < 32 && c0 + l < nloc; ++l) {
+            const int jj = c0 + l;
+            const int st = jj % NS;
+            const PfCopy cp = s_copy[l];
+            if (jj >= NS && !pf_wait(&kv_empty[st], (uint32_t)((jj / NS) - 1) & 1u, abort, a.pv.err)) break;
+            const uint32_t kdst = sbase + Cfg::kStageOff + st * Cfg::kStageBytes;
+            const uint32_t vdst = kdst + Cfg::kKBytes;
+            mbar_arrive_expect_tx(&kv_full[st], Cfg::kStageBytes);
+            if (cp.mode == 0) {
+#pragma unroll
+              for (int hf = 0; hf < Cfg::kHalves; ++hf) {
+                tma_load_3d(kdst + hf * (kPfKeys * 128), &stage_map, hf * 64, cp.a, cp.b, &kv_full[st]);
+                tma_load_3d(vdst + hf * (kPfKeys * 128), &stage_map, hf * 64, bs + cp.a, cp.b, &kv_full[st]);
+              }
+            } else if (cp.mode == 1) {
+              const int z = s * a.n_max + cp.a;
+#pragma unroll
+              for (int hf = 0; hf < Cfg::kHalves; ++hf) {
+                tma_load_3d(kdst + hf * (kPfKeys * 128), &knew64_map, hf * 64, h, z, &kv_full[st]);
+                tma_load_3d(vdst + hf * (kPfKeys * 128), &vnew64_map, hf * 64, h, z, &kv_full[st]);
+              }
+            } else {
+#pragma unroll
+              for (int u = 0; u < kPfSub; ++u) {
+#pragma unroll
+                for (int hf = 0; hf < Cfg::kHalves; ++hf) {
+                  const uint32_t off = hf * (kPfKeys * 128) + u * (kTile * 128);
+                  if (cp.row[u] < 0) {
+                    const int z = s * a.n_max + (-1 - cp.row[u]);
+                    tma_load_3d(kdst + off, &knew_map, hf * 64, h, z, &kv_full[st]);
+                    tma_load_3d(vdst + off, &vnew_map, hf * 64, h, z, &kv_full[st]);
+                  } else {
+                    tma_load_2d_l2(kdst + off, &pool_map, hf * 64, cp.row[u], &kv_full[st]);
+                    tma_load_2d_l2(vdst + off, &pool_map, hf * 64, cp.row[u] + bs, &kv_full[st]);
+                  }
+                }
+              }
+            }
+            ++issued;
+          }
+        }
+        __syncwarp();
       }
-      if (*abort) {  // let the copies in flight land before the shared memory is released
+      if (lane == 0 && *abort) {  // let the copies in flight land before the shared memory is released
         for (int j = max(0, issued - NS); j < issued; ++j)
           if (!mbar_wait_bounded(&kv_full[j % NS], (uint32_t)(j / NS) & 1u)) break;
       }
