@@ -144,6 +144,30 @@ __device__ __forceinline__ PfKeyTile key_tile(const PfTiles& tl, int t, int C) {
   return k;
 }
 
+// Whether every key of stream stage j is visible to every live row of a query tile whose live
+// tokens sit at positions [pq_lo, pq_hi]: all four tiles full (resident ring slots or chunk
+// rows) and every key position in (pq_hi - w, pq_lo].  Such a stage needs no mask.
+__device__ __forceinline__ bool stage_clean(const PfTiles& tl, int j, int C, int p0, int n, int w, int pq_lo,
+                                            int pq_hi) {
+  bool clean = pq_lo <= pq_hi;
+#pragma unroll
+  for (int u = 0; u < 4; ++u) {
+    const PfKeyTile kt = key_tile(tl, j * 4 + u, C);
+    int k_lo = 0;
+    if (kt.kind == 0) {
+      clean = clean && kt.a + kTile - 1 < tl.rs.n;
+      k_lo = tl.p_oldest + kt.a;
+    } else if (kt.kind == 1) {
+      clean = clean && kt.a + kTile - 1 < n;
+      k_lo = p0 + kt.a;
+    } else {
+      clean = false;
+    }
+    clean = clean && k_lo + kTile - 1 <= pq_lo && k_lo > pq_hi - w;
+  }
+  return clean;
+}
+
 // bits lo .. hi (inclusive, clamped to 0 .. 15) of a 16-key tile
 __device__ __forceinline__ uint32_t range_bits(int lo, int hi) {
   lo = max(lo, 0);
@@ -171,6 +195,10 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_kernel(const __grid_con
   __shared__ uint32_t s_tmem;
   __shared__ int s_abort;
   __shared__ PfCopy s_copy[32];  // copy plan of the producer's next 32 stages
+  // bit jj: stage jj of this CTA needs no mask for query tile x (set by warp 3 ahead of the
+  // softmax; a bit not yet set only costs the masked path, which is exact for any stage)
+  constexpr int kCleanWords = 48;
+  __shared__ uint32_t s_clean[2][kCleanWords];
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int H = a.pv.kv_heads;
@@ -226,6 +254,9 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_kernel(const __grid_con
   }
   const int ntiles = tl.prior_tiles + tl.chunk_tiles;
   const int nst = (ntiles + kPfSub - 1) / kPfSub;
+  // the stage holding chunk rows past n, if any (only the stream's last tile can)
+  const int vz_stage =
+      (tl.chunk_tiles > 0 && ((tl.chunk_first + tl.chunk_tiles) << 4) > n) ? (ntiles - 1) / kPfSub : -1;
   // this CTA's stages [j0, j0 + nloc) of the stream; a split stream leaves a partial per CTA
   const bool split = sp > 1;
   const int j0 = split ? piece * a.split_stages[hi] : 0;
@@ -250,6 +281,7 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_kernel(const __grid_con
       }
       mbar_init(&o_final[x], 1);
     }
+    for (int i = 0; i < 2 * kCleanWords; ++i) s_clean[i / kCleanWords][i % kCleanWords] = 0u;
     mbar_init(&drain[0], 1);
     mbar_init(&drain[1], 1);
     s_abort = 0;
@@ -451,6 +483,25 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_kernel(const __grid_con
       umma_commit(&drain[warp - 1]);  // every MMA this lane issued completes before tensor memory is freed
       mbar_wait_bounded(&drain[warp - 1], 0);
     }
+  } else if (warp == 3) {
+    // ---- which stages are clean, 32 at a time ------------------------------------------
+    int pql[2], pqh[2];
+#pragma unroll
+    for (int x = 0; x < 2; ++x) {
+      pql[x] = p0 + qa + x * QT;
+      pqh[x] = p0 + min(n, qa + (x + 1) * QT) - 1;
+    }
+    for (int c0 = 0; c0 < nloc && c0 < 32 * kCleanWords; c0 += 32) {
+      const int jj = c0 + lane;
+      const bool in = jj < nloc;
+      const bool c_0 = in && stage_clean(tl, j0 + jj, C, p0, n, w, pql[0], pqh[0]);
+      const bool c_1 = in && stage_clean(tl, j0 + jj, C, p0, n, w, pql[1], pqh[1]);
+      const uint32_t b0 = __ballot_sync(0xffffffffu, c_0), b1 = __ballot_sync(0xffffffffu, c_1);
+      if (lane == 0) {
+        reinterpret_cast<volatile uint32_t*>(s_clean[0])[c0 >> 5] = b0;
+        reinterpret_cast<volatile uint32_t*>(s_clean[1])[c0 >> 5] = b1;
+      }
+    }
   } else if (warp >= 4) {
     // ---- softmax of query tile x: thread = row ----------------------------------------
     const int x = (warp - 4) >> 2;
@@ -479,25 +530,13 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_kernel(const __grid_con
       float sv[kPfKeys];
       tmem_ld64(lane_base + (2 * x + b) * kPfKeys, sv);
 
-      // where the stage's keys come from; a "clean" stage needs no mask for any live row
-      PfKeyTile kt[kPfSub];
-      bool clean = t_first <= t_last;
-#pragma unroll
-      for (int u = 0; u < kPfSub; ++u) {
-        kt[u] = key_tile(tl, j * kPfSub + u, C);
-        int k_lo = 0;
-        if (kt[u].kind == 0) {
-          clean = clean && kt[u].a + kTile - 1 < tl.rs.n;
-          k_lo = tl.p_oldest + kt[u].a;
-        } else if (kt[u].kind == 1) {
-          clean = clean && kt[u].a + kTile - 1 < n;
-          k_lo = p0 + kt[u].a;
-        } else {
-          clean = false;
-        }
-        clean = clean && k_lo + kTile - 1 <= pq_lo && k_lo > pq_hi - w;
-      }
+      // a "clean" stage needs no mask for any live row (precomputed by warp 3)
+      const bool clean =
+          jj < 32 * kCleanWords && ((reinterpret_cast<volatile uint32_t*>(s_clean[x])[jj >> 5] >> (jj & 31)) & 1u);
       if (!clean) {
+        PfKeyTile kt[kPfSub];
+#pragma unroll
+        for (int u = 0; u < kPfSub; ++u) kt[u] = key_tile(tl, j * kPfSub + u, C);
         // visible keys of this row per 16-key tile: position in (pq - w, pq], resident or in
         // the chunk, as intervals of the tile's key index
 #pragma unroll
@@ -566,12 +605,13 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_kernel(const __grid_con
       }
       const float bm = m_ref == kNegInf ? 0.f : m_ref;
 
-      // V rows past the chunk are zeroed: their P is 0, but 0 times a non-finite value is not
-      if (x == 0) {
-        bool need = false;
+      // V rows past the chunk are zeroed: their P is 0, but 0 times a non-finite value is not.
+      // Only the stream's last tile, a chunk tile, can hold such rows.
+      if (x == 0 && j == vz_stage) {
+        PfKeyTile kt[kPfSub];
 #pragma unroll
-        for (int u = 0; u < kPfSub; ++u) need = need || (kt[u].kind == 1 && kt[u].a + kTile > n);
-        if (need) {
+        for (int u = 0; u < kPfSub; ++u) kt[u] = key_tile(tl, j * kPfSub + u, C);
+        {
           ok = __all_sync(0xffffffffu, pf_wait(&kv_full[jj % NS], (uint32_t)(jj / NS) & 1u, abort, a.pv.err));
           if (!ok) break;
           const uint32_t vst = sbase + Cfg::kStageOff + (jj % NS) * Cfg::kStageBytes + Cfg::kKBytes;
