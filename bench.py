@@ -36,8 +36,8 @@ FALLBACK_HBM_GBS = 6800.0
 # dram__bytes_read.sum + dram__bytes_write.sum per decode launch from one ncu capture of
 # the tensor-core decode kernel, with the sha256 of hwkv_decode_tc.cu it was taken on.  When
 # the kernel source changes the figure no longer applies and is reported as null.
-DECODE_TRAFFIC = {"source_sha256": "131952ec1f3bec1a1ad73f3c34094ffaeb4bef3506ac06bb7497e158ccda61e9",
-                  "bytes_per_launch": (621.202688 + 3.634176 + 489.018624 + 3.222784) / 2 * 1e6,
+DECODE_TRAFFIC = {"source_sha256": "57d9ccf2aa8683ba903041e9ebb22f058c78562168cb59a324dde5d331600873",
+                  "bytes_per_launch": (621.200128 + 3.629056 + 489.014272 + 3.395584) / 2 * 1e6,
                   "launch": "layers 0 and 1 of the full workload (2-layer run, same per-launch shape)"}
 
 
