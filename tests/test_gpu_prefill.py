@@ -146,6 +146,10 @@ CASES = {
     # long key streams (about 130 stages of 64 keys per CTA), so the kernel's pipeline barriers
     # run through many phases
     "deep": dict(kv_heads=2, windows=((8192, 2048),), prefill=(9000, 2100), chunks=[[160, 70]]),
+    # block sizes 32 and 128: whole-stage pool copies of two blocks x 32 rows and of 64 rows
+    # inside one block (at several row offsets), plus the per-tile fallback where they do not fit
+    "bs32": dict(kv_heads=2, block_size=32, windows=((200, 1000),), prefill=(700, 50), chunks=[[90, 40]]),
+    "bs128": dict(kv_heads=2, block_size=128, windows=((256, 2048),), prefill=(3000, 129), chunks=[[100, 300]]),
     # key streams split over several CTAs and merged (forced by a small stage cap): long and
     # short streams, empty splits past short contexts, a zero-length chunk, group 16, two layers
     "split_deep": dict(kv_heads=2, windows=((8192, 2048),), prefill=(9000, 2100), chunks=[[160, 70]], max_stages=9),
@@ -263,3 +267,38 @@ def test_prefill_full_size_sampled(name):
             got = out[s, t].float().cpu().double().numpy()
             assert_close(got, ref, cfg, f"{name} seq {s} token {t}")
     pool.close()
+
+
+@pytest.mark.parametrize("block_size", [16, 64])
+def test_prefill_block_permutation_leaves_output_bit_identical(block_size):
+    """The same chunk through an identity and a permuted block table (blocks moved with it):
+    outputs bit-identical, rings equal after moving back.  With permuted ids a stage's ring tiles
+    are no longer consecutive blocks, so the kernel copies tile by tile instead of per stage."""
+    cfg = small_config(name="pfperm", cfg_id=95, kv_heads=2, block_size=block_size, windows=((1024, 192),),
+                       prefill=(1500, 300))
+    dev = torch.device("cuda")
+    wl = workloads.Workload(cfg, device=dev)
+    pre = torch.tensor(cfg.prefill, dtype=torch.int32, device=dev)
+    K, V = wl.prefill_layer(0, dev)
+    q, k, v = wl.chunk_inputs(0, 0, 150, dev)
+    nt = torch.tensor([150, 97], dtype=torch.int32, device=dev)
+    pools = [hw.Pool(1, 2, 128, block_size, cfg.windows_array(), 2, torch.bfloat16, q_heads=cfg.q_heads)
+             for _ in range(2)]
+    for p in pools:
+        p.materialize(0, K, V, pre)
+    _, total, _ = pools[1].geometry()
+    perm = np.random.default_rng(1).permutation(total).astype(np.int32)
+    blocks = pools[1].blocks()
+    moved = torch.empty_like(blocks)
+    moved[torch.as_tensor(perm, device=dev).long()] = blocks
+    blocks.copy_(moved)
+    pools[1].set_block_table(perm)
+    outs = [p.prefill(0, q, cfg.scale, k, v, pre, nt) for p in pools]
+    torch.cuda.synchronize()
+    for s, n in enumerate((150, 97)):
+        assert torch.equal(outs[0][s, :n], outs[1][s, :n]), f"seq {s}"
+    back = pools[1].blocks()[torch.as_tensor(perm, device=dev).long()]
+    assert torch.equal(back, pools[0].blocks())
+    for p in pools:
+        assert p.check_device_errors() == 0
+        p.close()
