@@ -216,6 +216,8 @@ __global__ void __launch_bounds__(kWarps * 32, 2) decode_sk_kernel(const __grid_
   const int bs = a.pv.block_size;
   __nv_bfloat16* const out = static_cast<__nv_bfloat16*>(a.out);
 
+  // the descriptor is a kernel parameter, so it may be fetched before the wait below
+  if (threadIdx.x == 0) prefetch_tensormap(&tmap);
   // launched as a programmatic dependent: everything below reads what earlier kernels wrote
   griddep_wait();
 

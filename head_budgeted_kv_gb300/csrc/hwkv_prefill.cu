@@ -201,6 +201,15 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_kernel(const __grid_con
   __shared__ uint32_t s_clean[2][kCleanWords];
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) {  // the TMA descriptors, ahead of their first use
+    prefetch_tensormap(&q_map);
+    prefetch_tensormap(&stage_map);
+    prefetch_tensormap(&pool_map);
+    prefetch_tensormap(&knew64_map);
+    prefetch_tensormap(&vnew64_map);
+    prefetch_tensormap(&knew_map);
+    prefetch_tensormap(&vnew_map);
+  }
   const int H = a.pv.kv_heads;
   const int G = a.group;
   const int QT = kPfM / G;  // tokens per query tile
