@@ -195,7 +195,8 @@ def bench_config(cfg, args, world_size: int, step_bytes=None) -> dict:
          "parallelism": "replicas" if world_size > 1 else "single",
          "path": args.path + (" (CUDA graph per step)" if args.graph else ""),
          "kernel": ["auto", "tensor", "simt"][args.kernel],
-         "workers": args.workers or "auto", "split_tokens": args.split or "auto"}
+         "workers": args.workers or "auto", "split_tokens": args.split or "auto",
+         "early_reads": args.path == "fused" and not args.no_early_reads}
     if step_bytes is None:
         step_bytes = mean_step_bytes(cfg, args.warmup, args.steps)
     c["l2"] = f"inputs larger than L2: {step_bytes / 1e9:.2f} GB of resident KV read per step"
@@ -344,6 +345,8 @@ def run_hwkv(args, cfg):
         graph = DecodeStepGraph(pool, cfg.scale, cfg.q_heads, pos_all[0], fused=fused)
         launches_per_step = hw.binding.hwkv_kernel_launches() - before  # kernels recorded per step
 
+    early = fused and not args.no_early_reads
+
     def run_step(i, ev=None):
         if graph is not None and ev is None:
             # the step's inputs land in the graph's static buffers; positions advance in-graph
@@ -356,7 +359,10 @@ def run_hwkv(args, cfg):
             if fused:
                 if ev is not None:
                     ev[l][0].record(stream)
-                pool.append_decode(l, qs[i][l], cfg.scale, kns[i][l], vns[i][l], pos_all[i], out=outs[l])
+                # positions are prepared before the timed region and this layer's pool was last
+                # written a step ago: the schedule may start before the previous launch ends
+                pool.append_decode(l, qs[i][l], cfg.scale, kns[i][l], vns[i][l], pos_all[i], out=outs[l],
+                                   early_reads=early)
             else:
                 pool.append(l, kns[i][l], vns[i][l], pos_all[i])
                 if ev is not None:
@@ -449,7 +455,7 @@ def run_hwkv(args, cfg):
         d_pos.copy_(h_pos[k], non_blocking=True)
         if fused:
             for l in range(cfg.layers):
-                pool.append_decode(l, d_q[l], cfg.scale, d_k[l], d_v[l], d_pos, out=outs[l])
+                pool.append_decode(l, d_q[l], cfg.scale, d_k[l], d_v[l], d_pos, out=outs[l], early_reads=early)
         else:
             torch.add(d_pos, 1, out=d_lens)
             for l in range(cfg.layers):
@@ -607,6 +613,8 @@ def main(argv=None):
                    help="prefill mode: split key streams longer than this many 64-key stages (0 = automatic)")
     p.add_argument("--kernel", type=int, default=0)
     p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--no-early-reads", action="store_true",
+                   help="decode without HWKV_DECODE_EARLY_READS (schedule waits for the previous launch)")
     p.add_argument("--cpu-budget", type=float, default=12.0)
     args = p.parse_args(argv)
     if args.warmup < 3:

@@ -84,23 +84,27 @@ class Pool:
     def append(self, layer: int, k_new, v_new, pos, stream=None):
         hwkv_append(self.handle, layer, k_new, v_new, pos, stream)
 
-    def decode(self, layer: int, q, scale: float, lens, out=None, stream=None):
+    def decode(self, layer: int, q, scale: float, lens, out=None, stream=None, early_reads: bool = False):
         if out is None:
             out = torch.empty_like(q)
         if q.shape[1] != self.q_heads:
             self.q_heads = q.shape[1]
             self._size_workspace()
-        hwkv_decode_attn(self.handle, layer, q, scale, lens, out, self.workspace, stream)
+        hwkv_decode_attn(self.handle, layer, q, scale, lens, out, self.workspace, stream, early_reads)
         return out
 
-    def append_decode(self, layer: int, q, scale: float, k_new, v_new, pos, out=None, stream=None):
-        """Append the new token (positions ``pos``) and decode at ``pos + 1`` in one call."""
+    def append_decode(self, layer: int, q, scale: float, k_new, v_new, pos, out=None, stream=None,
+                      early_reads: bool = False):
+        """Append the new token (positions ``pos``) and decode at ``pos + 1`` in one call.
+        early_reads: the caller's guarantee of HWKV_DECODE_EARLY_READS (lengths, block table
+        and this layer's pool not written by the kernel just before in the stream)."""
         if out is None:
             out = torch.empty_like(q)
         if q.shape[1] != self.q_heads:
             self.q_heads = q.shape[1]
             self._size_workspace()
-        hwkv_append_decode_attn(self.handle, layer, q, scale, k_new, v_new, pos, out, self.workspace, stream)
+        hwkv_append_decode_attn(self.handle, layer, q, scale, k_new, v_new, pos, out, self.workspace, stream,
+                                early_reads)
         return out
 
     def prefill(self, layer: int, q, scale: float, k_new, v_new, pos, n, out=None, stream=None):

@@ -32,6 +32,7 @@ HWKV_F32 = 0
 HWKV_BF16 = 1
 HWKV_KERNEL_AUTO, HWKV_KERNEL_TENSOR, HWKV_KERNEL_SIMT = 0, 1, 2
 HWKV_DEVERR_NEG_LENGTH, HWKV_DEVERR_BAD_BLOCK, HWKV_DEVERR_SRC_RANGE, HWKV_DEVERR_WAIT_TIMEOUT = 1, 2, 4, 8
+HWKV_DECODE_EARLY_READS = 1
 
 _c_i32p = ctypes.POINTER(ctypes.c_int32)
 _c_u64p = ctypes.POINTER(ctypes.c_uint64)
@@ -57,6 +58,7 @@ SIGNATURES = [
     ("hwkv_decode_workspace_bytes", _i, [_vp, _i, _c_u64p]),
     ("hwkv_decode_attn", _i, [_vp, _i, _vp, _i, ctypes.c_float, _vp, _vp, _vp, _u64, _vp]),
     ("hwkv_append_decode_attn", _i, [_vp, _i, _vp, _i, ctypes.c_float, _vp, _vp, _vp, _vp, _vp, _u64, _vp]),
+    ("hwkv_decode_attn_ex", _i, [_vp, _i, _vp, _i, ctypes.c_float, _vp, _vp, _vp, _vp, _vp, _u64, _i, _vp]),
     ("hwkv_decode_attn_noalloc", _i, [_vp, _i, _vp, _i, ctypes.c_float, _vp, _vp, _vp]),
     ("hwkv_prefill_attn", _i, [_vp, _i, _vp, _i, ctypes.c_float, _vp, _vp, _i, _vp, _vp, _vp, _vp, _u64, _vp]),
     ("hwkv_prefill_workspace_bytes", _i, [_vp, _i, _i, _i, ctypes.POINTER(_u64)]),
@@ -95,7 +97,7 @@ def load(build_if_missing: bool = True):
         fn = getattr(lib, name)
         fn.restype = res
         fn.argtypes = args
-    if lib.hwkv_abi_version() != 2:
+    if lib.hwkv_abi_version() != 3:
         raise RuntimeError("libhwkv.so ABI version mismatch")
     _lib = lib
     return lib
@@ -218,22 +220,34 @@ def hwkv_decode_workspace_bytes(pool: int, q_heads: int) -> int:
 
 
 def hwkv_decode_attn(pool: int, layer: int, q: torch.Tensor, scale: float, lens: torch.Tensor, out: torch.Tensor,
-                     workspace: Optional[torch.Tensor], stream=None):
-    """q, out: contiguous [B][Hq][D]; lens: int32 [B] lengths after the append."""
+                     workspace: Optional[torch.Tensor], stream=None, early_reads: bool = False):
+    """q, out: contiguous [B][Hq][D]; lens: int32 [B] lengths after the append.  early_reads sets
+    HWKV_DECODE_EARLY_READS (see the header for the caller's guarantee)."""
     if not (q.is_contiguous() and out.is_contiguous()):
         raise ValueError("q and out must be contiguous")
     ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    if early_reads:
+        _check(load().hwkv_decode_attn_ex(pool, layer, _ptr(q), q.shape[1], float(scale), None, None, _ptr(lens),
+                                          _ptr(out), _ptr(workspace), ws_bytes, HWKV_DECODE_EARLY_READS,
+                                          _stream_ptr(stream)))
+        return
     _check(load().hwkv_decode_attn(pool, layer, _ptr(q), q.shape[1], float(scale), _ptr(lens), _ptr(out),
                                    _ptr(workspace), ws_bytes, _stream_ptr(stream)))
 
 
 def hwkv_append_decode_attn(pool: int, layer: int, q: torch.Tensor, scale: float, k_new: torch.Tensor,
                             v_new: torch.Tensor, pos: torch.Tensor, out: torch.Tensor,
-                            workspace: Optional[torch.Tensor], stream=None):
-    """Append (k_new, v_new at positions pos) then decode at pos + 1, in one call."""
+                            workspace: Optional[torch.Tensor], stream=None, early_reads: bool = False):
+    """Append (k_new, v_new at positions pos) then decode at pos + 1, in one call.  early_reads
+    sets HWKV_DECODE_EARLY_READS (see the header for the caller's guarantee)."""
     if not (q.is_contiguous() and out.is_contiguous() and k_new.is_contiguous() and v_new.is_contiguous()):
         raise ValueError("q, out, k_new and v_new must be contiguous")
     ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    if early_reads:
+        _check(load().hwkv_decode_attn_ex(pool, layer, _ptr(q), q.shape[1], float(scale), _ptr(k_new), _ptr(v_new),
+                                          _ptr(pos), _ptr(out), _ptr(workspace), ws_bytes, HWKV_DECODE_EARLY_READS,
+                                          _stream_ptr(stream)))
+        return
     _check(load().hwkv_append_decode_attn(pool, layer, _ptr(q), q.shape[1], float(scale), _ptr(k_new), _ptr(v_new),
                                           _ptr(pos), _ptr(out), _ptr(workspace), ws_bytes, _stream_ptr(stream)))
 

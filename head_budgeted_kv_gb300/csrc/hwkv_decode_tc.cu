@@ -50,7 +50,7 @@ __device__ __forceinline__ Group load_group(const DecodeArgs& a, int g) {
   const int H = a.pv.kv_heads;
   gr.s = g / H;
   gr.h = g - gr.s * H;
-  int len = a.lens[gr.s] + a.len_add;
+  int len = __ldcg(a.lens + gr.s) + a.len_add;  // L2: may be read before the dependent-launch wait
   gr.len = len < 0 ? 0 : len;
   const int C = (a.g.nblk_prefix[gr.h + 1] - a.g.nblk_prefix[gr.h]) * a.pv.block_size;
   gr.rs = resident(gr.len, a.g.window[gr.h], C);
@@ -218,12 +218,16 @@ __global__ void __launch_bounds__(kWarps * 32, 2) decode_sk_kernel(const __grid_
 
   // the descriptor is a kernel parameter, so it may be fetched before the wait below
   if (threadIdx.x == 0) prefetch_tensormap(&tmap);
-  // launched as a programmatic dependent: everything below reads what earlier kernels wrote
-  griddep_wait();
+  // Launched as a programmatic dependent.  By default everything waits for the grids this one
+  // depends on.  With a.early the caller guarantees that the lengths, the block table and this
+  // layer's pool were written before the preceding grid in the stream started, so the schedule
+  // and the first tile loads run before the wait; q, k_new / v_new and every write of this
+  // grid come after it.
+  if (!a.early) griddep_wait();
 
   if (cta == 0) {
     for (int s = threadIdx.x; s < B; s += W * 32)
-      if (a.lens[s] + a.len_add < 0) atomicOr(a.pv.err, HWKV_DEVERR_NEG_LENGTH);
+      if (__ldcg(a.lens + s) + a.len_add < 0) atomicOr(a.pv.err, HWKV_DEVERR_NEG_LENGTH);
   }
 
   // ---- schedule: needed tiles per group, their prefix sums, this CTA's range ----------
@@ -247,21 +251,14 @@ __global__ void __launch_bounds__(kWarps * 32, 2) decode_sk_kernel(const __grid_
       pre += c;
     }
   }
-  // groups with nothing resident (length 0) get a zero output, each from one CTA
-  for (int g = cta; g < ngroups; g += nctas) {
-    const Group gr = load_group(a, g);
-    if (gr.tiles == 0)
-      for (int e = threadIdx.x; e < G * D; e += W * 32)
-        out[((int64_t)gr.s * Hq + gr.h * G + e / D) * D + e % D] = __float2bfloat16_rn(0.f);
-  }
   if (threadIdx.x == 0) {
     for (int i = 0; i < W * NS; ++i) mbar_init(&bars[i], 1);
     fence_mbar_init();
   }
   __syncthreads();
-  if (t_lo >= t_hi || s_start[0] < 0) return;
-  const int g_start = (int)s_start[0];
-  const long long pre_start = s_start[1];
+  const bool has_range = t_lo < t_hi && s_start[0] >= 0;
+  const int g_start = has_range ? (int)s_start[0] : 0;
+  const long long pre_start = has_range ? s_start[1] : 0;
 
   // ---- per-warp TMA pipeline ---------------------------------------------------------
   uint64_t* wbar = bars + warp * NS;
@@ -283,7 +280,8 @@ __global__ void __launch_bounds__(kWarps * 32, 2) decode_sk_kernel(const __grid_
       const int t0 = tile_slot(igr, j_issue - ipre);
       const int jb = t0 / bs;
       const int r0 = t0 - jb * bs;
-      int32_t blk = igr.tbl[jb];
+      // the first stages may be issued before the dependent-launch wait: read through L2
+      int32_t blk = issued < NS ? __ldcg(igr.tbl + jb) : igr.tbl[jb];
       if (blk < 0 || (int64_t)blk >= a.pv.total_blocks) {
         atomicOr(a.pv.err, HWKV_DEVERR_BAD_BLOCK);
         blk = 0;  // keep the barrier accounting intact; the result is flagged
@@ -302,7 +300,17 @@ __global__ void __launch_bounds__(kWarps * 32, 2) decode_sk_kernel(const __grid_
     ++issued;
   };
   // the first stages are issued by different lanes so their table lookups overlap
-  for (int i = 0; i < NS && j_issue < t_hi; ++i) issue_next(i);
+  if (has_range)
+    for (int i = 0; i < NS && j_issue < t_hi; ++i) issue_next(i);
+  if (a.early) griddep_wait();
+  // groups with nothing resident (length 0) get a zero output, each from one CTA
+  for (int g = cta; g < ngroups; g += nctas) {
+    const Group gr = load_group(a, g);
+    if (gr.tiles == 0)
+      for (int e = threadIdx.x; e < G * D; e += W * 32)
+        out[((int64_t)gr.s * Hq + gr.h * G + e / D) * D + e % D] = __float2bfloat16_rn(0.f);
+  }
+  if (!has_range) return;
 
   // ldmatrix lane roles: matrix mi = lane/8, row rr = lane%8
   const int mi = lane >> 3, rr = lane & 7;

@@ -607,8 +607,9 @@ namespace {
 // (len_add 1: lens are the positions before the append, k_new / v_new are appended).
 int decode_common(hwkv_pool_t p, int layer, const void* q, int q_heads, float scale, const int32_t* lens_dev,
                   int len_add, const void* k_new, const void* v_new, void* out, void* workspace, uint64_t ws_bytes,
-                  void* stream) {
+                  int flags, void* stream) {
   if (!p) return fail(HWKV_ERR_INVALID_ARG, "pool is NULL");
+  if (flags & ~HWKV_DECODE_EARLY_READS) return fail(HWKV_ERR_INVALID_ARG, "unknown decode flags %#x", flags);
   const Geometry& g = p->g;
   if (layer < 0 || layer >= g.layers) return fail(HWKV_ERR_INVALID_ARG, "layer %d out of range", layer);
   if (q_heads < g.kv_heads || q_heads % g.kv_heads != 0 || q_heads / g.kv_heads > kMaxGroup)
@@ -646,6 +647,7 @@ int decode_common(hwkv_pool_t p, int layer, const void* q, int q_heads, float sc
   a.out = out;
   a.lens = lens_dev;
   a.len_add = len_add;
+  a.early = (flags & HWKV_DECODE_EARLY_READS) ? 1 : 0;
   const WorkspaceLayout wl = workspace_layout(p, G);
   char* ws = static_cast<char*>(workspace);
   a.part_acc = ws ? reinterpret_cast<float*>(ws + wl.acc1) : nullptr;
@@ -690,13 +692,22 @@ extern "C" {
 
 int hwkv_decode_attn(hwkv_pool_t p, int layer, const void* q, int q_heads, float scale, const int32_t* lens_dev,
                      void* out, void* workspace, uint64_t ws_bytes, void* stream) {
-  return decode_common(p, layer, q, q_heads, scale, lens_dev, 0, nullptr, nullptr, out, workspace, ws_bytes, stream);
+  return decode_common(p, layer, q, q_heads, scale, lens_dev, 0, nullptr, nullptr, out, workspace, ws_bytes, 0,
+                       stream);
+}
+
+int hwkv_decode_attn_ex(hwkv_pool_t p, int layer, const void* q, int q_heads, float scale, const void* k_new,
+                        const void* v_new, const int32_t* lens_dev, void* out, void* workspace, uint64_t ws_bytes,
+                        int flags, void* stream) {
+  const bool fused = k_new != nullptr || v_new != nullptr;
+  return decode_common(p, layer, q, q_heads, scale, lens_dev, fused ? 1 : 0, k_new, v_new, out, workspace, ws_bytes,
+                       flags, stream);
 }
 
 int hwkv_append_decode_attn(hwkv_pool_t p, int layer, const void* q, int q_heads, float scale, const void* k_new,
                             const void* v_new, const int32_t* pos_dev, void* out, void* workspace, uint64_t ws_bytes,
                             void* stream) {
-  return decode_common(p, layer, q, q_heads, scale, pos_dev, 1, k_new, v_new, out, workspace, ws_bytes, stream);
+  return decode_common(p, layer, q, q_heads, scale, pos_dev, 1, k_new, v_new, out, workspace, ws_bytes, 0, stream);
 }
 
 int hwkv_prefill_workspace_bytes(hwkv_pool_t p, int layer, int q_heads, int n_max, uint64_t* out) {

@@ -54,6 +54,7 @@ struct DecodeArgs {
   void* out;               // [B][Hq][D]
   const int32_t* lens;     // [B]; length after the append = lens[s] + len_add
   int32_t len_add;         // 0: lens are lengths after the append; 1: positions (fused append)
+  int32_t early;           // schedule and first tile loads may run before the dependent-launch wait
   const void* k_new;       // fused append: new K / V rows [B][H][D], else null
   const void* v_new;
   float* part_acc;         // [slots][G][D]   unnormalised split accumulators

@@ -53,7 +53,10 @@ class DecodeStepGraph:
             torch.add(self.pos, 1, out=self.lens)
         for l in range(p.layers):
             if self.fused:
-                p.append_decode(l, self.q[l], self.scale, self.k_new[l], self.v_new[l], self.pos, out=self.out[l])
+                # after layer 0 the kernel just before is the previous layer's attention, which
+                # writes neither the positions nor this layer's pool
+                p.append_decode(l, self.q[l], self.scale, self.k_new[l], self.v_new[l], self.pos, out=self.out[l],
+                                early_reads=l > 0)
             else:
                 p.append(l, self.k_new[l], self.v_new[l], self.pos)
                 p.decode(l, self.q[l], self.scale, self.lens, out=self.out[l])

@@ -43,7 +43,7 @@
 extern "C" {
 #endif
 
-#define HWKV_ABI_VERSION 2
+#define HWKV_ABI_VERSION 3
 
 /* status codes */
 #define HWKV_OK 0
@@ -177,6 +177,25 @@ int hwkv_decode_attn(hwkv_pool_t pool, int layer, const void* q, int q_heads, fl
 int hwkv_append_decode_attn(hwkv_pool_t pool, int layer, const void* q, int q_heads, float scale,
                             const void* k_new, const void* v_new, const int32_t* pos_dev, void* out,
                             void* workspace, uint64_t workspace_bytes, void* stream);
+
+/* Flags of hwkv_decode_attn_ex. */
+#define HWKV_DECODE_EARLY_READS 1
+
+/* hwkv_decode_attn (k_new = v_new = NULL; lens_dev = lengths after the append) or
+ * hwkv_append_decode_attn (k_new, v_new given; lens_dev = positions before the append), with
+ * flags:
+ *   HWKV_DECODE_EARLY_READS  the caller guarantees that lens_dev, the block table and this
+ *     layer's pool were last written by work that completed before the kernel that immediately
+ *     precedes this call in `stream` started (e.g. lengths set once per step before layer 0,
+ *     and a previous layer's attention just before).  The tensor-core kernel then computes its
+ *     schedule and issues its first K/V loads while that kernel is still finishing (it is
+ *     launched as a programmatic dependent), and waits for it only before it reads q, k_new,
+ *     v_new or writes anything.  Same results as without the flag.  Do not set it on the call
+ *     that follows the kernel which updates the lengths.  Ignored by the CUDA-core kernel.
+ * Errors as hwkv_decode_attn; HWKV_ERR_INVALID_ARG for unknown flags. */
+int hwkv_decode_attn_ex(hwkv_pool_t pool, int layer, const void* q, int q_heads, float scale, const void* k_new,
+                        const void* v_new, const int32_t* lens_dev, void* out, void* workspace,
+                        uint64_t workspace_bytes, int flags, void* stream);
 
 /* Bytes of the static scratch array behind hwkv_decode_attn_noalloc. */
 #define HWKV_NOALLOC_SCRATCH_BYTES (4u << 20)

@@ -36,7 +36,7 @@ def test_every_declared_function_is_exported(lib):
 
 
 def test_abi_version_and_status_strings(lib):
-    assert binding.hwkv_abi_version() == 2
+    assert binding.hwkv_abi_version() == 3
     assert binding.status_string(0) == "HWKV_OK"
     assert binding.status_string(binding.HWKV_ERR_POOL_TOO_SMALL) == "HWKV_ERR_POOL_TOO_SMALL"
 

@@ -49,3 +49,32 @@ def test_graph_replay_equals_eager(fused, kernel):
     assert eager.device_errors() == 0 and graphed.device_errors() == 0
     eager.close()
     graphed.close()
+
+
+def test_early_reads_equal_default_bit_for_bit():
+    """Chained fused launches with HWKV_DECODE_EARLY_READS (positions prepared up front, no
+    synchronisation between launches, so each schedule may start while the previous launch
+    finishes) give the same outputs and rings as the default launches."""
+    cfg = small_config(name="early", cfg_id=96, layers=3, kv_heads=2, windows=((4096, 64), (256, 1024), (32, 2048)),
+                       prefill=(3000, 700, 90), steps=4)
+    results = []
+    for early in (False, True):
+        run = Run(cfg, fused=True)
+        run.materialize()
+        dev = run.dev
+        pre = torch.tensor(cfg.prefill, dtype=torch.int32, device=dev)
+        pos = [(pre + i).contiguous() for i in range(cfg.steps)]
+        ins = [run.wl.step_inputs(i, dev) for i in range(cfg.steps)]
+        outs = torch.zeros((cfg.steps, cfg.layers, cfg.batch, cfg.q_heads, cfg.head_dim), dtype=torch.bfloat16,
+                           device=dev)
+        torch.cuda.synchronize()
+        for i in range(cfg.steps):
+            q, kn, vn = ins[i]
+            for l in range(cfg.layers):
+                run.pool.append_decode(l, q[l], cfg.scale, kn[l], vn[l], pos[i], out=outs[i, l], early_reads=early)
+        torch.cuda.synchronize()
+        assert run.device_errors() == 0
+        results.append((outs.clone(), run.pool.buffer.clone()))
+        run.close()
+    assert torch.equal(results[0][0], results[1][0])
+    assert torch.equal(results[0][1], results[1][1])
