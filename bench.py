@@ -36,8 +36,8 @@ FALLBACK_HBM_GBS = 6800.0
 # dram__bytes_read.sum + dram__bytes_write.sum per decode launch from one ncu capture of
 # the tensor-core decode kernel, with the sha256 of hwkv_decode_tc.cu it was taken on.  When
 # the kernel source changes the figure no longer applies and is reported as null.
-DECODE_TRAFFIC = {"source_sha256": "f71a5c9d165b74a2c83c17e56018b6571a58cc9a5d1856524f889f431cd811ec",
-                  "bytes_per_launch": (621.217280 + 3.211264 + 489.059584 + 0.260352) / 2 * 1e6,
+DECODE_TRAFFIC = {"source_sha256": "9fabd4485475a464623225c16a523e7a943b2701658ce689121c1f39e1629bc0",
+                  "bytes_per_launch": (621.200384 + 2.865664 + 489.036800 + 0.393472) / 2 * 1e6,
                   "launch": "layers 0 and 1 of the full workload (2-layer run, same per-launch shape)"}
 
 
@@ -501,7 +501,10 @@ def run_hwkv(args, cfg):
         achieved = isolated
         how = "events around each launch in a separate pass of the same steps"
     sha = decode_source_sha()
-    traffic = DECODE_TRAFFIC["bytes_per_launch"] if DECODE_TRAFFIC["source_sha256"] == sha else None
+    # the DRAM counters were taken on the full workload's fused launches: they describe no other
+    # workload's launches
+    traffic = (DECODE_TRAFFIC["bytes_per_launch"]
+               if DECODE_TRAFFIC["source_sha256"] == sha and cfg.name.split("_")[0] == "full" and fused else None)
     value = units / (max_ms / 1e3)
     line = {
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": ws, "steps": args.steps,

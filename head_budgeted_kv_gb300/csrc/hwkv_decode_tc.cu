@@ -15,7 +15,10 @@
 // of a segment the warps' online-softmax states are merged in shared memory; a group held by
 // one CTA is written out directly, otherwise the CTA stores a partial (m, l, acc) and bumps
 // the group's arrival counter, and the CTA that arrives last merges all partials of the group
-// and writes the output (no CTA ever waits for another).
+// and writes the output (no CTA ever waits for another).  After a CTA's last tile its stage
+// buffers are free, and a merge there fetches the whole partial block with one bulk copy.
+// The sequence lengths are staged in shared memory once, so crossing into the next group
+// costs no global round trip.
 //
 // Per tile (16 tokens), per warp, with the GQA group (G <= 16 query heads, zero-padded to one
 // or two 8-column n-tiles) on the N side of mma.sync.m16n8k16 bf16 -> fp32:
@@ -45,13 +48,21 @@ struct Group {
   const int32_t* tbl;
 };
 
-__device__ __forceinline__ Group load_group(const DecodeArgs& a, int g) {
+constexpr int kLensCache = 256;  // sequence lengths a CTA stages in shared memory
+
+// length of sequence s after the append, clamped at 0
+__device__ __forceinline__ int seq_len(const DecodeArgs& a, int s) {
+  const int len = __ldcg(a.lens + s) + a.len_add;  // L2: may be read before the dependent-launch wait
+  return len < 0 ? 0 : len;
+}
+
+// Group g; its sequence length comes from `s_lens` (shared memory) when that is non-null.
+__device__ __forceinline__ Group load_group(const DecodeArgs& a, const int* s_lens, int g) {
   Group gr;
   const int H = a.pv.kv_heads;
   gr.s = g / H;
   gr.h = g - gr.s * H;
-  int len = __ldcg(a.lens + gr.s) + a.len_add;  // L2: may be read before the dependent-launch wait
-  gr.len = len < 0 ? 0 : len;
+  gr.len = s_lens != nullptr ? s_lens[gr.s] : seq_len(a, gr.s);
   const int C = (a.g.nblk_prefix[gr.h + 1] - a.g.nblk_prefix[gr.h]) * a.pv.block_size;
   gr.rs = resident(gr.len, a.g.window[gr.h], C);
   gr.C16 = C >> 4;
@@ -109,16 +120,34 @@ __device__ __forceinline__ long long block_exclusive_scan(long long v, long long
   return base + x - v;
 }
 
+// Writes a merged (M, L, acc) of query head q, columns 4*d4 .. 4*d4 + 3: normalised to the bf16
+// output `out_grp` when it is non-null, else unnormalised to partial slot `dst_slot`.
+template <int D>
+__device__ __forceinline__ void store_merged(float M, float L, float4 acc, int q, int d4, int G,
+                                             __nv_bfloat16* out_grp, float* dst_acc, float* dst_ml,
+                                             long long dst_slot) {
+  if (out_grp != nullptr) {
+    const float inv = L > 0.f ? 1.f / L : 0.f;
+    __nv_bfloat162 lo = __floats2bfloat162_rn(acc.x * inv, acc.y * inv);
+    __nv_bfloat162 hi = __floats2bfloat162_rn(acc.z * inv, acc.w * inv);
+    uint2 packed;
+    packed.x = *reinterpret_cast<uint32_t*>(&lo);
+    packed.y = *reinterpret_cast<uint32_t*>(&hi);
+    *reinterpret_cast<uint2*>(out_grp + (int64_t)q * D + d4 * 4) = packed;
+  } else {
+    const long long slot = dst_slot * G + q;
+    reinterpret_cast<float4*>(dst_acc + slot * D)[d4] = acc;
+    if (d4 == 0) reinterpret_cast<float2*>(dst_ml)[slot] = make_float2(M, L);
+  }
+}
 // Folds `count` consecutive partial slots [first, first + count) of a partial buffer with the
 // online rule (running max M, weight sum L, accumulator rescaled by 2^(M_old - M_new)).  Each
 // thread owns 4 consecutive output columns of one query head and keeps 8 slots' loads in
-// flight.  The result goes to the normalised bf16 output `out_grp` when it is non-null, else
-// to partial slot `dst_slot` of (dst_acc, dst_ml).  `live(i)` tells whether slot first + i
-// holds a partial.
+// flight.  Output as store_merged.  `live(i)` tells whether slot first + i holds a partial.
 template <int D, typename Live>
-__device__ __forceinline__ void merge_slots(const float* src_acc, const float* src_ml, long long first, int count,
-                                            int G, Live live, __nv_bfloat16* out_grp, float* dst_acc, float* dst_ml,
-                                            long long dst_slot) {
+__device__ __forceinline__ void merge_slots_online(const float* src_acc, const float* src_ml, long long first,
+                                                   int count, int G, Live live, __nv_bfloat16* out_grp,
+                                                   float* dst_acc, float* dst_ml, long long dst_slot) {
   constexpr int kV = D / 4;  // float4 columns per query head
   constexpr int kBatch = 8;
   for (int e = threadIdx.x; e < G * kV; e += blockDim.x) {
@@ -153,36 +182,109 @@ __device__ __forceinline__ void merge_slots(const float* src_acc, const float* s
         M = Mn;
       }
     }
-    if (out_grp != nullptr) {
-      const float inv = L > 0.f ? 1.f / L : 0.f;
-      __nv_bfloat162 lo = __floats2bfloat162_rn(acc.x * inv, acc.y * inv);
-      __nv_bfloat162 hi = __floats2bfloat162_rn(acc.z * inv, acc.w * inv);
-      uint2 packed;
-      packed.x = *reinterpret_cast<uint32_t*>(&lo);
-      packed.y = *reinterpret_cast<uint32_t*>(&hi);
-      *reinterpret_cast<uint2*>(out_grp + (int64_t)q * D + d4 * 4) = packed;
-    } else {
-      const long long slot = dst_slot * G + q;
-      reinterpret_cast<float4*>(dst_acc + slot * D)[d4] = acc;
-      if (d4 == 0) reinterpret_cast<float2*>(dst_ml)[slot] = make_float2(M, L);
+    store_merged<D>(M, L, acc, q, d4, G, out_grp, dst_acc, dst_ml, dst_slot);
+  }
+}
+constexpr int kMergeMax = 64;          // most slots the shared-memory merge takes
+constexpr uint32_t kBulkChunk = 16384;  // bytes per bulk copy of a partial block
+
+// Shared-memory resources a merge may use: the stage buffers (free once the CTA has consumed
+// its last tile), an mbarrier for the bulk copy and the phase it is at.
+struct MergeStage {
+  float* buf;      // null: not available
+  uint32_t bytes;
+  uint64_t* bar;
+  uint32_t phase;  // completed uses of `bar` (uniform in the CTA)
+  int stuck;       // parity of a use whose wait timed out, else -1
+};
+
+// Folds `count` consecutive partial slots [first, first + count) into the output or partial
+// slot of store_merged.  When every slot holds a partial (`dense`), the stage buffers are free
+// and the accumulators fit, they are fetched in one bulk copy while the (m, l) of every
+// (slot, head) are read into `s_ml` (2 * count * G floats); the maxima M = max_i m_i and the
+// weights w_i = 2^(m_i - M) are formed once per (slot, head), and each thread sums
+// w_i * acc_i over its 4 columns of one query head out of shared memory, L = sum_i w_i * l_i.
+// The whole merge then waits for about one round trip to L2.  Otherwise the online merge is
+// used.  `live(i)` tells whether slot first + i holds a partial.
+template <int D, typename Live>
+__device__ __forceinline__ void merge_slots(const float* src_acc, const float* src_ml, long long first, int count,
+                                            int G, Live live, bool dense, __nv_bfloat16* out_grp, float* dst_acc,
+                                            float* dst_ml, long long dst_slot, float* s_ml, float* s_ML,
+                                            MergeStage& ms, int32_t* err) {
+  const uint32_t bytes = (uint32_t)count * (uint32_t)G * D * 4u;
+  if (!dense || ms.buf == nullptr || count > kMergeMax || bytes > ms.bytes) {
+    merge_slots_online<D>(src_acc, src_ml, first, count, G, live, out_grp, dst_acc, dst_ml, dst_slot);
+    return;
+  }
+  if (threadIdx.x == 0) {
+    // the partials were written and acquired, and the buffer last read, through the generic proxy
+    fence_proxy_async_all();
+    mbar_arrive_expect_tx(ms.bar, bytes);
+    const char* src = reinterpret_cast<const char*>(src_acc + first * G * D);
+    for (uint32_t off = 0; off < bytes; off += kBulkChunk)
+      bulk_load(smem_addr(ms.buf) + off, src + off, bytes - off < kBulkChunk ? bytes - off : kBulkChunk, ms.bar);
+  }
+  for (int p = threadIdx.x; p < count * G; p += blockDim.x) {
+    const float2 ml = __ldcg(reinterpret_cast<const float2*>(src_ml) + first * G + p);
+    s_ml[p] = ml.x;
+    s_ml[count * G + p] = ml.y;
+  }
+  __syncthreads();
+  if (threadIdx.x < G) {
+    const int q = threadIdx.x;
+    float M = kNegInf;
+    for (int i = 0; i < count; ++i) M = fmaxf(M, s_ml[i * G + q]);
+    float L = 0.f;
+    for (int i = 0; i < count; ++i) {
+      const float w = M == kNegInf ? 0.f : ex2(s_ml[i * G + q] - M);
+      s_ml[i * G + q] = w;
+      L = fmaf(s_ml[count * G + i * G + q], w, L);
     }
+    s_ML[q] = M;
+    s_ML[G + q] = L;
+  }
+  __syncthreads();
+  const bool landed = mbar_wait_bounded(ms.bar, ms.phase & 1u);
+  ++ms.phase;
+  if (!landed && threadIdx.x == 0) atomicOr(err, HWKV_DEVERR_WAIT_TIMEOUT);
+  constexpr int kV = D / 4;  // float4 columns per query head
+  const float4* sacc = reinterpret_cast<const float4*>(ms.buf);
+  for (int e = threadIdx.x; e < G * kV; e += blockDim.x) {
+    const int q = e / kV, d4 = e - (e / kV) * kV;
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (landed) {
+      for (int i = 0; i < count; ++i) {
+        const float w = s_ml[i * G + q];
+        const float4 v = sacc[(i * G + q) * kV + d4];
+        acc.x = fmaf(v.x, w, acc.x);
+        acc.y = fmaf(v.y, w, acc.y);
+        acc.z = fmaf(v.z, w, acc.z);
+        acc.w = fmaf(v.w, w, acc.w);
+      }
+    }
+    store_merged<D>(s_ML[q], s_ML[G + q], acc, q, d4, G, out_grp, dst_acc, dst_ml, dst_slot);
+  }
+  if (!landed) {  // a copy may still be in flight: no later merge reuses the buffer
+    ms.stuck = (int)((ms.phase - 1u) & 1u);
+    ms.buf = nullptr;
   }
 }
 
-// Bumps an arrival counter (thread 0) and tells the whole CTA whether it arrived last; the
-// last arriver resets the counter to 0 for the next launch.  Call after the CTA's partial is
-// written and fenced.
+// Bumps an arrival counter and tells the whole CTA whether it arrived last; the last arriver
+// resets the counter to 0 for the next launch.  Call after the CTA's partial is written (by any
+// of its threads): the barrier orders those writes before thread 0's atomic, whose release
+// half makes them visible device-wide before the count moves, and whose acquire half (with
+// the second barrier) lets the last arriver's threads read every other contributor's partial.
 __device__ __forceinline__ bool arrive_last(uint32_t* counter, int expected, int* s_flag) {
   __syncthreads();
   if (threadIdx.x == 0) {
-    const unsigned old = atomicAdd(counter, 1u);
+    unsigned old;
+    asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], 1;" : "=r"(old) : "l"(counter) : "memory");
     *s_flag = old + 1u == (unsigned)expected;
     if (*s_flag) *counter = 0u;
   }
   __syncthreads();
-  const bool last = *s_flag != 0;
-  if (last) __threadfence();
-  return last;
+  return *s_flag != 0;
 }
 
 template <int D, int GP, int NS>
@@ -202,9 +304,14 @@ __global__ void __launch_bounds__(kWarps * 32, 2) decode_sk_kernel(const __grid_
   float* sc_acc = reinterpret_cast<float*>(smem + W * NS * kStageBytes);  // [W][SG][D]
   __shared__ __align__(8) uint64_t bars[W * NS];
   __shared__ float sc_m[W * SG], sc_l[W * SG];
+  __shared__ float s_ML[2 * kMaxGroup];  // per-head maxima and weight sums of a partial merge
+  __shared__ __align__(8) uint64_t merge_bar;  // bulk copies of partial blocks
+  // the partial merge's (m, l) scratch reuses the warps' merge area
+  static_assert(2 * kMergeMax * GP <= W * SG * D, "partial-merge scratch exceeds the warp merge area");
   __shared__ long long s_scan[W];
   __shared__ long long s_start[2];
   __shared__ int s_last;
+  __shared__ int s_lens_buf[kLensCache];
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int H = a.pv.kv_heads;
@@ -229,20 +336,26 @@ __global__ void __launch_bounds__(kWarps * 32, 2) decode_sk_kernel(const __grid_
     for (int s = threadIdx.x; s < B; s += W * 32)
       if (__ldcg(a.lens + s) + a.len_add < 0) atomicOr(a.pv.err, HWKV_DEVERR_NEG_LENGTH);
   }
+  // the lengths are staged once, so crossing into the next group never waits on global memory
+  const int* s_lens = B <= kLensCache ? s_lens_buf : nullptr;
+  if (s_lens != nullptr) {
+    for (int s = threadIdx.x; s < B; s += W * 32) s_lens_buf[s] = seq_len(a, s);
+    __syncthreads();
+  }
 
   // ---- schedule: needed tiles per group, their prefix sums, this CTA's range ----------
   if (threadIdx.x == 0) s_start[0] = -1;
   const int per = (ngroups + W * 32 - 1) / (W * 32);
   const int g_lo = min(ngroups, (int)threadIdx.x * per), g_hi = min(ngroups, g_lo + per);
   long long mine = 0;
-  for (int g = g_lo; g < g_hi; ++g) mine += load_group(a, g).tiles;
+  for (int g = g_lo; g < g_hi; ++g) mine += load_group(a, s_lens, g).tiles;
   long long T;
   const long long excl = block_exclusive_scan<W>(mine, s_scan, T);
   const long long t_lo = range_start(T, cta, nctas), t_hi = range_start(T, cta + 1, nctas);
   if (t_lo < t_hi && excl <= t_lo && t_lo < excl + mine) {
     long long pre = excl;
     for (int g = g_lo; g < g_hi; ++g) {
-      const int c = load_group(a, g).tiles;
+      const int c = load_group(a, s_lens, g).tiles;
       if (t_lo < pre + c) {
         s_start[0] = g;
         s_start[1] = pre;
@@ -253,6 +366,7 @@ __global__ void __launch_bounds__(kWarps * 32, 2) decode_sk_kernel(const __grid_
   }
   if (threadIdx.x == 0) {
     for (int i = 0; i < W * NS; ++i) mbar_init(&bars[i], 1);
+    mbar_init(&merge_bar, 1);
     fence_mbar_init();
   }
   __syncthreads();
@@ -267,13 +381,13 @@ __global__ void __launch_bounds__(kWarps * 32, 2) decode_sk_kernel(const __grid_
 
   int ig = g_start;            // issue cursor: group, its first tile on the line, the group
   long long ipre = pre_start;
-  Group igr = load_group(a, ig);
+  Group igr = load_group(a, s_lens, ig);
   long long j_issue = t_lo + warp;
   int issued = 0;
   auto issue_next = [&](int issuer) {
     while (j_issue >= ipre + igr.tiles) {
       ipre += igr.tiles;
-      igr = load_group(a, ++ig);
+      igr = load_group(a, s_lens, ++ig);
     }
     if (lane == issuer) {
       const int st = issued % NS;
@@ -305,7 +419,7 @@ __global__ void __launch_bounds__(kWarps * 32, 2) decode_sk_kernel(const __grid_
   if (a.early) griddep_wait();
   // groups with nothing resident (length 0) get a zero output, each from one CTA
   for (int g = cta; g < ngroups; g += nctas) {
-    const Group gr = load_group(a, g);
+    const Group gr = load_group(a, s_lens, g);
     if (gr.tiles == 0)
       for (int e = threadIdx.x; e < G * D; e += W * 32)
         out[((int64_t)gr.s * Hq + gr.h * G + e / D) * D + e % D] = __float2bfloat16_rn(0.f);
@@ -323,11 +437,12 @@ __global__ void __launch_bounds__(kWarps * 32, 2) decode_sk_kernel(const __grid_
 
   int sg = g_start;            // segment cursor (uniform in the CTA)
   long long spre = pre_start;
-  Group sgr = load_group(a, sg);
+  Group sgr = load_group(a, s_lens, sg);
   long long j_cons = t_lo + warp;
   int consumed = 0;
   int drain_from = -1;         // set when a wait timed out
   bool patched_stage = false;  // a generic-proxy write went into the stage just released
+  MergeStage ms{nullptr, (uint32_t)(W * NS * kStageBytes), &merge_bar, 0u, -1};
 
   for (;;) {
     const long long seg_begin = t_lo > spre ? t_lo : spre;
@@ -533,11 +648,14 @@ __global__ void __launch_bounds__(kWarps * 32, 2) decode_sk_kernel(const __grid_
       // CTA of the group merges them all.  More (long windows at small batch): blocks of
       // kMergeBlock consecutive contributors are merged by their last arriver into a second-
       // level partial, and the last of those merges the blocks.
+      // After the last segment no copy is in flight (unless a wait timed out): merges may
+      // stage partial blocks in the stage buffers.
+      if (seg_end >= t_hi)
+        ms.buf = __syncthreads_or(drain_from >= 0) ? nullptr : reinterpret_cast<float*>(smem);
       const int c_lo = cta_of(spre, T, nctas), c_hi = cta_of(spre + sgr.tiles - 1, T, nctas);
       const bool all_live = T >= nctas;  // then no CTA range is empty
       const int k = c_hi - c_lo + 1;
       __nv_bfloat16* const out_grp = out + ((int64_t)sgr.s * Hq + sgr.h * G) * D;
-      __threadfence();
       if (!all_live || k <= kFlatMerge) {
         int expected = k;
         if (!all_live) {
@@ -548,7 +666,8 @@ __global__ void __launch_bounds__(kWarps * 32, 2) decode_sk_kernel(const __grid_
           auto live = [&](int i) {
             return all_live || range_start(T, c_lo + i + 1, nctas) > range_start(T, c_lo + i, nctas);
           };
-          merge_slots<D>(a.part_acc, a.part_ml, (long long)sg + c_lo, k, G, live, out_grp, nullptr, nullptr, 0);
+          merge_slots<D>(a.part_acc, a.part_ml, (long long)sg + c_lo, k, G, live, all_live, out_grp, nullptr,
+                         nullptr, 0, sc_acc, s_ML, ms, a.pv.err);
         }
       } else {
         auto live = [](int) { return true; };
@@ -558,12 +677,11 @@ __global__ void __launch_bounds__(kWarps * 32, 2) decode_sk_kernel(const __grid_
         const int b_n = min(kMergeBlock, c_hi - b_lo + 1);
         const long long slot2 = (long long)sg * a.merge_blocks + b;
         if (arrive_last(&a.counters1[slot2], b_n, &s_last)) {
-          merge_slots<D>(a.part_acc, a.part_ml, (long long)sg + b_lo, b_n, G, live, nullptr, a.part2_acc,
-                         a.part2_ml, slot2);
-          __threadfence();
+          merge_slots<D>(a.part_acc, a.part_ml, (long long)sg + b_lo, b_n, G, live, true, nullptr, a.part2_acc,
+                         a.part2_ml, slot2, sc_acc, s_ML, ms, a.pv.err);
           if (arrive_last(&a.counters[sg], nb, &s_last))
-            merge_slots<D>(a.part2_acc, a.part2_ml, (long long)sg * a.merge_blocks, nb, G, live, out_grp, nullptr,
-                           nullptr, 0);
+            merge_slots<D>(a.part2_acc, a.part2_ml, (long long)sg * a.merge_blocks, nb, G, live, true, out_grp,
+                           nullptr, nullptr, 0, sc_acc, s_ML, ms, a.pv.err);
         }
       }
     }
@@ -571,7 +689,7 @@ __global__ void __launch_bounds__(kWarps * 32, 2) decode_sk_kernel(const __grid_
     if (seg_end >= t_hi) break;
     do {
       spre += sgr.tiles;
-      sgr = load_group(a, ++sg);
+      sgr = load_group(a, s_lens, ++sg);
     } while (sgr.tiles == 0);
   }
 
@@ -580,6 +698,7 @@ __global__ void __launch_bounds__(kWarps * 32, 2) decode_sk_kernel(const __grid_
     for (int c = drain_from; c < issued; ++c)
       if (!mbar_wait_bounded(&wbar[c % NS], (uint32_t)(c / NS) & 1u)) break;
   }
+  if (ms.stuck >= 0) mbar_wait_bounded(&merge_bar, (uint32_t)ms.stuck);
 }
 
 template <int D, int GP, int NS>
