@@ -36,8 +36,8 @@ FALLBACK_HBM_GBS = 6800.0
 # dram__bytes_read.sum + dram__bytes_write.sum per decode launch from one ncu capture of
 # the tensor-core decode kernel, with the sha256 of hwkv_decode_tc.cu it was taken on.  When
 # the kernel source changes the figure no longer applies and is reported as null.
-DECODE_TRAFFIC = {"source_sha256": "9fabd4485475a464623225c16a523e7a943b2701658ce689121c1f39e1629bc0",
-                  "bytes_per_launch": (621.200384 + 2.865664 + 489.036800 + 0.393472) / 2 * 1e6,
+DECODE_TRAFFIC = {"source_sha256": "17c949f0b84021866ce46ea77cb1aab01d05c9a891c1392a2f48258c5cdb46a5",
+                  "bytes_per_launch": (621.199104 + 3.200000 + 489.070592 + 0.174848) / 2 * 1e6,
                   "launch": "layers 0 and 1 of the full workload (2-layer run, same per-launch shape)"}
 
 

@@ -77,6 +77,14 @@ __device__ __forceinline__ Group load_group(const DecodeArgs& a, const int* s_le
   return gr;
 }
 
+// Line positions charged for each group's boundary.  A group with tiles spans kGapTiles
+// positions that hold no tile, then its tiles; a CTA whose range takes in a group's start thus
+// streams kGapTiles fewer tiles, which pays for what a boundary costs it (the warps' merge,
+// publishing a partial, the next group's q), so CTAs with boundaries do not end last.
+constexpr int kGapTiles = 24;
+
+__device__ __forceinline__ int group_span(const Group& gr) { return gr.tiles > 0 ? gr.tiles + kGapTiles : 0; }
+
 // ring slot of the first token of the i-th needed tile of a group
 __device__ __forceinline__ int tile_slot(const Group& gr, long long i) {
   int t = gr.t_first + (int)i;
@@ -348,14 +356,14 @@ __global__ void __launch_bounds__(kWarps * 32, 2) decode_sk_kernel(const __grid_
   const int per = (ngroups + W * 32 - 1) / (W * 32);
   const int g_lo = min(ngroups, (int)threadIdx.x * per), g_hi = min(ngroups, g_lo + per);
   long long mine = 0;
-  for (int g = g_lo; g < g_hi; ++g) mine += load_group(a, s_lens, g).tiles;
+  for (int g = g_lo; g < g_hi; ++g) mine += group_span(load_group(a, s_lens, g));
   long long T;
   const long long excl = block_exclusive_scan<W>(mine, s_scan, T);
   const long long t_lo = range_start(T, cta, nctas), t_hi = range_start(T, cta + 1, nctas);
   if (t_lo < t_hi && excl <= t_lo && t_lo < excl + mine) {
     long long pre = excl;
     for (int g = g_lo; g < g_hi; ++g) {
-      const int c = load_group(a, s_lens, g).tiles;
+      const int c = group_span(load_group(a, s_lens, g));
       if (t_lo < pre + c) {
         s_start[0] = g;
         s_start[1] = pre;
@@ -370,7 +378,9 @@ __global__ void __launch_bounds__(kWarps * 32, 2) decode_sk_kernel(const __grid_
     fence_mbar_init();
   }
   __syncthreads();
-  const bool has_range = t_lo < t_hi && s_start[0] >= 0;
+  // the range holds a tile unless it lies within one group's gap
+  const bool has_range =
+      t_lo < t_hi && s_start[0] >= 0 && t_hi > (t_lo > s_start[1] + kGapTiles ? t_lo : s_start[1] + kGapTiles);
   const int g_start = has_range ? (int)s_start[0] : 0;
   const long long pre_start = has_range ? s_start[1] : 0;
 
@@ -385,13 +395,22 @@ __global__ void __launch_bounds__(kWarps * 32, 2) decode_sk_kernel(const __grid_
   long long j_issue = t_lo + warp;
   int issued = 0;
   auto issue_next = [&](int issuer) {
-    while (j_issue >= ipre + igr.tiles) {
-      ipre += igr.tiles;
-      igr = load_group(a, s_lens, ++ig);
+    // this warp's next position that holds a tile: past a group's end go to the next group,
+    // within its gap step on; nothing is issued once the range is done
+    for (;;) {
+      if (j_issue >= t_hi) return;
+      if (j_issue >= ipre + group_span(igr)) {
+        ipre += group_span(igr);
+        igr = load_group(a, s_lens, ++ig);
+      } else if (j_issue < ipre + kGapTiles) {
+        j_issue += W;
+      } else {
+        break;
+      }
     }
     if (lane == issuer) {
       const int st = issued % NS;
-      const int t0 = tile_slot(igr, j_issue - ipre);
+      const int t0 = tile_slot(igr, j_issue - ipre - kGapTiles);
       const int jb = t0 / bs;
       const int r0 = t0 - jb * bs;
       // the first stages may be issued before the dependent-launch wait: read through L2
@@ -445,8 +464,12 @@ __global__ void __launch_bounds__(kWarps * 32, 2) decode_sk_kernel(const __grid_
   MergeStage ms{nullptr, (uint32_t)(W * NS * kStageBytes), &merge_bar, 0u, -1};
 
   for (;;) {
-    const long long seg_begin = t_lo > spre ? t_lo : spre;
-    const long long seg_end = t_hi < spre + sgr.tiles ? t_hi : spre + sgr.tiles;
+    // the segment: the group's tiles within the range
+    const long long seg_begin = t_lo > spre + kGapTiles ? t_lo : spre + kGapTiles;
+    const long long seg_end = t_hi < spre + group_span(sgr) ? t_hi : spre + group_span(sgr);
+    // another segment follows when the next group's first tile is within the range
+    const bool more = spre + group_span(sgr) + kGapTiles < t_hi;
+    while (j_cons < seg_begin) j_cons += W;  // over the group's gap
 
     // Q of this group as the B operand of S = K . Q^T: in n-tile nt the lane holds
     // q[g][16i + 2*q4 + {0,1}] and the same +8, g = 8*nt + lane/4; heads g >= G are zero.
@@ -482,7 +505,7 @@ __global__ void __launch_bounds__(kWarps * 32, 2) decode_sk_kernel(const __grid_
       if (drain_from < 0) {
         const uint32_t sK = wstage + st * kStageBytes;
         const uint32_t sV = sK + kTileBytes;
-        const int t0 = tile_slot(sgr, j_cons - spre);
+        const int t0 = tile_slot(sgr, j_cons - spre - kGapTiles);
 
         // fused append: the new token's rows replace the tile's copy of its slot and go to
         // the pool (no other CTA reads this tile in this launch)
@@ -582,7 +605,7 @@ __global__ void __launch_bounds__(kWarps * 32, 2) decode_sk_kernel(const __grid_
     }
 
     // ---- end of segment: merge the warps, then store output or partial -----------------
-    if (seg_end >= t_hi) griddep_launch_dependents();  // this CTA reads no more tiles
+    if (!more) griddep_launch_dependents();  // this CTA reads no more tiles
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
@@ -590,7 +613,7 @@ __global__ void __launch_bounds__(kWarps * 32, 2) decode_sk_kernel(const __grid_
         ls[nt][0] += __shfl_xor_sync(0xffffffffu, ls[nt][0], off);
         ls[nt][1] += __shfl_xor_sync(0xffffffffu, ls[nt][1], off);
       }
-    const bool whole = seg_begin == spre && seg_end == spre + sgr.tiles;
+    const bool whole = seg_begin == spre + kGapTiles && seg_end == spre + group_span(sgr);
     const long long slot = (long long)sg + cta;  // unique per (group, CTA) along the line
     // one pass per n-tile: the warps' states of query heads [8*nt, 8*nt + SG) meet in shared
     // memory and are folded into the output or this CTA's partial
@@ -650,9 +673,8 @@ __global__ void __launch_bounds__(kWarps * 32, 2) decode_sk_kernel(const __grid_
       // level partial, and the last of those merges the blocks.
       // After the last segment no copy is in flight (unless a wait timed out): merges may
       // stage partial blocks in the stage buffers.
-      if (seg_end >= t_hi)
-        ms.buf = __syncthreads_or(drain_from >= 0) ? nullptr : reinterpret_cast<float*>(smem);
-      const int c_lo = cta_of(spre, T, nctas), c_hi = cta_of(spre + sgr.tiles - 1, T, nctas);
+      if (!more) ms.buf = __syncthreads_or(drain_from >= 0) ? nullptr : reinterpret_cast<float*>(smem);
+      const int c_lo = cta_of(spre + kGapTiles, T, nctas), c_hi = cta_of(spre + group_span(sgr) - 1, T, nctas);
       const bool all_live = T >= nctas;  // then no CTA range is empty
       const int k = c_hi - c_lo + 1;
       __nv_bfloat16* const out_grp = out + ((int64_t)sgr.s * Hq + sgr.h * G) * D;
@@ -686,9 +708,9 @@ __global__ void __launch_bounds__(kWarps * 32, 2) decode_sk_kernel(const __grid_
       }
     }
     __syncthreads();  // the merge scratch is rewritten by the next segment
-    if (seg_end >= t_hi) break;
+    if (!more) break;
     do {
-      spre += sgr.tiles;
+      spre += group_span(sgr);
       sgr = load_group(a, s_lens, ++sg);
     } while (sgr.tiles == 0);
   }
