@@ -9,7 +9,7 @@
 namespace hwkv {
 
 constexpr int kMaxKvHeads = 32;
-constexpr int kMergeBlock = 16;  // CTAs whose partials one first-level merge folds
+constexpr int kMergeBlock = 8;   // CTAs whose partials one first-level merge folds
 constexpr int kMaxGroup = 16;  // query heads per KV head (GQA group)
 constexpr int kGroupPads = 3;   // tensor-core decode instances: 4, 8 or 16 query-head columns
 
