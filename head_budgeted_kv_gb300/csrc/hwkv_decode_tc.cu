@@ -83,6 +83,13 @@ __device__ __forceinline__ Group load_group(const DecodeArgs& a, const int* s_le
 // publishing a partial, the next group's q), so CTAs with boundaries do not end last.
 constexpr int kGapTiles = 24;
 
+// Tiles per warp pulled into L2 while the CTA waits for the preceding grid (early reads only),
+// when its range holds at least kL2PrefetchMin positions.  Short ranges (small batches) skip it:
+// there the preceding grid's last streams and merges, which the prefetch would slow, are most of
+// what the wait is for.
+constexpr int kL2Prefetch = 2;
+constexpr int kL2PrefetchMin = 64;
+
 __device__ __forceinline__ int group_span(const Group& gr) { return gr.tiles > 0 ? gr.tiles + kGapTiles : 0; }
 
 // ring slot of the first token of the i-th needed tile of a group
@@ -435,6 +442,31 @@ __global__ void __launch_bounds__(kWarps * 32, 2) decode_sk_kernel(const __grid_
   // the first stages are issued by different lanes so their table lookups overlap
   if (has_range)
     for (int i = 0; i < NS && j_issue < t_hi; ++i) issue_next(i);
+  if (a.early && has_range && lane < kL2Prefetch && t_hi - t_lo >= kL2PrefetchMin) {
+    // Until the wait below ends, the preceding grid only merges and completes and the memory
+    // system is nearly idle: pull the tiles this warp takes after its staged ones into L2
+    // (lane i: the position i steps on; a position inside a gap is skipped).
+    const long long p = j_issue + (long long)lane * W;
+    if (p < t_hi) {
+      int g = ig;
+      long long pre = ipre;
+      Group gr = igr;
+      while (p >= pre + group_span(gr)) {
+        pre += group_span(gr);
+        gr = load_group(a, s_lens, ++g);
+      }
+      if (p >= pre + kGapTiles) {
+        const int t0 = tile_slot(gr, p - pre - kGapTiles);
+        const int jb = t0 / bs;
+        const int32_t blk = __ldcg(gr.tbl + jb);
+        if (blk >= 0 && (int64_t)blk < a.pv.total_blocks) {
+          const char* rows = static_cast<const char*>(a.pv.pool) + ((int64_t)blk * 2 * bs + (t0 - jb * bs)) * D * 2;
+          prefetch_l2_bulk(rows, kTileBytes);                       // K rows of the tile
+          prefetch_l2_bulk(rows + (int64_t)bs * D * 2, kTileBytes);  // V rows
+        }
+      }
+    }
+  }
   if (a.early) griddep_wait();
   // groups with nothing resident (length 0) get a zero output, each from one CTA
   for (int g = cta; g < ngroups; g += nctas) {
