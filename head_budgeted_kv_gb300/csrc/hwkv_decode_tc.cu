@@ -155,19 +155,33 @@ __device__ __forceinline__ void store_merged(float M, float L, float4 acc, int q
     if (d4 == 0) reinterpret_cast<float2*>(dst_ml)[slot] = make_float2(M, L);
   }
 }
-// Folds `count` consecutive partial slots [first, first + count) of a partial buffer with the
-// online rule (running max M, weight sum L, accumulator rescaled by 2^(M_old - M_new)).  Each
-// thread owns 4 consecutive output columns of one query head and keeps 8 slots' loads in
-// flight.  Output as store_merged.  `live(i)` tells whether slot first + i holds a partial.
+// Folds `count` consecutive partial slots [first, first + count) of a partial buffer out of
+// registers, with exactly the arithmetic of the shared-memory merge below: first the maximum
+// M = max_i m_i, then, slot after slot, w_i = 2^(m_i - M), L = fma(l_i, w_i, L) and
+// acc = fma(acc_i, w_i, acc).  Whichever path a group's last arriver takes, the output is the
+// same bit for bit.  Each thread owns 4 consecutive output columns of one query head and keeps
+// 8 slots' loads in flight.  Output as store_merged.  `live(i)` tells whether slot first + i
+// holds a partial.
 template <int D, typename Live>
-__device__ __forceinline__ void merge_slots_online(const float* src_acc, const float* src_ml, long long first,
-                                                   int count, int G, Live live, __nv_bfloat16* out_grp,
-                                                   float* dst_acc, float* dst_ml, long long dst_slot) {
+__device__ __forceinline__ void merge_slots_regs(const float* src_acc, const float* src_ml, long long first,
+                                                 int count, int G, Live live, __nv_bfloat16* out_grp,
+                                                 float* dst_acc, float* dst_ml, long long dst_slot) {
   constexpr int kV = D / 4;  // float4 columns per query head
   constexpr int kBatch = 8;
   for (int e = threadIdx.x; e < G * kV; e += blockDim.x) {
     const int q = e / kV, d4 = e - (e / kV) * kV;
-    float M = kNegInf, L = 0.f;
+    float M = kNegInf;
+    for (int i0 = 0; i0 < count; i0 += kBatch) {
+      float m[kBatch];
+#pragma unroll
+      for (int j = 0; j < kBatch; ++j) {
+        const int i = i0 + j;
+        m[j] = i < count && live(i) ? __ldcg(src_ml + ((first + i) * G + q) * 2) : kNegInf;
+      }
+#pragma unroll
+      for (int j = 0; j < kBatch; ++j) M = fmaxf(M, m[j]);
+    }
+    float L = 0.f;
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
     for (int i0 = 0; i0 < count; i0 += kBatch) {
       float2 ml[kBatch];
@@ -186,15 +200,14 @@ __device__ __forceinline__ void merge_slots_online(const float* src_acc, const f
       }
 #pragma unroll
       for (int j = 0; j < kBatch; ++j) {
-        const float Mn = fmaxf(M, ml[j].x);
-        if (Mn == kNegInf) continue;
-        const float fo = ex2(M - Mn), fn = ex2(ml[j].x - Mn);
-        L = fmaf(L, fo, ml[j].y * fn);
-        acc.x = fmaf(acc.x, fo, v[j].x * fn);
-        acc.y = fmaf(acc.y, fo, v[j].y * fn);
-        acc.z = fmaf(acc.z, fo, v[j].z * fn);
-        acc.w = fmaf(acc.w, fo, v[j].w * fn);
-        M = Mn;
+        if (i0 + j < count && live(i0 + j)) {
+          const float w = M == kNegInf ? 0.f : ex2(ml[j].x - M);
+          L = fmaf(ml[j].y, w, L);
+          acc.x = fmaf(v[j].x, w, acc.x);
+          acc.y = fmaf(v[j].y, w, acc.y);
+          acc.z = fmaf(v[j].z, w, acc.z);
+          acc.w = fmaf(v[j].w, w, acc.w);
+        }
       }
     }
     store_merged<D>(M, L, acc, q, d4, G, out_grp, dst_acc, dst_ml, dst_slot);
@@ -219,8 +232,8 @@ struct MergeStage {
 // (slot, head) are read into `s_ml` (2 * count * G floats); the maxima M = max_i m_i and the
 // weights w_i = 2^(m_i - M) are formed once per (slot, head), and each thread sums
 // w_i * acc_i over its 4 columns of one query head out of shared memory, L = sum_i w_i * l_i.
-// The whole merge then waits for about one round trip to L2.  Otherwise the online merge is
-// used.  `live(i)` tells whether slot first + i holds a partial.
+// The whole merge then waits for about one round trip to L2.  Otherwise the register merge
+// above runs, with the same arithmetic.  `live(i)` tells whether slot first + i holds a partial.
 template <int D, typename Live>
 __device__ __forceinline__ void merge_slots(const float* src_acc, const float* src_ml, long long first, int count,
                                             int G, Live live, bool dense, __nv_bfloat16* out_grp, float* dst_acc,
@@ -228,7 +241,7 @@ __device__ __forceinline__ void merge_slots(const float* src_acc, const float* s
                                             MergeStage& ms, int32_t* err) {
   const uint32_t bytes = (uint32_t)count * (uint32_t)G * D * 4u;
   if (!dense || ms.buf == nullptr || count > kMergeMax || bytes > ms.bytes) {
-    merge_slots_online<D>(src_acc, src_ml, first, count, G, live, out_grp, dst_acc, dst_ml, dst_slot);
+    merge_slots_regs<D>(src_acc, src_ml, first, count, G, live, out_grp, dst_acc, dst_ml, dst_slot);
     return;
   }
   if (threadIdx.x == 0) {

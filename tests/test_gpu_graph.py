@@ -51,12 +51,25 @@ def test_graph_replay_equals_eager(fused, kernel):
     graphed.close()
 
 
-def test_early_reads_equal_default_bit_for_bit():
+EARLY_CASES = {
+    # about one tile per CTA: single segments, merges of contributors with empty ranges
+    "small": dict(name="early", cfg_id=96, layers=3, kv_heads=2, windows=((4096, 64), (256, 1024), (32, 2048)),
+                  prefill=(3000, 700, 90), steps=4),
+    # ~100 line positions per CTA: boundary segments, bulk-copy and two-level merges, and the
+    # L2 prefetch before the dependent-launch wait
+    "long_ranges": dict(name="early_long", cfg_id=97, layers=2, kv_heads=4, windows=((65536, 65536, 65536, 65536),
+                                                                                    (16384, 65536, 65536, 1024)),
+                        prefill=(70000, 66000), steps=3),
+}
+
+
+@pytest.mark.parametrize("case", sorted(EARLY_CASES))
+def test_early_reads_equal_default_bit_for_bit(case):
     """Chained fused launches with HWKV_DECODE_EARLY_READS (positions prepared up front, no
     synchronisation between launches, so each schedule may start while the previous launch
-    finishes) give the same outputs and rings as the default launches."""
-    cfg = small_config(name="early", cfg_id=96, layers=3, kv_heads=2, windows=((4096, 64), (256, 1024), (32, 2048)),
-                       prefill=(3000, 700, 90), steps=4)
+    finishes) give the same outputs and rings as the default launches.  Which CTA merges a
+    group depends on timing; the outputs must not."""
+    cfg = small_config(**EARLY_CASES[case])
     results = []
     for early in (False, True):
         run = Run(cfg, fused=True)
