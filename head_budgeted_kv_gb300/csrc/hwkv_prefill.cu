@@ -519,8 +519,6 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_kernel(const __grid_con
     const int tok = qa + x * QT + r / G;
     const bool live = r < QT * G && tok < n;
     const int pq = p0 + tok;
-    const int t_first = qa + x * QT, t_last = min(n, qa + (x + 1) * QT) - 1;  // live tokens of the tile
-    const int pq_lo = p0 + t_first, pq_hi = p0 + t_last;
     const uint32_t lane_base = tmem + ((uint32_t)(quarter * 32) << 16);
     const uint32_t colO = Cfg::kColO + x * D;
     const float sl2 = a.scale_log2;
@@ -530,6 +528,10 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_kernel(const __grid_con
     const float masked = pos_scale ? kNegInf : -kNegInf;
     float m_ref = kNegInf, l = 0.f;
     bool ok = true;
+    // clean-stage bits of stages [32 * k, 32 * k + 32), read once per 32 stages: a shared-memory
+    // load waits behind the tensor cores' operand reads (hundreds of cycles while an S product
+    // runs), so it is kept off the per-stage path
+    uint32_t clean_word = 0u;
     for (int jj = 0; jj < nloc; ++jj) {
       const int j = j0 + jj;  // stage of the stream; jj counts this CTA's stages (barrier phases)
       const int b = jj & 1;
@@ -539,9 +541,11 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_kernel(const __grid_con
       float sv[kPfKeys];
       tmem_ld64(lane_base + (2 * x + b) * kPfKeys, sv);
 
-      // a "clean" stage needs no mask for any live row (precomputed by warp 3)
-      const bool clean =
-          jj < 32 * kCleanWords && ((reinterpret_cast<volatile uint32_t*>(s_clean[x])[jj >> 5] >> (jj & 31)) & 1u);
+      // a "clean" stage needs no mask for any live row (precomputed by warp 3; a bit it has not
+      // set yet only costs the masked path, which is exact for any stage)
+      if ((jj & 31) == 0)
+        clean_word = jj < 32 * kCleanWords ? reinterpret_cast<volatile uint32_t*>(s_clean[x])[jj >> 5] : 0u;
+      const bool clean = (clean_word >> (jj & 31)) & 1u;
       if (!clean) {
         PfKeyTile kt[kPfSub];
 #pragma unroll
