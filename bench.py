@@ -36,8 +36,8 @@ FALLBACK_HBM_GBS = 6800.0
 # dram__bytes_read.sum + dram__bytes_write.sum per decode launch from one ncu capture of
 # the tensor-core decode kernel, with the sha256 of hwkv_decode_tc.cu it was taken on.  When
 # the kernel source changes the figure no longer applies and is reported as null.
-DECODE_TRAFFIC = {"source_sha256": "4b7f650d3f57926997ea540da23b953e660270fdc3402c6f080e3b0b1a81fb2d",
-                  "bytes_per_launch": (621.264896 + 3.133696 + 489.026048 + 0.091136) / 2 * 1e6,
+DECODE_TRAFFIC = {"source_sha256": "aae7baccddf24e17c03b18b78b18b2467be752f2c8575b2e4b84ce5a30819750",
+                  "bytes_per_launch": (621.199616 + 2.799616 + 489.044480 + 0.113664) / 2 * 1e6,
                   "launch": "layers 0 and 1 of the full workload (2-layer run, same per-launch shape)"}
 
 
