@@ -315,6 +315,14 @@ __device__ __forceinline__ bool arrive_last(uint32_t* counter, int expected, int
   return *s_flag != 0;
 }
 
+// Query heads whose warp states meet in shared memory per merge pass: a whole 8-column n-tile,
+// except at head_dim 128 with 8 or 16 columns, where passes of 4 keep the scratch at 8 KB so two
+// CTAs fit an SM.
+template <int D, int GP>
+__host__ __device__ constexpr int merge_heads() {
+  return GP < 8 ? GP : (D == 128 ? 4 : 8);
+}
+
 template <int D, int GP, int NS>
 __global__ void __launch_bounds__(kWarps * 32, 2) decode_sk_kernel(const __grid_constant__ CUtensorMap tmap,
                                                                 const __grid_constant__ DecodeArgs a) {
@@ -325,7 +333,8 @@ __global__ void __launch_bounds__(kWarps * 32, 2) decode_sk_kernel(const __grid_
   constexpr int kSteps = D / 16;               // k-steps of QK, m-tiles of PV
   constexpr int kRowVecs = D * 2 / 16;         // 16-byte vectors per row
   constexpr int NT = (GP + 7) / 8;             // 8-column n-tiles of query heads
-  constexpr int SG = GP < 8 ? GP : 8;          // query heads merged per pass in shared memory
+  constexpr int SG = merge_heads<D, GP>();      // query heads merged per pass in shared memory
+  constexpr int kPasses = GP < 8 ? 1 : 8 / SG;  // passes per 8-column n-tile
 
   extern __shared__ uint8_t smem_dyn[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_dyn) + 1023) & ~uintptr_t(1023));
@@ -660,30 +669,33 @@ __global__ void __launch_bounds__(kWarps * 32, 2) decode_sk_kernel(const __grid_
       }
     const bool whole = seg_begin == spre + kGapTiles && seg_end == spre + group_span(sgr);
     const long long slot = (long long)sg + cta;  // unique per (group, CTA) along the line
-    // one pass per n-tile: the warps' states of query heads [8*nt, 8*nt + SG) meet in shared
-    // memory and are folded into the output or this CTA's partial
+    // pass (nt, hh): the warps' states of query heads [8*nt + hh*SG, 8*nt + (hh+1)*SG) meet in
+    // shared memory and are folded into the output or this CTA's partial
 #pragma unroll
-    for (int nt = 0; nt < NT; ++nt) {
-      if (nt > 0) __syncthreads();  // the previous pass has read the scratch
-      if (2 * q4 < SG) {
+    for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+    for (int hh = 0; hh < kPasses; ++hh) {
+      if (nt > 0 || hh > 0) __syncthreads();  // the previous pass has read the scratch
+      const int c0 = 2 * q4 - hh * SG;  // this lane's first column within the pass
+      if (c0 >= 0 && c0 < SG) {
         if (gq == 0) {
-          sc_m[warp * SG + 2 * q4] = mx[nt][0];
-          sc_m[warp * SG + 2 * q4 + 1] = mx[nt][1];
-          sc_l[warp * SG + 2 * q4] = ls[nt][0];
-          sc_l[warp * SG + 2 * q4 + 1] = ls[nt][1];
+          sc_m[warp * SG + c0] = mx[nt][0];
+          sc_m[warp * SG + c0 + 1] = mx[nt][1];
+          sc_l[warp * SG + c0] = ls[nt][0];
+          sc_l[warp * SG + c0 + 1] = ls[nt][1];
         }
         float* wacc = sc_acc + warp * SG * D;
 #pragma unroll
         for (int j = 0; j < kSteps; ++j) {
           const int d = 16 * j + gq;
-          wacc[(2 * q4) * D + d] = acc[j][nt][0];
-          wacc[(2 * q4 + 1) * D + d] = acc[j][nt][1];
-          wacc[(2 * q4) * D + d + 8] = acc[j][nt][2];
-          wacc[(2 * q4 + 1) * D + d + 8] = acc[j][nt][3];
+          wacc[c0 * D + d] = acc[j][nt][0];
+          wacc[(c0 + 1) * D + d] = acc[j][nt][1];
+          wacc[c0 * D + d + 8] = acc[j][nt][2];
+          wacc[(c0 + 1) * D + d + 8] = acc[j][nt][3];
         }
       }
       __syncthreads();
-      const int g0 = 8 * nt;
+      const int g0 = 8 * nt + hh * SG;
       const int ng = min(SG, G - g0);  // real query heads of this pass
       for (int e = threadIdx.x; e < ng * D; e += W * 32) {
         const int gl = e / D, d = e - (e / D) * D;
@@ -770,8 +782,8 @@ __global__ void __launch_bounds__(kWarps * 32, 2) decode_sk_kernel(const __grid_
 
 template <int D, int GP, int NS>
 constexpr int sk_smem_bytes() {
-  // stages + merge scratch (at most 8 query heads per pass) + align slack
-  return kWarps * NS * (2 * kTile * D * 2) + kWarps * (GP < 8 ? GP : 8) * D * 4 + 1024;
+  // stages + merge scratch (merge_heads query heads per pass) + align slack
+  return kWarps * NS * (2 * kTile * D * 2) + kWarps * merge_heads<D, GP>() * D * 4 + 1024;
 }
 
 // pipeline depth: 3 (head_dim 128) or 6 (head_dim 64) stages of 16 tokens per warp
