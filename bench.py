@@ -580,6 +580,35 @@ def prefill_flops(cfg, layer: int, pos0, n: int) -> int:
     return total
 
 
+def prefill_oracle_sample(cfg, wl, n_chunk: int, budget_s: float):
+    """Times the fp64 oracle's chunked prefill on the first tokens of sequence 0's chunk in
+    layer 0 (each token attends to its full window: the prior context and the chunk rows before
+    it) until ``budget_s`` seconds are spent.  Returns (seconds, tokens, threads)."""
+    import numpy as np
+    import oracle
+    import workloads
+    threads = oracle.default_threads()
+    l, s = 0, 0
+    p0 = cfg.prefill[s]
+    k, v = wl.prefill_seq(l, s, "cpu")
+    q, kc, vc = wl.chunk_inputs(l, 0, n_chunk, "cpu")
+    spent, done, batch = 0.0, 0, 8
+    while spent < budget_s and done < n_chunk:
+        m = min(batch, n_chunk - done)
+        hist = {}
+        for h in range(cfg.kv_heads):
+            lo = max(0, p0 + done + 1 - int(cfg.windows[l][h]))
+            hk = np.concatenate([workloads.to_raw(k[h, min(lo, p0):p0]), workloads.to_raw(kc[s, :done + m, h])])
+            hv = np.concatenate([workloads.to_raw(v[h, min(lo, p0):p0]), workloads.to_raw(vc[s, :done + m, h])])
+            hist[h] = (min(lo, p0), hk, hv)
+        qs = workloads.to_raw(q[s, done:done + m])
+        t0 = time.perf_counter()
+        oracle.prefill_attention(qs, hist, p0 + done, cfg.windows[l], cfg.scale, threads=threads)
+        spent += time.perf_counter() - t0
+        done += m
+    return spent, done, threads
+
+
 def run_prefill(args, cfg):
     import torch
     import workloads
@@ -602,13 +631,22 @@ def run_prefill(args, cfg):
     nt = torch.full((cfg.batch,), n, dtype=torch.int32, device=dev)
     chunks = [wl.chunk_inputs(l, 0, n, dev) for l in range(cfg.layers)]
     outs = [torch.empty_like(c[0]) for c in chunks]
+    # a pass over every layer per step: warm-up, timed, then end-to-end steps (positions keep
+    # advancing by one chunk per step)
     total = args.warmup + args.steps
-    pos = [(prefill + i * n).contiguous() for i in range(total)]
+    pos = [(prefill + i * n).contiguous() for i in range(total + args.steps)]
     torch.cuda.synchronize()
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
-    ms, flops = 0.0, 0
+    clocks = ClockSampler(local)
+    if rank == 0:
+        clocks.start()
+    ms, flops, launches = 0.0, 0, 0
     for i in range(total):
         k = i - args.warmup
+        if k == 0:
+            torch.cuda.synchronize()
+            clocks.mark_start()
+            launches0 = hw.binding.hwkv_kernel_launches()
         if k >= 0:
             ev[k][0].record(stream)
         for l in range(cfg.layers):
@@ -619,11 +657,69 @@ def run_prefill(args, cfg):
             flops += sum(prefill_flops(cfg, l, [cfg.prefill[s] + i * n for s in range(cfg.batch)], n)
                          for l in range(cfg.layers))
     torch.cuda.synchronize()
+    clocks.mark_end()
+    launches = hw.binding.hwkv_kernel_launches() - launches0
+    clock_info = clocks.stop() if rank == 0 else None
     for a, b in ev:
         ms += a.elapsed_time(b)
     bits = pool.check_device_errors()
     if bits:
         raise RuntimeError(f"device error bits {bits:#x}")
+
+    # ---- e2e: every step's chunk inputs from pinned host memory, its outputs back; two device
+    # sets, so step k + 1's inputs arrive and step k's outputs leave while the other computes ----
+    h_in = [[t.cpu().pin_memory() for t in chunks[l]] for l in range(cfg.layers)]
+    h_pos = [pos[total + k].cpu().pin_memory() for k in range(args.steps)]
+    h_out = [torch.empty(outs[l].shape, dtype=outs[l].dtype).pin_memory() for l in range(cfg.layers)]
+    d_in = [[[torch.empty_like(t) for t in chunks[l]] for l in range(cfg.layers)] for _ in range(2)]
+    d_pos = [torch.empty_like(prefill) for _ in range(2)]
+    d_out = [outs, [torch.empty_like(o) for o in outs]]
+    cs = torch.cuda.Stream(device=dev)
+    ev_in = [torch.cuda.Event() for _ in range(2)]
+    ev_done = [torch.cuda.Event() for _ in range(2)]
+    ev_out = [torch.cuda.Event() for _ in range(2)]
+    h2d = sum(t.numel() * t.element_size() for row in h_in for t in row) + cfg.batch * 4
+    d2h = sum(o.numel() * o.element_size() for o in h_out)
+
+    def send_inputs(k):
+        b = k % 2
+        with torch.cuda.stream(cs):
+            if k >= 2:
+                cs.wait_event(ev_done[b])
+            for l in range(cfg.layers):
+                for dst, src in zip(d_in[b][l], h_in[l]):
+                    dst.copy_(src, non_blocking=True)
+            d_pos[b].copy_(h_pos[k], non_blocking=True)
+            ev_in[b].record(cs)
+
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    cs.wait_event(e0)  # every copy lies inside the timed region
+    send_inputs(0)
+    for k in range(args.steps):
+        b = k % 2
+        if k + 1 < args.steps:
+            send_inputs(k + 1)
+        stream.wait_event(ev_in[b])
+        if k >= 2:
+            stream.wait_event(ev_out[b])
+        for l in range(cfg.layers):
+            q, kk, vv = d_in[b][l]
+            pool.prefill(l, q, cfg.scale, kk, vv, d_pos[b], nt, out=d_out[b][l])
+        ev_done[b].record(stream)
+        with torch.cuda.stream(cs):
+            cs.wait_event(ev_done[b])
+            for l in range(cfg.layers):
+                h_out[l].copy_(d_out[b][l], non_blocking=True)
+            ev_out[b].record(cs)
+    stream.wait_event(ev_out[(args.steps - 1) % 2])
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = e0.elapsed_time(e1)
+    bits = pool.check_device_errors()
+    if bits:
+        raise RuntimeError(f"device error bits {bits:#x} in the e2e pass")
     pool.close()
     if rank != 0:
         return
@@ -634,15 +730,27 @@ def run_prefill(args, cfg):
         peak, kind = 1900.0, "fallback"
     tflops = flops / (ms / 1e3) / 1e12
     tokens = cfg.batch * n * args.steps
+    cpu = None
+    if ws == 1 and not args.no_cpu_baseline:
+        spent, done, threads = prefill_oracle_sample(cfg, wl, n, budget_s=args.cpu_budget)
+        cpu = {"value": done / (spent * cfg.layers), "unit": "tokens/s", "cores": threads, "kind": "oracle",
+               "sample": f"the first {done} chunk tokens of sequence 0 in layer 0 (every query head, full windows), "
+                         f"{spent:.1f} s of fp64 oracle time; per-token time scaled by {cfg.layers} layers"}
     line = {"metric": "chunked prefill tokens/s (windowed attention + ring append, all layers)",
             "value": tokens / (ms / 1e3), "unit": "tokens/s", "n_gpus": ws, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms / args.steps, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": cfg.dtype, "data": "synthetic",
             "config": {"workload": workload_desc(cfg) + f", chunk {n} tokens per sequence on top of the context",
-                       "global_batch": cfg.batch, "seq_len": max(cfg.prefill)},
+                       "global_batch": cfg.batch, "seq_len": max(cfg.prefill),
+                       "l2": "each step streams every layer's prior windows (GBs) from HBM"},
             "roofline": {"bound": "tensor", "achieved": tflops, "peak": peak, "unit": "TFLOP/s",
                          "frac": tflops / peak, "traffic": None, "peak_kind": kind,
-                         "kernel": "prefill_kernel (tcgen05 bf16, accumulators in tensor memory) + chunk append, one pair per layer"}}
+                         "kernel": "prefill_kernel (tcgen05 bf16, accumulators in tensor memory) + chunk append, one pair per layer"},
+            "cpu_baseline": cpu,
+            "e2e": {"value": cfg.batch * n * args.steps / (e2e_ms / 1e3), "unit": "tokens/s",
+                    "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+            "gpu_launches": launches,
+            "clocks": clock_info}
     print(json.dumps(line), flush=True)
 
 
