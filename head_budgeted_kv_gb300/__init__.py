@@ -16,7 +16,7 @@ from typing import Optional
 import torch
 
 from . import binding
-from .binding import (HWKV_BF16, HWKV_F32, HWKV_KERNEL_AUTO, HWKV_KERNEL_SIMT, HWKV_KERNEL_TENSOR, HwkvError,
+from .binding import (HWKV_BF16, HWKV_F32, HWKV_KERNEL_AUTO, HWKV_KERNEL_SIMT, HWKV_KERNEL_TENSOR, DecodeLaunch, HwkvError,
                       hwkv_abi_version, hwkv_append, hwkv_append_decode_attn, hwkv_block_table,
                       hwkv_check_device_errors, hwkv_kernel_launches,
                       hwkv_decode_attn, hwkv_decode_workspace_bytes, hwkv_materialize, hwkv_pool_bytes,
@@ -25,7 +25,7 @@ from .binding import (HWKV_BF16, HWKV_F32, HWKV_KERNEL_AUTO, HWKV_KERNEL_SIMT, H
                       hwkv_set_prefill_config)
 
 __all__ = [
-    "Pool", "HwkvError", "binding", "HWKV_F32", "HWKV_BF16", "HWKV_KERNEL_AUTO", "HWKV_KERNEL_TENSOR",
+    "Pool", "DecodeLaunch", "HwkvError", "binding", "HWKV_F32", "HWKV_BF16", "HWKV_KERNEL_AUTO", "HWKV_KERNEL_TENSOR",
     "HWKV_KERNEL_SIMT", "hwkv_abi_version", "hwkv_append", "hwkv_append_decode_attn", "hwkv_block_table",
     "hwkv_check_device_errors", "hwkv_kernel_launches",
     "hwkv_decode_attn", "hwkv_decode_workspace_bytes", "hwkv_materialize", "hwkv_pool_bytes", "hwkv_pool_create",
@@ -106,6 +106,15 @@ class Pool:
         hwkv_append_decode_attn(self.handle, layer, q, scale, k_new, v_new, pos, out, self.workspace, stream,
                                 early_reads)
         return out
+
+    def decode_launch(self, layer: int, q, scale: float, lens, out, k_new=None, v_new=None, stream=None,
+                      early_reads: bool = False) -> DecodeLaunch:
+        """A prepared launch of decode (k_new None, ``lens`` = lengths after the append) or of the
+        fused append + decode (``lens`` = positions) on fixed buffers: calling it launches."""
+        if q.shape[1] != self.q_heads:
+            self.q_heads = q.shape[1]
+            self._size_workspace()
+        return DecodeLaunch(self.handle, layer, q, scale, lens, out, self.workspace, k_new, v_new, stream, early_reads)
 
     def prefill(self, layer: int, q, scale: float, k_new, v_new, pos, n, out=None, stream=None):
         """Chunked prefill: q [B][n_max][Hq][D], k_new/v_new [B][n_max][Hkv][D]; pos, n int32 [B].

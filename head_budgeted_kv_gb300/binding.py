@@ -252,6 +252,34 @@ def hwkv_append_decode_attn(pool: int, layer: int, q: torch.Tensor, scale: float
                                           _ptr(pos), _ptr(out), _ptr(workspace), ws_bytes, _stream_ptr(stream)))
 
 
+class DecodeLaunch:
+    """One hwkv_decode_attn_ex launch whose arguments are checked and marshalled once; each call
+    issues the launch again with the same buffers (a serving loop's static q / k_new / v_new /
+    positions / output, or inputs prepared ahead of a timed loop).  k_new and v_new None: decode
+    at lengths `lens` (after the append); given: append at positions `lens`, then decode.  The
+    tensors are kept alive by the object.  Each call costs about one ctypes call plus the launch,
+    against ~17 us for the checks, pointer reads and current-stream lookup of a plain call."""
+
+    def __init__(self, pool: int, layer: int, q: torch.Tensor, scale: float, lens: torch.Tensor, out: torch.Tensor,
+                 workspace: Optional[torch.Tensor], k_new: Optional[torch.Tensor] = None,
+                 v_new: Optional[torch.Tensor] = None, stream=None, early_reads: bool = False):
+        tensors = [t for t in (q, out, k_new, v_new) if t is not None]
+        if not all(t.is_contiguous() for t in tensors):
+            raise ValueError("q, out, k_new and v_new must be contiguous")
+        if (k_new is None) != (v_new is None):
+            raise ValueError("k_new and v_new go together")
+        ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+        self._keep = (q, lens, out, workspace, k_new, v_new)
+        self._fn = load().hwkv_decode_attn_ex
+        self._args = (pool, layer, _ptr(q), q.shape[1], float(scale), _ptr(k_new), _ptr(v_new), _ptr(lens), _ptr(out),
+                      _ptr(workspace), ws_bytes, HWKV_DECODE_EARLY_READS if early_reads else 0, _stream_ptr(stream))
+
+    def __call__(self):
+        status = self._fn(*self._args)
+        if status != HWKV_OK:
+            raise HwkvError(status, last_error())
+
+
 def hwkv_decode_attn_noalloc(pool: int, layer: int, q: torch.Tensor, scale: float, lens: torch.Tensor,
                              out: torch.Tensor, stream=None):
     """hwkv_decode_attn with the library's static scratch instead of a caller workspace."""

@@ -91,3 +91,42 @@ def test_early_reads_equal_default_bit_for_bit(case):
         run.close()
     assert torch.equal(results[0][0], results[1][0])
     assert torch.equal(results[0][1], results[1][1])
+
+
+def test_prepared_launch_equals_plain_calls_bit_for_bit():
+    """Pool.decode_launch (arguments marshalled once, then launched per step) gives the same
+    outputs and rings as the plain append_decode calls, for the fused and the decode-only forms."""
+    cfg = small_config(name="prepared", cfg_id=98, layers=2, kv_heads=2, windows=((1024, 64), (256, 2048)),
+                       prefill=(1500, 300), steps=3)
+    results = []
+    for prepared in (False, True):
+        run = Run(cfg, fused=True)
+        run.materialize()
+        dev = run.dev
+        pre = torch.tensor(cfg.prefill, dtype=torch.int32, device=dev)
+        pos = [(pre + i).contiguous() for i in range(cfg.steps)]
+        ins = [run.wl.step_inputs(i, dev) for i in range(cfg.steps)]
+        outs = torch.zeros((cfg.steps + 1, cfg.layers, cfg.batch, cfg.q_heads, cfg.head_dim), dtype=torch.bfloat16,
+                           device=dev)
+        torch.cuda.synchronize()
+        for i in range(cfg.steps):
+            q, kn, vn = ins[i]
+            for l in range(cfg.layers):
+                if prepared:
+                    run.pool.decode_launch(l, q[l], cfg.scale, pos[i], outs[i, l], kn[l], vn[l])()
+                else:
+                    run.pool.append_decode(l, q[l], cfg.scale, kn[l], vn[l], pos[i], out=outs[i, l])
+        # decode only (no append) at the lengths after the last step
+        lens = (pre + cfg.steps).contiguous()
+        q = ins[-1][0]
+        for l in range(cfg.layers):
+            if prepared:
+                run.pool.decode_launch(l, q[l], cfg.scale, lens, outs[cfg.steps, l])()
+            else:
+                run.pool.decode(l, q[l], cfg.scale, lens, out=outs[cfg.steps, l])
+        torch.cuda.synchronize()
+        assert run.device_errors() == 0
+        results.append((outs.clone(), run.pool.buffer.clone()))
+        run.close()
+    assert torch.equal(results[0][0], results[1][0])
+    assert torch.equal(results[0][1], results[1][1])
