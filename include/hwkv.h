@@ -250,7 +250,9 @@ int hwkv_set_prefill_config(hwkv_pool_t pool, int max_stages);
 
 /* Decode configuration.  kernel = HWKV_KERNEL_*.  split_tokens: tokens of one split-K chunk of
  * the CUDA-core kernel (0 = automatic; else a power of two in [16, 65536]).  workers: CTAs of
- * the tensor-core kernel's persistent grid (0 = automatic: every SM, as many CTAs as fit).
+ * the tensor-core kernel's persistent grid (0 = automatic: every SM, as many CTAs as fit; 95% of
+ * that when a layer's ring capacity is under 128 16-token tiles per CTA, so the next launch's
+ * first CTAs find free slots).
  * Changes the workspace size.  Results differ between configurations only by rounding. */
 int hwkv_set_decode_config(hwkv_pool_t pool, int split_tokens, int workers, int kernel);
 
