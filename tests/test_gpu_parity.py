@@ -308,3 +308,39 @@ def test_host_side_argument_errors():
     assert e.value.status == hw.binding.HWKV_ERR_POOL_TOO_SMALL
     assert run.device_errors() == 0
     run.close()
+
+
+def _random_case(seed: int):
+    """A seeded random small geometry: GQA group, head_dim, block size, per-head windows (some
+    not multiples of the block size, some beyond the context), ragged lengths, fused or not,
+    and a persistent grid from one CTA to more CTAs than tiles."""
+    rng = np.random.default_rng(1000 + seed)
+    kv_heads = int(rng.integers(1, 6))
+    group = int(rng.choice([1, 2, 3, 4, 5, 8, 12, 16]))
+    head_dim = int(rng.choice([64, 128]))
+    block_size = int(rng.choice([16, 32, 64]))
+    layers = int(rng.integers(1, 3))
+    batch = int(rng.integers(1, 5))
+    windows = tuple(tuple(int(rng.choice([int(rng.integers(1, 200)), 256, 1000, 2048, 4096, 8192]))
+                          for _ in range(kv_heads)) for _ in range(layers))
+    prefill = tuple(int(rng.integers(0, 9000)) for _ in range(batch))
+    fused = bool(rng.integers(0, 2))
+    workers = int(rng.choice([0, 0, 1, 3, 17, 100, 288, 1000]))
+    cfg = small_config(name=f"random{seed}", cfg_id=200 + seed, layers=layers, kv_heads=kv_heads, group=group,
+                       head_dim=head_dim, block_size=block_size, windows=windows, prefill=prefill, steps=2)
+    return cfg, fused, workers
+
+
+@pytest.mark.parametrize("seed", range(16))
+def test_random_geometries_match_the_oracle(seed):
+    cfg, fused, workers = _random_case(seed)
+    run = Run(cfg, fused=fused, workers=workers)
+    run.materialize()
+    for i in range(cfg.steps):
+        res = run.step(keep_layers=range(cfg.layers))
+        for l, (q_raw, got) in res.items():
+            ref = run.reference(i, l, q_raw)
+            assert_close(got, ref, cfg, f"random {seed} (fused {fused}, workers {workers}) step {i} layer {l}")
+    _check_all_pool_blocks(run)
+    assert run.device_errors() == 0
+    run.close()
