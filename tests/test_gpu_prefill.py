@@ -302,3 +302,31 @@ def test_prefill_block_permutation_leaves_output_bit_identical(block_size):
     for p in pools:
         assert p.check_device_errors() == 0
         p.close()
+
+
+def _random_prefill_case(seed: int):
+    """A seeded random chunked-prefill geometry: GQA group, head_dim, block size, per-head
+    windows (some odd, some beyond the context), context from empty to a few thousand tokens,
+    one or two ragged chunks (some empty), and a forced split of long key streams in some."""
+    rng = np.random.default_rng(2000 + seed)
+    kv_heads = int(rng.integers(1, 4))
+    group = int(rng.choice([1, 2, 3, 4, 5, 8, 12, 16]))
+    head_dim = int(rng.choice([64, 128]))
+    block_size = int(rng.choice([16, 32, 64, 128]))
+    layers = int(rng.integers(1, 3))
+    batch = int(rng.integers(1, 4))
+    windows = tuple(tuple(int(rng.choice([int(rng.integers(1, 130)), 64, 256, 1000, 4096])) for _ in range(kv_heads))
+                    for _ in range(layers))
+    prefill = tuple(int(rng.choice([0, int(rng.integers(1, 5000))])) for _ in range(batch))
+    chunks = [[int(rng.choice([0, int(rng.integers(1, 200))])) for _ in range(batch)]
+              for _ in range(int(rng.integers(1, 3)))]
+    max_stages = int(rng.choice([0, 0, 2, 5]))
+    cfg = small_config(name=f"pf_random{seed}", cfg_id=300 + seed, layers=layers, kv_heads=kv_heads, group=group,
+                       head_dim=head_dim, block_size=block_size, windows=windows, prefill=prefill, steps=2)
+    return cfg, chunks, max_stages
+
+
+@pytest.mark.parametrize("seed", range(12))
+def test_random_prefill_geometries_match_the_oracle(seed):
+    cfg, chunks, max_stages = _random_prefill_case(seed)
+    _run(cfg, chunks, max_stages=max_stages)
