@@ -37,8 +37,8 @@ FALLBACK_HBM_GBS = 6800.0
 # dram__bytes_read.sum + dram__bytes_write.sum per decode launch from one ncu capture of
 # the tensor-core decode kernel, with the sha256 of hwkv_decode_tc.cu it was taken on.  When
 # the kernel source changes the figure no longer applies and is reported as null.
-DECODE_TRAFFIC = {"source_sha256": "57c534862ac976efae700de3d4ccc231bcb0526c3a5bbafb0b0134c5c7351bcb",
-                  "bytes_per_launch": (621.248768 + 3.091456 + 489.043456 + 0.199680) / 2 * 1e6,
+DECODE_TRAFFIC = {"source_sha256": "2aef5002e637a4e966876b5daa5708d21c62a522874d73735a9809640c89345a",
+                  "bytes_per_launch": (621.199616 + 2.796800 + 489.053696 + 0.107776) / 2 * 1e6,
                   "launch": "layers 0 and 1 of the full workload (2-layer run, same per-launch shape)"}
 
 

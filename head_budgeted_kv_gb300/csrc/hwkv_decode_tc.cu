@@ -323,8 +323,10 @@ __host__ __device__ constexpr int merge_heads() {
   return GP < 8 ? GP : (D == 128 ? 4 : 8);
 }
 
+// Two CTAs per SM at head_dim 128; three at 64 (4 stages of half-size tiles fit three in shared
+// memory, and the per-tile instruction chain, twice as long per byte there, needs the warps).
 template <int D, int GP, int NS>
-__global__ void __launch_bounds__(kWarps * 32, 2) decode_sk_kernel(const __grid_constant__ CUtensorMap tmap,
+__global__ void __launch_bounds__(kWarps * 32, D == 64 ? 3 : 2) decode_sk_kernel(const __grid_constant__ CUtensorMap tmap,
                                                                 const __grid_constant__ DecodeArgs a) {
   constexpr int W = kWarps;
   constexpr int kHalves = D / 64;
@@ -786,10 +788,12 @@ constexpr int sk_smem_bytes() {
   return kWarps * NS * (2 * kTile * D * 2) + kWarps * merge_heads<D, GP>() * D * 4 + 1024;
 }
 
-// pipeline depth: 3 (head_dim 128) or 6 (head_dim 64) stages of 16 tokens per warp
+// pipeline depth: 3 (head_dim 128) or 4 (head_dim 64) stages of 16 tokens per warp; at 64 the
+// same bytes stay in flight per SM with three CTAs (4 stages: D64 decode 0.75 -> 0.81 of the copy
+// peak against 6 stages and two CTAs)
 template <int D>
 constexpr int stages() {
-  return D == 128 ? 3 : 6;
+  return D == 128 ? 3 : 4;
 }
 
 template <int D, int GP>
