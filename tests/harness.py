@@ -89,6 +89,36 @@ class Run:
         self.steps_done += 1
         return res
 
+    def run_prepared(self, keep_steps: Iterable[int], keep_layers: Iterable[int]):
+        """All remaining steps as the decode benchmark issues them: every step's inputs and
+        positions prepared first, then one prepared fused launch per layer with early reads,
+        back to back with no host synchronisation.  Returns {(step, layer): (q raw, out)}."""
+        cfg = self.cfg
+        first = self.steps_done
+        steps = range(first, cfg.steps)
+        inputs = []
+        for i in steps:
+            q, kn, vn = self.wl.step_inputs(i, self.dev)
+            if self.host_steps is not None:
+                self.host_steps.append((None, kn.cpu(), vn.cpu()))
+            inputs.append((q, kn, vn, (self.prefill + i).contiguous()))
+        outs = torch.empty((len(inputs), cfg.layers, cfg.batch, cfg.q_heads, cfg.head_dim),
+                           dtype=cfg.torch_dtype, device=self.dev)
+        launches = [[self.pool.decode_launch(l, q[l], cfg.scale, pos, outs[j, l], kn[l], vn[l], early_reads=True)
+                     for l in range(cfg.layers)] for j, (q, kn, vn, pos) in enumerate(inputs)]
+        torch.cuda.synchronize()
+        for step in launches:
+            for launch in step:
+                launch()
+        torch.cuda.synchronize()
+        self.steps_done = cfg.steps
+        res = {}
+        for i in keep_steps:
+            for l in keep_layers:
+                res[(i, l)] = (workloads.to_raw(inputs[i - first][0][l]),
+                               outs[i - first, l].float().cpu().double().numpy())
+        return res
+
     def device_errors(self) -> int:
         return self.pool.check_device_errors()
 

@@ -1,10 +1,12 @@
-"""Parity at full size, in the launch configuration bench.py times (fused append + decode,
-automatic persistent grid), on sampled outputs the oracle computes one by one.
+"""Parity at full size, in the launch configuration bench.py times (prepared fused append +
+decode launches with early reads, back to back, automatic persistent grid), on sampled outputs
+the oracle computes one by one.
 
-Each workload runs all of its decode steps.  At the first, middle and last step the outputs
-of layers {0, 1, last} are compared with the oracle (every query head; for the 64-sequence
-ragged batch, 8 sequences spread over its length range).  After the last step the ring
-contents of sampled heads are compared bit for bit with the oracle's ring model."""
+Each workload runs all of its decode steps without a host synchronisation between them.  At the
+first, middle and last step the outputs of layers {0, 1, last} are compared with the oracle
+(every query head; for the 64-sequence ragged batch, 8 sequences spread over its length range).
+After the last step the ring contents of sampled heads are compared bit for bit with the
+oracle's ring model."""
 import numpy as np
 import pytest
 import torch
@@ -47,12 +49,11 @@ def test_full_size_sampled_parity(name):
     seqs = _sample_seqs(cfg)
     check_steps = {0, cfg.steps // 2, cfg.steps - 1}
     check_layers = sorted({0, 1, cfg.layers - 1})
-    for i in range(cfg.steps):
-        res = run.step(keep_layers=check_layers if i in check_steps else ())
-        for l, (q_raw, got) in res.items():
-            ref = run.reference(i, l, q_raw, seqs=seqs)
-            sel = slice(None) if seqs is None else seqs
-            assert_close(got[sel], ref[sel], cfg, f"{name} step {i} layer {l}")
+    res = run.run_prepared(sorted(check_steps), check_layers)
+    for (i, l), (q_raw, got) in sorted(res.items()):
+        ref = run.reference(i, l, q_raw, seqs=seqs)
+        sel = slice(None) if seqs is None else seqs
+        assert_close(got[sel], ref[sel], cfg, f"{name} step {i} layer {l}")
     assert run.device_errors() == 0
 
     # ring contents of sampled heads, bit for bit
