@@ -750,14 +750,34 @@ __global__ void __launch_bounds__(256) chunk_append_kernel(const __grid_constant
 
 // Merges the partials of split key streams: per (seq, head, tile pair) whose stream was split,
 // each live row's output is the online-softmax merge of its splits' (O, reference maximum m,
-// sum l): out = sum_i O_i 2^(m_i - M) / sum_i l_i 2^(m_i - M), M = max_i m_i.  One warp per row,
-// lanes over head_dim.
+// sum l): out = sum_i O_i 2^(m_i - M) / sum_i l_i 2^(m_i - M), M = max_i m_i.  A CTA takes
+// kCombineRows rows of one tile pair and a warp a quarter of those, one row at a time: lane i
+// holds split i's (m, l) and split i + 32's, so the maximum is one warp reduction and every
+// weight is known before the partial rows (lanes over head_dim) stream in, kCombineAhead splits
+// per batch of loads.  The sums run in split order.
+constexpr int kCombineRows = 32;
+constexpr int kCombineAhead = 8;
+
+template <int C>
+struct CombineVec;
+template <>
+struct CombineVec<4> {
+  using T = float4;
+};
+template <>
+struct CombineVec<2> {
+  using T = float2;
+};
+
 template <int D>
 __global__ void __launch_bounds__(256) prefill_combine_kernel(const __grid_constant__ PrefillArgs a) {
   constexpr int kC = D / 32;  // columns per lane
+  constexpr int kSlabs = 2 * kPfM / kCombineRows;
+  using Vec = typename CombineVec<kC>::T;
   const int per_head = a.pv.num_seqs * a.q_tiles;
-  const int hi = blockIdx.x / per_head;
-  const int item = blockIdx.x - hi * per_head;
+  const int unit = blockIdx.x / kSlabs, slab = blockIdx.x - unit * kSlabs;
+  const int hi = unit / per_head;
+  const int item = unit - hi * per_head;
   const int sp = a.splits[hi];
   if (sp <= 1) return;
   const int h = a.head_order[hi];
@@ -769,25 +789,45 @@ __global__ void __launch_bounds__(256) prefill_combine_kernel(const __grid_const
   if (qa >= n) return;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const size_t slot0 = (size_t)a.head_ctas[hi] + (size_t)item * sp;
-  for (int row = warp; row < 2 * kPfM; row += 8) {
+  const float2* part_ml = reinterpret_cast<const float2*>(a.part_ml);
+  const size_t split_stride = (size_t)2 * kPfM * D;  // floats from one split's row to the next's
+  for (int k = 0; k < kCombineRows / 8; ++k) {
+    const int row = slab * kCombineRows + warp * (kCombineRows / 8) + k;
     const int x = row / kPfM, r = row - x * kPfM;
     const int tok = qa + x * QT + r / G;
     if (r >= QT * G || tok >= n) continue;
-    float M = kNegInf;
-    for (int i = 0; i < sp; ++i) M = fmaxf(M, reinterpret_cast<const float2*>(a.part_ml)[(slot0 + i) * 2 * kPfM + row].x);
+    float2 e0 = make_float2(kNegInf, 0.f), e1 = e0;
+    if (lane < sp) e0 = part_ml[(slot0 + lane) * 2 * kPfM + row];
+    if (lane + 32 < sp) e1 = part_ml[(slot0 + lane + 32) * 2 * kPfM + row];
+    float M = fmaxf(e0.x, e1.x);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
     float L = 0.f, acc[kC];
 #pragma unroll
     for (int c = 0; c < kC; ++c) acc[c] = 0.f;
     if (M != kNegInf) {
-      for (int i = 0; i < sp; ++i) {
-        const size_t pr = (slot0 + i) * 2 * kPfM + row;
-        const float2 ml = reinterpret_cast<const float2*>(a.part_ml)[pr];
-        if (ml.x == kNegInf) continue;
-        const float f = ex2(ml.x - M);
-        L = fmaf(ml.y, f, L);
-        const float* po = a.part_o + pr * D + lane * kC;
+      const float f0 = e0.x == kNegInf ? 0.f : ex2(e0.x - M);
+      const float f1 = e1.x == kNegInf ? 0.f : ex2(e1.x - M);
+      const float* po = a.part_o + (slot0 * 2 * kPfM + row) * D + lane * kC;
+      for (int i0 = 0; i0 < sp; i0 += kCombineAhead) {
+        Vec v[kCombineAhead];
 #pragma unroll
-        for (int c = 0; c < kC; ++c) acc[c] = fmaf(po[c], f, acc[c]);
+        for (int j = 0; j < kCombineAhead; ++j)
+          if (i0 + j < sp) v[j] = *reinterpret_cast<const Vec*>(po + (size_t)(i0 + j) * split_stride);
+#pragma unroll
+        for (int j = 0; j < kCombineAhead; ++j) {
+          const int i = i0 + j;
+          if (i >= sp) break;
+          const bool lo = i < 32;
+          const float mi = __shfl_sync(0xffffffffu, lo ? e0.x : e1.x, i & 31);
+          const float li = __shfl_sync(0xffffffffu, lo ? e0.y : e1.y, i & 31);
+          const float fi = __shfl_sync(0xffffffffu, lo ? f0 : f1, i & 31);
+          if (mi == kNegInf) continue;  // an empty partial
+          L = fmaf(li, fi, L);
+          const float* vf = reinterpret_cast<const float*>(&v[j]);
+#pragma unroll
+          for (int c = 0; c < kC; ++c) acc[c] = fmaf(vf[c], fi, acc[c]);
+        }
       }
     }
     const float inv = L > 0.f ? 1.f / L : 0.f;
@@ -837,7 +877,12 @@ cudaError_t launch_prefill(const PrefillArgs& a, const CUtensorMap* pool_map, co
 }
 
 cudaError_t launch_prefill_combine(const PrefillArgs& a, cudaStream_t st) {
-  const int blocks = a.pv.kv_heads * a.pv.num_seqs * a.q_tiles;
+  // split heads come first in the work order (decreasing windows); only their units get CTAs
+  int split_heads = 0;
+  for (int i = 0; i < a.pv.kv_heads; ++i)
+    if (a.splits[i] > 1) split_heads = i + 1;
+  const int blocks = split_heads * a.pv.num_seqs * a.q_tiles * (2 * kPfM / kCombineRows);
+  if (blocks == 0) return cudaSuccess;
   if (a.pv.head_dim == 128) prefill_combine_kernel<128><<<blocks, 256, 0, st>>>(a);
   else if (a.pv.head_dim == 64) prefill_combine_kernel<64><<<blocks, 256, 0, st>>>(a);
   else return cudaErrorInvalidValue;

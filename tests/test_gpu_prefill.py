@@ -156,6 +156,8 @@ CASES = {
     "split_ragged": dict(layers=2, kv_heads=3, windows=((64, 1024, 16), (256, 48, 500)), prefill=(700, 20, 130),
                          chunks=[[33, 0, 90]], max_stages=2),
     "split_g16": dict(kv_heads=2, group=16, windows=((900, 512),), prefill=(600, 7), chunks=[[45, 9]], max_stages=3),
+    # 64 and 33 splits of one stream: the combine's lanes hold splits i and i + 32
+    "split_wide": dict(kv_heads=2, windows=((4096, 2000),), prefill=(4500, 3000), chunks=[[50, 17]], max_stages=1),
 }
 
 
