@@ -12,9 +12,13 @@
 #include <cstdarg>
 #include <cstdio>
 #include <cstring>
+#include <functional>
 #include <limits>
+#include <map>
+#include <mutex>
 #include <new>
 #include <string>
+#include <tuple>
 #include <vector>
 
 #include "hwkv_internal.h"
@@ -166,6 +170,9 @@ struct hwkv_pool {
   alignas(64) CUtensorMap stage_map;
   int stage_tb = 0;
   int prefill_max_stages = 0;  // cap on a prefill CTA's key stages (0 = automatic)
+  // automatic prefill split counts per head, by (layer, group, chunk size)
+  mutable std::map<std::tuple<int, int, int>, std::vector<int>> prefill_plans;
+  mutable std::mutex prefill_plans_mu;
 };
 
 namespace {
@@ -208,43 +215,141 @@ void plan_decode(hwkv_pool* p) {
   }
 }
 
-// Work plan of one prefill launch: heads by decreasing window; a head whose key stream (upper
-// bound over lengths) is much longer than an even share of the work is split over several CTAs
-// per (seq, query-tile pair), whose fp32 partials a combine kernel merges.  Returns the
-// workspace bytes the split needs (0 when nothing is split).  allow_split = false plans one
-// CTA per stream.
+// Time model of a prefill launch for choosing its split, in units of one 64-key stage of one
+// CTA (0.853 us on GB300, the same on every geometry measured).  A CTA costs its stages plus a
+// fixed cost (tensor-memory and barrier setup, the Q load and first stage, the epilogue: ~7.2 us
+// unsplit, ~8.8 us when it stores fp32 partials) and ~0.6 us before the next CTA starts on its
+// SM; each split CTA adds ~0.047 us to the merge kernel.  CTAs are handed to SMs in launch order
+// (one CTA per SM), each to the SM that frees first.  Measured per CTA with %globaltimer stamps:
+// the model reproduces the spans of four long and full-geometry launches within 1%.
+constexpr double kPfFixed = 8.4, kPfFixedSplit = 10.3, kPfGap = 0.7, kPfMergePerCta = 0.055, kPfEmptyCta = 1.2;
+// the split search runs only for launches of at most this many unsplit CTAs (beyond that, many
+// CTAs per SM balance well as they are)
+constexpr int64_t kPfSearchMaxCtas = 2048;
+
+struct PfHead {
+  int h, window, maxst;
+  std::vector<int> stages;  // estimated stages of each tile pair's key stream
+};
+
+// Launch order of the heads for splits sp (indexed like hd): longest CTAs first (the classic
+// longest-processing-time order), then longer windows, then head index.
+std::vector<int> prefill_launch_order(const std::vector<PfHead>& hd, const std::vector<int>& sp) {
+  std::vector<int> order(hd.size());
+  for (size_t i = 0; i < hd.size(); ++i) order[i] = (int)i;
+  std::stable_sort(order.begin(), order.end(), [&](int x, int y) {
+    const int cx = (hd[x].maxst + sp[x] - 1) / sp[x], cy = (hd[y].maxst + sp[y] - 1) / sp[y];
+    if (cx != cy) return cx > cy;
+    return hd[x].window > hd[y].window;
+  });
+  return order;
+}
+
+double predict_prefill(const std::vector<PfHead>& hd, const std::vector<int>& sp, int seqs, int sms) {
+  std::vector<double> free_at((size_t)std::max(1, sms), 0.0);  // min-heap of SM free times
+  double merge = 0.0;
+  for (int i : prefill_launch_order(hd, sp)) {
+    const PfHead& e = hd[(size_t)i];
+    const int ss = (e.maxst + sp[i] - 1) / sp[i];
+    for (int s = 0; s < seqs; ++s)
+      for (int nst : e.stages)
+        for (int k = 0; k < sp[i]; ++k) {
+          const int nloc = std::min(nst, (k + 1) * ss) - k * ss;
+          const double d = nloc > 0 ? nloc + (sp[i] > 1 ? kPfFixedSplit : kPfFixed) + kPfGap : kPfEmptyCta;
+          std::pop_heap(free_at.begin(), free_at.end(), std::greater<double>());
+          free_at.back() += d;
+          std::push_heap(free_at.begin(), free_at.end(), std::greater<double>());
+        }
+    if (sp[i] > 1) merge += kPfMergePerCta * seqs * (double)e.stages.size() * sp[i];
+  }
+  return *std::max_element(free_at.begin(), free_at.end()) + merge;
+}
+
+// Work plan of one prefill launch.  A head whose key stream (upper bound over lengths) is much
+// longer than an even share of the work (about three waves of one CTA per SM, or the configured
+// stage cap) is split over several CTAs per (seq, query-tile pair), whose fp32 partials a merge
+// kernel combines.  In the automatic mode the split counts are then refined per head by a
+// coordinate search on the time model above, and the heads launch longest CTAs first; the plan
+// is kept per (layer, group, chunk size).  Returns the workspace bytes the split needs (0 when
+// nothing is split).  allow_split = false plans one CTA per stream.
 uint64_t plan_prefill(const hwkv_pool* p, int layer, int G, int n_max, bool allow_split, PrefillArgs& a) {
   const Geometry& g = p->g;
   const int H = g.kv_heads;
-  std::vector<int> order(H);
-  for (int h = 0; h < H; ++h) order[h] = h;
   const int* win = &g.windows[(size_t)layer * H];
-  std::stable_sort(order.begin(), order.end(), [&](int x, int y) { return win[x] > win[y]; });
   const int per_pair = prefill_tokens_per_cta(G);
   const int pairs = (n_max + per_pair - 1) / per_pair;
   const int64_t items = (int64_t)g.num_seqs * pairs;
-  std::vector<int> maxst(H);
+  std::vector<PfHead> hd((size_t)H);
   int64_t work = 0;
-  for (int i = 0; i < H; ++i) {
-    const int h = order[i];
+  for (int h = 0; h < H; ++h) {
     const int C = g.nblk[(size_t)layer * H + h] * g.block_size;
-    maxst[i] = prefill_max_stages(win[h], C, G, n_max);
-    work += items * maxst[i];
+    hd[(size_t)h].h = h;
+    hd[(size_t)h].window = win[h];
+    hd[(size_t)h].maxst = prefill_max_stages(win[h], C, G, n_max);
+    work += items * hd[(size_t)h].maxst;
   }
-  // about three waves of one CTA per SM
-  int64_t target = p->prefill_max_stages > 0 ? p->prefill_max_stages
-                                            : std::max<int64_t>(16, (work + 3LL * p->num_sms - 1) / (3LL * p->num_sms));
+  std::vector<int> sp((size_t)H, 1);
+  std::vector<int> order;
+  if (allow_split) {
+    const bool automatic = p->prefill_max_stages <= 0;
+    const int64_t target = !automatic ? p->prefill_max_stages
+                                      : std::max<int64_t>(16, (work + 3LL * p->num_sms - 1) / (3LL * p->num_sms));
+    for (int h = 0; h < H; ++h)
+      if (hd[(size_t)h].maxst > target)
+        sp[(size_t)h] = (int)std::min<int64_t>(64, (hd[(size_t)h].maxst + target - 1) / target);
+    if (automatic && items * H <= kPfSearchMaxCtas) {
+      std::lock_guard<std::mutex> lock(p->prefill_plans_mu);
+      const auto key = std::make_tuple(layer, G, n_max);
+      auto it = p->prefill_plans.find(key);
+      if (it == p->prefill_plans.end()) {
+        for (int h = 0; h < H; ++h) {
+          const int C = g.nblk[(size_t)layer * H + h] * g.block_size;
+          for (int qt = 0; qt < pairs; ++qt)
+            hd[(size_t)h].stages.push_back(prefill_stages_estimate(win[h], C, G, n_max, qt * per_pair));
+        }
+        const double start = predict_prefill(hd, sp, g.num_seqs, p->num_sms);
+        std::vector<int> best = sp;
+        double best_t = start;
+        for (int round = 0; round < 6; ++round) {
+          bool improved = false;
+          for (int h = 0; h < H; ++h)
+            for (int d : {-1, 1, 2}) {
+              std::vector<int> t = best;
+              t[(size_t)h] += d;
+              if (t[(size_t)h] < 1 || t[(size_t)h] > 64) continue;
+              const double v = predict_prefill(hd, t, g.num_seqs, p->num_sms);
+              if (v < best_t - 1e-9) {
+                best_t = v;
+                best = t;
+                improved = true;
+              }
+            }
+          if (!improved) break;
+        }
+        // keep the plain rule unless the model predicts a clear gain
+        if (best_t > 0.98 * start) best = sp;
+        it = p->prefill_plans.emplace(key, best).first;
+      }
+      sp = it->second;
+      order = prefill_launch_order(hd, sp);
+    }
+  }
+  if (order.empty()) {  // heads by decreasing window
+    order.resize((size_t)H);
+    for (int h = 0; h < H; ++h) order[(size_t)h] = h;
+    std::stable_sort(order.begin(), order.end(), [&](int x, int y) { return win[x] > win[y]; });
+  }
   int64_t ctas = 0;
   bool any = false;
   for (int i = 0; i < H; ++i) {
-    int sp = 1;
-    if (allow_split && maxst[i] > target) sp = (int)std::min<int64_t>(64, (maxst[i] + target - 1) / target);
-    a.head_order[i] = order[i];
-    a.splits[i] = sp;
-    a.split_stages[i] = (maxst[i] + sp - 1) / sp;
+    const int h = order[(size_t)i];
+    const int n_sp = sp[(size_t)h];
+    a.head_order[i] = h;
+    a.splits[i] = n_sp;
+    a.split_stages[i] = (hd[(size_t)h].maxst + n_sp - 1) / n_sp;
     a.head_ctas[i] = (int32_t)ctas;
-    ctas += items * sp;
-    any = any || sp > 1;
+    ctas += items * n_sp;
+    any = any || n_sp > 1;
   }
   a.head_ctas[H] = (int32_t)ctas;
   a.q_tiles = pairs;

@@ -127,5 +127,8 @@ cudaError_t launch_chunk_append(const PrefillArgs& a, int max_rows, cudaStream_t
 cudaError_t launch_prefill_combine(const PrefillArgs& a, cudaStream_t st);
 // upper bound on the 64-key stages of one prefill CTA's key stream for a head
 int prefill_max_stages(int window, int ring_capacity, int group, int n_max);
+// the 64-key stages the tile pair starting at chunk row qa streams when the context before the
+// chunk is longer than the ring and the chunk holds n_max rows (work estimate for planning)
+int prefill_stages_estimate(int window, int ring_capacity, int group, int n_max, int qa);
 
 }  // namespace hwkv

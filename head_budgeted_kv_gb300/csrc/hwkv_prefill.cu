@@ -864,6 +864,24 @@ int prefill_max_stages(int window, int ring_capacity, int group, int n_max) {
 
 int prefill_tile_tokens(int group) { return kPfM / group; }
 
+int prefill_stages_estimate(int window, int ring_capacity, int group, int n_max, int qa) {
+  // the kernel's key tiles (prior positions [lo, p0), chunk rows [clo, qb)) for p0 = 2 C
+  const int qt2 = 2 * (kPfM / group);
+  const int qb = std::min(n_max, qa + qt2);
+  if (qa >= qb) return 0;
+  const int64_t C = ring_capacity, p0 = 2 * C;
+  const int64_t lo = std::max<int64_t>(0, p0 + qa + 1 - window);
+  const int64_t need = p0 - lo;
+  int64_t prior = 0;
+  if (need > 0) {
+    const int64_t first = lo % C;
+    prior = std::min<int64_t>(C / 16, (first + need - 1) / 16 - first / 16 + 1);
+  }
+  const int clo = std::max(0, qa + 1 - window);
+  const int64_t chunk = (qb - 1) / 16 - clo / 16 + 1;
+  return (int)((prior + chunk + kPfSub - 1) / kPfSub);
+}
+
 cudaError_t launch_prefill(const PrefillArgs& a, const CUtensorMap* pool_map, const CUtensorMap* stage_map,
                            const CUtensorMap* knew_map, const CUtensorMap* vnew_map, const CUtensorMap* knew64_map,
                            const CUtensorMap* vnew64_map, const CUtensorMap* q_map, cudaStream_t st) {

@@ -245,7 +245,10 @@ int hwkv_prefill_attn(hwkv_pool_t pool, int layer, const void* q, int q_heads, f
 int hwkv_prefill_workspace_bytes(hwkv_pool_t pool, int layer, int q_heads, int n_max, uint64_t* out);
 
 /* Prefill configuration: max_stages caps the 64-key stages one CTA streams before its stream is
- * split (0 = automatic: about three waves of one CTA per SM).  Results differ only by rounding. */
+ * split, the same cap for every head (0 = automatic: a cap of about three waves of one CTA per
+ * SM, then, for launches of at most 2048 unsplit CTAs, split counts refined per head against a
+ * time model of the launch, planned once per (layer, q_heads, n_max) and kept).  Results differ
+ * only by rounding. */
 int hwkv_set_prefill_config(hwkv_pool_t pool, int max_stages);
 
 /* Decode configuration.  kernel = HWKV_KERNEL_*.  split_tokens: tokens of one split-K chunk of
