@@ -85,7 +85,7 @@ struct PrefillArgs {
   float scale_log2;
   int32_t bs_log2;         // log2(block_size), or -1 when it is not a power of two
   int32_t stage_tb;        // rows of one block in a 64-key pool copy (16, 32, 64), 0: per-tile copies only
-  int32_t head_order[kMaxKvHeads];  // heads by decreasing window (work order)
+  int32_t head_order[kMaxKvHeads];  // heads in work order (longest CTAs first)
   // split of long key streams: head order position i has splits[i] CTAs per (seq, tile pair),
   // each streaming split_stages[i] stages; its CTAs are [head_ctas[i], head_ctas[i + 1])
   int32_t splits[kMaxKvHeads];

@@ -216,7 +216,7 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_kernel(const __grid_con
   const int Hq = H * G;
   const int bs = a.pv.block_size;
 
-  // work item: heads in the host's order (longest windows first), then sequences, tile pairs,
+  // work item: heads in the host's order (longest CTAs first), then sequences, tile pairs,
   // then the splits of the pair's key stream
   int hi = 0;
   while (hi + 1 < H && (int)blockIdx.x >= a.head_ctas[hi + 1]) ++hi;
@@ -895,7 +895,7 @@ cudaError_t launch_prefill(const PrefillArgs& a, const CUtensorMap* pool_map, co
 }
 
 cudaError_t launch_prefill_combine(const PrefillArgs& a, cudaStream_t st) {
-  // split heads come first in the work order (decreasing windows); only their units get CTAs
+  // CTAs for the work-order positions up to the last split head (the others return at once)
   int split_heads = 0;
   for (int i = 0; i < a.pv.kv_heads; ++i)
     if (a.splits[i] > 1) split_heads = i + 1;
