@@ -37,8 +37,8 @@ FALLBACK_HBM_GBS = 6800.0
 # dram__bytes_read.sum + dram__bytes_write.sum per decode launch from one ncu capture of
 # the tensor-core decode kernel, with the sha256 of hwkv_decode_tc.cu it was taken on.  When
 # the kernel source changes the figure no longer applies and is reported as null.
-DECODE_TRAFFIC = {"source_sha256": "2aef5002e637a4e966876b5daa5708d21c62a522874d73735a9809640c89345a",
-                  "bytes_per_launch": (621.199616 + 2.796800 + 489.053696 + 0.107776) / 2 * 1e6,
+DECODE_TRAFFIC = {"source_sha256": "ca4a3fbd0a3621c234dbceb982cd3d695f6ff31850eef6be9bf8efb04c9f5765",
+                  "bytes_per_launch": (621.200128 + 3.054592 + 489.046528 + 0.115712) / 2 * 1e6,
                   "launch": "layers 0 and 1 of the full workload (2-layer run, same per-launch shape)"}
 
 

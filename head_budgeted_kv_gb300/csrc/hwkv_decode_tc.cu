@@ -362,6 +362,11 @@ __global__ void __launch_bounds__(kWarps * 32, D == 64 ? 3 : 2) decode_sk_kernel
   const int bs = a.pv.block_size;
   __nv_bfloat16* const out = static_cast<__nv_bfloat16*>(a.out);
 
+  // The next grid in the stream may start at once: its CTAs take the slots this grid's CTAs
+  // free, run their own early reads, and wait for this grid before anything else (with the
+  // trigger at the end of each CTA's stream instead, they started only after the slowest
+  // stream: full workload 961 -> 971 tokens/s, batch 1 unchanged).
+  griddep_launch_dependents();
   // the descriptor is a kernel parameter, so it may be fetched before the wait below
   if (threadIdx.x == 0) prefetch_tensormap(&tmap);
   // Launched as a programmatic dependent.  By default everything waits for the grids this one
@@ -661,7 +666,6 @@ __global__ void __launch_bounds__(kWarps * 32, D == 64 ? 3 : 2) decode_sk_kernel
     }
 
     // ---- end of segment: merge the warps, then store output or partial -----------------
-    if (!more) griddep_launch_dependents();  // this CTA reads no more tiles
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
