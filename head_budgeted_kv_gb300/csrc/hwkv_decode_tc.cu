@@ -86,8 +86,9 @@ constexpr int kGapTiles = 24;
 // Tiles per warp pulled into L2 while the CTA waits for the preceding grid (early reads only),
 // when its range holds at least kL2PrefetchMin positions.  Short ranges (small batches) skip it:
 // there the preceding grid's last streams and merges, which the prefetch would slow, are most of
-// what the wait is for.
-constexpr int kL2Prefetch = 2;
+// what the wait is for.  (Depth on the full workload, with the dependent-launch trigger at
+// kernel entry: 0 -> 957, 2 -> 969, 4 -> 982, 6 -> 989, 8 -> 988 tokens/s.)
+constexpr int kL2Prefetch = 6;
 constexpr int kL2PrefetchMin = 64;
 
 __device__ __forceinline__ int group_span(const Group& gr) { return gr.tiles > 0 ? gr.tiles + kGapTiles : 0; }
