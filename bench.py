@@ -37,8 +37,8 @@ FALLBACK_HBM_GBS = 6800.0
 # dram__bytes_read.sum + dram__bytes_write.sum per decode launch from one ncu capture of
 # the tensor-core decode kernel, with the sha256 of hwkv_decode_tc.cu it was taken on.  When
 # the kernel source changes the figure no longer applies and is reported as null.
-DECODE_TRAFFIC = {"source_sha256": "d6f5d59ff983218df0d8c3fc855079b2212113b65fb206927f21c8194d4fca0e",
-                  "bytes_per_launch": (621.350144 + 3.112448 + 489.176064 + 0.110336) / 2 * 1e6,
+DECODE_TRAFFIC = {"source_sha256": "2713eb527014c59ef868f1168f40222c47e18470ab5f3b3fc9db627c8656f95e",
+                  "bytes_per_launch": (621.362176 + 3.148288 + 489.192960 + 0.108800) / 2 * 1e6,
                   "launch": "layers 0 and 1 of the full workload (2-layer run, same per-launch shape)"}
 
 

@@ -86,9 +86,14 @@ constexpr int kGapTiles = 24;
 // Tiles per warp pulled into L2 while the CTA waits for the preceding grid (early reads only),
 // when its range holds at least kL2PrefetchMin positions.  Short ranges (small batches) skip it:
 // there the preceding grid's last streams and merges, which the prefetch would slow, are most of
-// what the wait is for.  (Depth on the full workload, with the dependent-launch trigger at
-// kernel entry: 0 -> 957, 2 -> 969, 4 -> 982, 6 -> 989, 8 -> 988 tokens/s.)
-constexpr int kL2Prefetch = 6;
+// what the wait is for.  Depth swept on the full geometry with the dependent-launch trigger at
+// kernel entry: head_dim 128, 0 -> 957, 2 -> 969, 4 -> 982, 6 -> 989, 8 -> 988 tokens/s; head_dim
+// 64 (three CTAs per SM, half the bytes per tile), GQA 4: 0 -> 0.828, 2 -> 0.836, 4 -> 0.819,
+// 6 -> 0.807 of the copy peak.
+template <int D>
+__host__ __device__ constexpr int l2_prefetch() {
+  return D == 128 ? 6 : 2;
+}
 constexpr int kL2PrefetchMin = 64;
 
 __device__ __forceinline__ int group_span(const Group& gr) { return gr.tiles > 0 ? gr.tiles + kGapTiles : 0; }
@@ -472,7 +477,7 @@ __global__ void __launch_bounds__(kWarps * 32, D == 64 ? 3 : 2) decode_sk_kernel
   // the first stages are issued by different lanes so their table lookups overlap
   if (has_range)
     for (int i = 0; i < NS && j_issue < t_hi; ++i) issue_next(i);
-  if (a.early && has_range && lane < kL2Prefetch && t_hi - t_lo >= kL2PrefetchMin) {
+  if (a.early && has_range && lane < l2_prefetch<D>() && t_hi - t_lo >= kL2PrefetchMin) {
     // Until the wait below ends, the preceding grid only merges and completes and the memory
     // system is nearly idle: pull the tiles this warp takes after its staged ones into L2
     // (lane i: the position i steps on; a position inside a gap is skipped).
