@@ -21,7 +21,7 @@ from .binding import (HWKV_BF16, HWKV_F32, HWKV_KERNEL_AUTO, HWKV_KERNEL_SIMT, H
                       hwkv_check_device_errors, hwkv_kernel_launches,
                       hwkv_decode_attn, hwkv_decode_workspace_bytes, hwkv_materialize, hwkv_pool_bytes,
                       hwkv_pool_create, hwkv_pool_destroy, hwkv_pool_geometry, hwkv_prefill_attn,
-                      hwkv_prefill_workspace_bytes, hwkv_set_block_table, hwkv_set_decode_config,
+                      hwkv_prefill_plan, hwkv_prefill_workspace_bytes, hwkv_set_block_table, hwkv_set_decode_config,
                       hwkv_set_prefill_config)
 
 __all__ = [
@@ -29,7 +29,7 @@ __all__ = [
     "HWKV_KERNEL_SIMT", "hwkv_abi_version", "hwkv_append", "hwkv_append_decode_attn", "hwkv_block_table",
     "hwkv_check_device_errors", "hwkv_kernel_launches",
     "hwkv_decode_attn", "hwkv_decode_workspace_bytes", "hwkv_materialize", "hwkv_pool_bytes", "hwkv_pool_create",
-    "hwkv_pool_destroy", "hwkv_pool_geometry", "hwkv_prefill_attn", "hwkv_prefill_workspace_bytes",
+    "hwkv_pool_destroy", "hwkv_pool_geometry", "hwkv_prefill_attn", "hwkv_prefill_plan", "hwkv_prefill_workspace_bytes",
     "hwkv_set_block_table", "hwkv_set_decode_config", "hwkv_set_prefill_config",
 ]
 

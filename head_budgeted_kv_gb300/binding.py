@@ -62,6 +62,7 @@ SIGNATURES = [
     ("hwkv_decode_attn_noalloc", _i, [_vp, _i, _vp, _i, ctypes.c_float, _vp, _vp, _vp]),
     ("hwkv_prefill_attn", _i, [_vp, _i, _vp, _i, ctypes.c_float, _vp, _vp, _i, _vp, _vp, _vp, _vp, _u64, _vp]),
     ("hwkv_prefill_workspace_bytes", _i, [_vp, _i, _i, _i, ctypes.POINTER(_u64)]),
+    ("hwkv_prefill_plan", _i, [_i, _i, _i, _i, _c_i32p, _i, _i, _i, _i, _i, _i, _c_i32p, _c_i32p, _c_i32p, _c_u64p]),
     ("hwkv_set_prefill_config", _i, [_vp, _i]),
     ("hwkv_set_decode_config", _i, [_vp, _i, _i, _i]),
     ("hwkv_kernel_launches", _i, [_c_u64p]),
@@ -305,6 +306,21 @@ def hwkv_prefill_workspace_bytes(pool: int, layer: int, q_heads: int, n_max: int
     out = _u64(0)
     _check(load().hwkv_prefill_workspace_bytes(pool, layer, q_heads, n_max, ctypes.byref(out)))
     return out.value
+
+
+def hwkv_prefill_plan(layers: int, kv_heads: int, head_dim: int, block_size: int, windows, num_seqs: int, layer: int,
+                      q_heads: int, n_max: int, num_sms: int, max_stages: int = 0):
+    """Host-only launch plan of hwkv_prefill_attn: (head_order, splits, split_stages) by launch
+    position (int32 arrays of kv_heads entries) and the workspace bytes."""
+    w = _windows(windows)
+    order = np.zeros(kv_heads, dtype=np.int32)
+    splits = np.zeros(kv_heads, dtype=np.int32)
+    stages = np.zeros(kv_heads, dtype=np.int32)
+    ws = _u64(0)
+    _check(load().hwkv_prefill_plan(layers, kv_heads, head_dim, block_size, w.ctypes.data_as(_c_i32p), num_seqs, layer,
+                                    q_heads, n_max, num_sms, max_stages, order.ctypes.data_as(_c_i32p),
+                                    splits.ctypes.data_as(_c_i32p), stages.ctypes.data_as(_c_i32p), ctypes.byref(ws)))
+    return order, splits, stages, ws.value
 
 
 def hwkv_set_prefill_config(pool: int, max_stages: int = 0):

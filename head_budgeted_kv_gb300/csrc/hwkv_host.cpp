@@ -835,6 +835,33 @@ int hwkv_prefill_workspace_bytes(hwkv_pool_t p, int layer, int q_heads, int n_ma
   return ok();
 }
 
+int hwkv_prefill_plan(int layers, int kv_heads, int head_dim, int block_size, const int32_t* windows, int num_seqs,
+                      int layer, int q_heads, int n_max, int num_sms, int max_stages, int32_t* head_order,
+                      int32_t* splits, int32_t* split_stages, uint64_t* workspace_bytes) {
+  if (!head_order || !splits || !split_stages || !workspace_bytes) return fail(HWKV_ERR_INVALID_ARG, "NULL output");
+  hwkv_pool p;  // host fields only: geometry, SM count, stage cap, plan cache
+  const int rc = plan_geometry(layers, kv_heads, head_dim, block_size, windows, num_seqs, HWKV_BF16, &p.g);
+  if (rc != HWKV_OK) return rc;
+  if (block_size % 16 != 0) return fail(HWKV_ERR_UNSUPPORTED, "prefill needs block_size % 16 == 0");
+  if (layer < 0 || layer >= layers) return fail(HWKV_ERR_INVALID_ARG, "layer %d out of range", layer);
+  if (q_heads < kv_heads || q_heads % kv_heads != 0 || q_heads / kv_heads > kMaxGroup)
+    return fail(HWKV_ERR_UNSUPPORTED, "q_heads must be G * kv_heads with 1 <= G <= %d", kMaxGroup);
+  if (n_max < 1) return fail(HWKV_ERR_INVALID_ARG, "n_max must be >= 1");
+  if (num_sms < 1) return fail(HWKV_ERR_INVALID_ARG, "num_sms must be >= 1");
+  if (max_stages < 0) return fail(HWKV_ERR_INVALID_ARG, "max_stages must be >= 0");
+  p.num_sms = num_sms;
+  p.prefill_max_stages = max_stages;
+  PrefillArgs a;
+  std::memset(&a, 0, sizeof a);
+  *workspace_bytes = plan_prefill(&p, layer, q_heads / kv_heads, n_max, true, a);
+  for (int i = 0; i < kv_heads; ++i) {
+    head_order[i] = a.head_order[i];
+    splits[i] = a.splits[i];
+    split_stages[i] = a.split_stages[i];
+  }
+  return ok();
+}
+
 int hwkv_set_prefill_config(hwkv_pool_t p, int max_stages) {
   if (!p) return fail(HWKV_ERR_INVALID_ARG, "pool is NULL");
   if (max_stages < 0) return fail(HWKV_ERR_INVALID_ARG, "max_stages must be >= 0");

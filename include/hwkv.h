@@ -244,6 +244,20 @@ int hwkv_prefill_attn(hwkv_pool_t pool, int layer, const void* q, int q_heads, f
  * the geometry, the GPU's SM count and hwkv_set_prefill_config. */
 int hwkv_prefill_workspace_bytes(hwkv_pool_t pool, int layer, int q_heads, int n_max, uint64_t* out);
 
+/* The launch plan hwkv_prefill_attn uses for `layer` (host only: no pool, no device).  The
+ * geometry arguments are those of hwkv_pool_create (bf16); num_sms is the GPU's SM count and
+ * max_stages the cap of hwkv_set_prefill_config (0 = automatic).  For launch position
+ * i < kv_heads: head_order[i] is the KV head, splits[i] its CTAs per (sequence, query-tile pair)
+ * and split_stages[i] the 64-key stages each of them streams (CTA k of a split stream takes
+ * stages [k * split_stages[i], (k + 1) * split_stages[i]) of it, so splits[i] * split_stages[i]
+ * covers the longest stream of the head).  *workspace_bytes is what hwkv_prefill_workspace_bytes
+ * returns for a pool of this geometry on such a GPU (0 when nothing is split).  The arrays hold
+ * kv_heads entries each and are caller-owned.  Errors as hwkv_pool_bytes and
+ * hwkv_prefill_attn's argument checks. */
+int hwkv_prefill_plan(int layers, int kv_heads, int head_dim, int block_size, const int32_t* windows, int num_seqs,
+                      int layer, int q_heads, int n_max, int num_sms, int max_stages, int32_t* head_order,
+                      int32_t* splits, int32_t* split_stages, uint64_t* workspace_bytes);
+
 /* Prefill configuration: max_stages caps the 64-key stages one CTA streams before its stream is
  * split, the same cap for every head (0 = automatic: a cap of about three waves of one CTA per
  * SM, then, for launches of at most 2048 unsplit CTAs, split counts refined per head against a
