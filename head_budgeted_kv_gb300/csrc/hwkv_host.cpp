@@ -438,6 +438,12 @@ int check_device(const hwkv_pool* p) {
   return HWKV_OK;
 }
 
+}  // namespace
+
+int hwkv::check_pool_device(const hwkv_pool* p) { return check_device(p); }
+
+namespace {
+
 PoolView pool_view(const hwkv_pool* p) {
   PoolView v;
   v.pool = p->dev_pool;

@@ -6,6 +6,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+struct hwkv_pool;
+
 namespace hwkv {
 
 constexpr int kMaxKvHeads = 32;
@@ -100,6 +102,9 @@ void count_launches(uint64_t n);
 
 // Records a message for hwkv_last_error() on this thread and returns `code`.
 int set_error(int code, const char* fmt, ...);
+
+// HWKV_OK when the pool's device is the current one, else an error (message recorded).
+int check_pool_device(const struct ::hwkv_pool* p);
 
 // Launchers (hwkv_copy.cu, hwkv_decode.cu).  dtype: 0 = f32, 1 = bf16.
 cudaError_t launch_append(const CopyArgs& a, int dtype, cudaStream_t st);

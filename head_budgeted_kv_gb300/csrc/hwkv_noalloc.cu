@@ -16,8 +16,11 @@
 
 namespace {
 
-// The scratch array.  Every GPU on which the library's device code is loaded holds these
-// bytes until the process exits, whether or not this entry point is ever called.
+// The scratch array.  It lives in this file's own device module.  Under CUDA's lazy module
+// loading (the default) that module is loaded on a device -- and the 4 MiB committed there --
+// by the first address lookup below, i.e. the first call of the entry point on that device;
+// with eager loading, when the library is loaded.  Either way the bytes stay committed until
+// the process exits.
 constexpr uint64_t kScratchBytes = HWKV_NOALLOC_SCRATCH_BYTES;
 static __device__ __align__(256) unsigned char g_decode_scratch[kScratchBytes];
 
@@ -58,6 +61,10 @@ extern "C" int hwkv_decode_attn_noalloc(hwkv_pool_t pool, int layer, const void*
                            "this decode configuration needs %llu bytes of scratch; the static scratch of "
                            "hwkv_decode_attn_noalloc holds %llu bytes (use hwkv_decode_attn with a workspace)",
                            (unsigned long long)need, (unsigned long long)kScratchBytes);
+  // the address is cached per device: look it up only with the pool's own device current
+  if (!pool) return hwkv::set_error(HWKV_ERR_INVALID_ARG, "pool is NULL");
+  rc = hwkv::check_pool_device(pool);
+  if (rc != HWKV_OK) return rc;
   void* scratch = nullptr;
   rc = scratch_on_current_device(&scratch);
   if (rc != HWKV_OK) return rc;

@@ -204,14 +204,16 @@ int hwkv_decode_attn_ex(hwkv_pool_t pool, int layer, const void* q, int q_heads,
  * memory where they run attention (during CUDA graph capture, under an allocator that owns
  * all device memory, inside hosts that forbid allocation after start-up).  The pages have
  * no counterpart: this is a service of this library, not a step of the method.
- *   Results are those of hwkv_decode_attn with the same arguments.  The split-K scratch is a
- *   fixed array of HWKV_NOALLOC_SCRATCH_BYTES (4 MiB) inside the library, present on every
- *   GPU that loads the library until the process exits; the call itself allocates nothing
- *   (no cudaMalloc / cudaFree, no allocating library routine).
+ *   Results are those of hwkv_decode_attn with the same arguments, bit for bit.  The split-K
+ *   scratch is a fixed array of HWKV_NOALLOC_SCRATCH_BYTES (4 MiB) inside the library; the
+ *   call allocates nothing (no cudaMalloc / cudaFree, no allocating library routine).
  *   A configuration whose scratch (hwkv_decode_workspace_bytes) exceeds the array is
  *   rejected with HWKV_ERR_WORKSPACE_TOO_SMALL before anything is launched.
- *   The first call on a device looks up the array's device address on that device (with
- *   that device current): make that first call before any stream capture.
+ *   The pool's device must be current (HWKV_ERR_INVALID_ARG otherwise).  The first call on a
+ *   device looks up the array's device address there; under CUDA's default lazy module
+ *   loading that lookup also loads the module holding the array and commits its 4 MiB on
+ *   that device, which then stay committed until the process exits.  Make that first call
+ *   before any stream capture.
  *   All calls share the one array and it keeps the last call's contents; nothing in it has
  *   to start at zero.  Calls whose kernels overlap on the GPU (other streams, other threads)
  *   race on the array: serialise them. */

@@ -1,9 +1,11 @@
 """hwkv_decode_attn_noalloc: decode attention for callers that cannot allocate device memory
 where they run attention (for example while a CUDA graph is being captured, or under an
 allocator that owns all device memory).  Its split-K scratch is a fixed array inside the
-library, so it must give the same results as hwkv_decode_attn, which takes a caller
-workspace -- here on two calls in a row, each after an append, so the second call starts
-from the first call's leftovers in the shared array.
+library.  Decode launches are deterministic (no output depends on which CTA arrives last),
+so it must give exactly the bits of hwkv_decode_attn, which takes a caller workspace -- here
+on two calls in a row, each after an append, so the second call starts from the first call's
+leftovers in the shared array -- and both must match the CPU oracle within the bf16
+tolerance.
 
 Kept in a file of its own, collected last."""
 import ctypes
@@ -13,6 +15,7 @@ import pytest
 import torch
 
 import head_budgeted_kv_gb300 as hw
+import workloads
 from harness import Run, assert_close, small_config
 
 pytestmark = pytest.mark.gpu
@@ -40,20 +43,30 @@ def test_noalloc_matches_decode_attn_on_two_consecutive_calls(kernel):
     cfg = small_config(name="noalloc", kv_heads=4, windows=((4096, 1024, 256, 2000),), prefill=(5000, 1500, 300))
     run = Run(cfg, kernel=kernel)
     run.materialize()
-    assert hw.hwkv_decode_workspace_bytes(run.pool.handle, cfg.q_heads) <= (4 << 20)
+    need = hw.hwkv_decode_workspace_bytes(run.pool.handle, cfg.q_heads)
+    assert 0 < need <= (4 << 20)  # the scratch is used, and fits the static array
     for step in range(2):
         q, kn, vn = run.wl.step_inputs(step, run.dev)
+        run.host_steps.append((None, kn.cpu(), vn.cpu()))
         pos = run.prefill + step
         lens = pos + 1
         run.pool.append(0, kn[0], vn[0], pos)
+        run.steps_done += 1
         ref = torch.empty_like(q[0])
         hw.hwkv_decode_attn(run.pool.handle, 0, q[0], cfg.scale, lens, ref, run.pool.workspace)
         got = torch.full_like(q[0], float("nan"))
+        torch.cuda.synchronize()
+        free0 = torch.cuda.mem_get_info()[0]
         rc = _call_noalloc(lib, run.pool.handle, 0, q[0], cfg.scale, lens, got)
         assert rc == hw.binding.HWKV_OK, hw.binding.last_error()
         torch.cuda.synchronize()
-        assert_close(got.float().cpu().double().numpy(), ref.float().cpu().double().numpy(), cfg,
-                     f"noalloc call {step + 1}")
+        if step == 1:
+            # the first call on the device may load the module that holds the array; later
+            # calls leave the device's free memory exactly as it was
+            assert torch.cuda.mem_get_info()[0] == free0
+        assert torch.equal(got, ref), f"noalloc call {step + 1} differs from hwkv_decode_attn"
+        oracle_out = run.reference(step, 0, workloads.to_raw(q[0]))
+        assert_close(got.float().cpu().double().numpy(), oracle_out, cfg, f"noalloc call {step + 1} vs the oracle")
     assert run.device_errors() == 0
     run.close()
 
