@@ -17,7 +17,7 @@ import torch
 
 from . import binding
 from .binding import (HWKV_BF16, HWKV_F32, HWKV_KERNEL_AUTO, HWKV_KERNEL_SIMT, HWKV_KERNEL_TENSOR, DecodeLaunch, HwkvError,
-                      hwkv_abi_version, hwkv_append, hwkv_append_decode_attn, hwkv_block_table,
+                      hwkv_abi_version, hwkv_advance_positions, hwkv_append, hwkv_append_decode_attn, hwkv_block_table,
                       hwkv_check_device_errors, hwkv_kernel_launches,
                       hwkv_decode_attn, hwkv_decode_workspace_bytes, hwkv_materialize, hwkv_pool_bytes,
                       hwkv_pool_create, hwkv_pool_destroy, hwkv_pool_geometry, hwkv_prefill_attn,
@@ -26,7 +26,7 @@ from .binding import (HWKV_BF16, HWKV_F32, HWKV_KERNEL_AUTO, HWKV_KERNEL_SIMT, H
 
 __all__ = [
     "Pool", "DecodeLaunch", "HwkvError", "binding", "HWKV_F32", "HWKV_BF16", "HWKV_KERNEL_AUTO", "HWKV_KERNEL_TENSOR",
-    "HWKV_KERNEL_SIMT", "hwkv_abi_version", "hwkv_append", "hwkv_append_decode_attn", "hwkv_block_table",
+    "HWKV_KERNEL_SIMT", "hwkv_abi_version", "hwkv_advance_positions", "hwkv_append", "hwkv_append_decode_attn", "hwkv_block_table",
     "hwkv_check_device_errors", "hwkv_kernel_launches",
     "hwkv_decode_attn", "hwkv_decode_workspace_bytes", "hwkv_materialize", "hwkv_pool_bytes", "hwkv_pool_create",
     "hwkv_pool_destroy", "hwkv_pool_geometry", "hwkv_prefill_attn", "hwkv_prefill_plan", "hwkv_prefill_workspace_bytes",
@@ -130,6 +130,12 @@ class Pool:
 
     def set_prefill_config(self, max_stages: int = 0):
         hwkv_set_prefill_config(self.handle, max_stages)
+
+    def advance_positions(self, pos, out=None, delta: int = 1, stream=None):
+        """out = pos + delta on the device with a library kernel (in place when out is None)."""
+        out = pos if out is None else out
+        hwkv_advance_positions(self.handle, pos, out, delta, stream)
+        return out
 
     def check_device_errors(self, stream=None) -> int:
         return hwkv_check_device_errors(self.handle, stream)

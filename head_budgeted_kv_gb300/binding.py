@@ -55,6 +55,7 @@ SIGNATURES = [
     ("hwkv_set_block_table", _i, [_vp, _c_i32p, _i64, _vp]),
     ("hwkv_materialize", _i, [_vp, _i, _vp, _vp, _i64, _i64, _i64, _vp, _vp]),
     ("hwkv_append", _i, [_vp, _i, _vp, _vp, _vp, _vp]),
+    ("hwkv_advance_positions", _i, [_vp, _vp, _vp, ctypes.c_int32, _vp]),
     ("hwkv_decode_workspace_bytes", _i, [_vp, _i, _c_u64p]),
     ("hwkv_decode_attn", _i, [_vp, _i, _vp, _i, ctypes.c_float, _vp, _vp, _vp, _u64, _vp]),
     ("hwkv_append_decode_attn", _i, [_vp, _i, _vp, _i, ctypes.c_float, _vp, _vp, _vp, _vp, _vp, _u64, _vp]),
@@ -212,6 +213,13 @@ def hwkv_append(pool: int, layer: int, k_new: torch.Tensor, v_new: torch.Tensor,
     if not (k_new.is_contiguous() and v_new.is_contiguous()):
         raise ValueError("k_new and v_new must be contiguous")
     _check(load().hwkv_append(pool, layer, _ptr(k_new), _ptr(v_new), _ptr(pos), _stream_ptr(stream)))
+
+
+def hwkv_advance_positions(pool: int, pos: torch.Tensor, out: torch.Tensor, delta: int = 1, stream=None):
+    """out[s] = pos[s] + delta on the device (int32 [num_seqs]; out may be pos)."""
+    if pos.dtype != torch.int32 or out.dtype != torch.int32:
+        raise ValueError("positions must be int32")
+    _check(load().hwkv_advance_positions(pool, _ptr(pos), _ptr(out), int(delta), _stream_ptr(stream)))
 
 
 def hwkv_decode_workspace_bytes(pool: int, q_heads: int) -> int:

@@ -123,7 +123,20 @@ __global__ void __launch_bounds__(kMatThreads) materialize_kernel(const __grid_c
   }
 }
 
+// One thread per sequence: out[s] = in[s] + delta, in unsigned arithmetic (a wrapped value is
+// negative and flagged by the kernels that read it as a length or position).
+__global__ void __launch_bounds__(256) advance_positions_kernel(const int32_t* in, int32_t* out, int n, int32_t delta) {
+  const int i = (int)(blockIdx.x * blockDim.x + threadIdx.x);
+  if (i < n) out[i] = (int32_t)((uint32_t)in[i] + (uint32_t)delta);
+}
+
 }  // namespace
+
+cudaError_t launch_advance_positions(const int32_t* in, int32_t* out, int n, int32_t delta, cudaStream_t st) {
+  advance_positions_kernel<<<(n + 255) / 256, 256, 0, st>>>(in, out, n, delta);
+  count_launches(1);
+  return cudaGetLastError();
+}
 
 cudaError_t launch_append(const CopyArgs& a, int dtype, cudaStream_t st) {
   const uint32_t row_bytes = (uint32_t)a.pv.head_dim * (dtype == HWKV_F32 ? 4u : 2u);

@@ -6,6 +6,7 @@
 // pre-allocated before serving) and abstract (the footprint is exact before serving).
 // Physical block ids start as the identity in (layer, seq, kv head, logical block) order.
 #include <cudaTypedefs.h>
+#include <nvtx3/nvToolsExt.h>
 
 #include <algorithm>
 #include <atomic>
@@ -45,6 +46,31 @@ int ok() {
   g_last_error.clear();
   return HWKV_OK;
 }
+
+// NVTX range of one library call, in the "hwkv" domain, with the layer as its payload, so a
+// profile of a serving step attributes each append / decode / prefill launch to its call.
+// Without a profiler attached a push or pop is a check of one function pointer.
+nvtxDomainHandle_t nvtx_domain() {
+  static nvtxDomainHandle_t d = nvtxDomainCreateA("hwkv");
+  return d;
+}
+
+struct NvtxRange {
+  explicit NvtxRange(const char* name, int layer) {
+    nvtxEventAttributes_t ev;
+    std::memset(&ev, 0, sizeof ev);
+    ev.version = NVTX_VERSION;
+    ev.size = NVTX_EVENT_ATTRIB_STRUCT_SIZE;
+    ev.messageType = NVTX_MESSAGE_TYPE_ASCII;
+    ev.message.ascii = name;
+    ev.payloadType = NVTX_PAYLOAD_TYPE_INT32;
+    ev.payload.iValue = layer;
+    nvtxDomainRangePushEx(nvtx_domain(), &ev);
+  }
+  ~NvtxRange() { nvtxDomainRangePop(nvtx_domain()); }
+  NvtxRange(const NvtxRange&) = delete;
+  NvtxRange& operator=(const NvtxRange&) = delete;
+};
 
 #define HWKV_CUDA_TRY(expr, what)                                                           \
   do {                                                                                     \
@@ -671,6 +697,7 @@ int hwkv_materialize(hwkv_pool_t p, int layer, const void* k_full, const void* v
   if (max_len > kInt32Max) return fail(HWKV_ERR_INVALID_ARG, "max_len must be below 2^31");
   int rc = check_device(p);
   if (rc != HWKV_OK) return rc;
+  NvtxRange range_("hwkv_materialize", layer);
   CopyArgs a;
   std::memset(&a, 0, sizeof a);
   a.pv = pool_view(p);
@@ -698,6 +725,7 @@ int hwkv_append(hwkv_pool_t p, int layer, const void* k_new, const void* v_new, 
     return fail(HWKV_ERR_ALIGNMENT, "k_new / v_new must be 16-byte aligned, pos 4-byte aligned");
   int rc = check_device(p);
   if (rc != HWKV_OK) return rc;
+  NvtxRange range_("hwkv_append", layer);
   CopyArgs a;
   std::memset(&a, 0, sizeof a);
   a.pv = pool_view(p);
@@ -706,6 +734,17 @@ int hwkv_append(hwkv_pool_t p, int layer, const void* k_new, const void* v_new, 
   a.v = v_new;
   a.lens = pos_dev;
   HWKV_CUDA_TRY(launch_append(a, g.dtype, static_cast<cudaStream_t>(stream)), "append launch");
+  return ok();
+}
+
+int hwkv_advance_positions(hwkv_pool_t p, const int32_t* pos_dev, int32_t* out_dev, int32_t delta, void* stream) {
+  if (!p) return fail(HWKV_ERR_INVALID_ARG, "pool is NULL");
+  if (!pos_dev || !out_dev) return fail(HWKV_ERR_INVALID_ARG, "NULL tensor argument");
+  if (!aligned(pos_dev, 4) || !aligned(out_dev, 4)) return fail(HWKV_ERR_ALIGNMENT, "positions must be 4-byte aligned");
+  int rc = check_device(p);
+  if (rc != HWKV_OK) return rc;
+  HWKV_CUDA_TRY(launch_advance_positions(pos_dev, out_dev, p->g.num_seqs, delta, static_cast<cudaStream_t>(stream)),
+                "advance-positions launch");
   return ok();
 }
 
@@ -754,6 +793,7 @@ int decode_common(hwkv_pool_t p, int layer, const void* q, int q_heads, float sc
   }
   int rc = check_device(p);
   if (rc != HWKV_OK) return rc;
+  NvtxRange range_(len_add ? "hwkv_append_decode_attn" : "hwkv_decode_attn", layer);
   if (p->kernel_choice == HWKV_KERNEL_TENSOR && !tc_eligible(p))
     return fail(HWKV_ERR_UNSUPPORTED, "tensor-core decode needs bf16 and block_size % 16 == 0");
 
@@ -897,6 +937,7 @@ int hwkv_prefill_attn(hwkv_pool_t p, int layer, const void* q, int q_heads, floa
     return fail(HWKV_ERR_ALIGNMENT, "tensors and workspace must be 16-byte aligned, lengths 4-byte aligned");
   int rc = check_device(p);
   if (rc != HWKV_OK) return rc;
+  NvtxRange range_("hwkv_prefill_attn", layer);
   PFN_cuTensorMapEncodeTiled_v12000 encode = tensor_map_encoder();
   if (!encode) return fail(HWKV_ERR_CUDA, "cuTensorMapEncodeTiled is unavailable");
   // the chunk as a 3-D tensor (head_dim, kv_heads, seq * n_max + row): boxes of 16 and of 64

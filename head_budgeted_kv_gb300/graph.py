@@ -5,8 +5,9 @@ only on the pool's static geometry, nothing is allocated inside a call, and the 
 kernel launches as a programmatic dependent so consecutive layers keep their overlap inside
 the graph.  ``DecodeStepGraph`` records, for every layer, the append of the new token and the
 windowed attention (``hwkv_append_decode_attn``, or ``hwkv_append`` + ``hwkv_decode_attn``),
-followed by the advance of the positions, and replays that whole step with one launch from
-the host.  Inputs are read from, and outputs written to, the static buffers it owns.
+followed by the advance of the positions (``hwkv_advance_positions``), and replays that whole
+step with one launch from the host: every kernel of a replayed step is the library's.
+Inputs are read from, and outputs written to, the static buffers it owns.
 """
 from __future__ import annotations
 
@@ -50,7 +51,7 @@ class DecodeStepGraph:
     def _record(self):
         p = self.pool
         if not self.fused:
-            torch.add(self.pos, 1, out=self.lens)
+            p.advance_positions(self.pos, out=self.lens)  # lengths after the append
         for l in range(p.layers):
             if self.fused:
                 # after layer 0 the kernel just before is the previous layer's attention, which
@@ -60,7 +61,7 @@ class DecodeStepGraph:
             else:
                 p.append(l, self.k_new[l], self.v_new[l], self.pos)
                 p.decode(l, self.q[l], self.scale, self.lens, out=self.out[l])
-        self.pos.add_(1)
+        p.advance_positions(self.pos)  # the next step's positions
 
     def replay(self):
         self.graph.replay()

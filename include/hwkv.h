@@ -146,6 +146,14 @@ int hwkv_materialize(hwkv_pool_t pool, int layer, const void* k_full, const void
 int hwkv_append(hwkv_pool_t pool, int layer, const void* k_new, const void* v_new, const int32_t* pos_dev,
                 void* stream);
 
+/* Position bookkeeping of a serving loop, on the device: out_dev[s] = pos_dev[s] + delta for the
+ * pool's num_seqs sequences (int32, wrapping; out_dev may be pos_dev).  It lets a decode step
+ * captured in a CUDA graph advance its positions after the step (delta 1), or form the lengths
+ * after the append from the positions before it, without a kernel from outside this library.
+ * The pages have no counterpart: this is a service of this library, not a step of the method.
+ *   pos_dev, out_dev: device int32 [num_seqs], 4-byte aligned.  One kernel on `stream`. */
+int hwkv_advance_positions(hwkv_pool_t pool, const int32_t* pos_dev, int32_t* out_dev, int32_t delta, void* stream);
+
 /* Bytes of scratch hwkv_decode_attn / hwkv_append_decode_attn need for the current decode
  * configuration (fp32 split-K partials; maximum over layers). */
 int hwkv_decode_workspace_bytes(hwkv_pool_t pool, int q_heads, uint64_t* out);

@@ -89,10 +89,11 @@ class Run:
         self.steps_done += 1
         return res
 
-    def run_prepared(self, keep_steps: Iterable[int], keep_layers: Iterable[int]):
+    def run_prepared(self, keep_steps: Iterable[int] = (), keep_layers: Iterable[int] = (), pairs=None):
         """All remaining steps as the decode benchmark issues them: every step's inputs and
         positions prepared first, then one prepared fused launch per layer with early reads,
-        back to back with no host synchronisation.  Returns {(step, layer): (q raw, out)}."""
+        back to back with no host synchronisation.  Returns {(step, layer): (q raw, out)} for
+        keep_steps x keep_layers, or for the (step, layer) pairs given."""
         cfg = self.cfg
         first = self.steps_done
         steps = range(first, cfg.steps)
@@ -113,10 +114,10 @@ class Run:
         torch.cuda.synchronize()
         self.steps_done = cfg.steps
         res = {}
-        for i in keep_steps:
-            for l in keep_layers:
-                res[(i, l)] = (workloads.to_raw(inputs[i - first][0][l]),
-                               outs[i - first, l].float().cpu().double().numpy())
+        want = sorted(pairs) if pairs is not None else [(i, l) for i in keep_steps for l in keep_layers]
+        for i, l in want:
+            res[(i, l)] = (workloads.to_raw(inputs[i - first][0][l]),
+                           outs[i - first, l].float().cpu().double().numpy())
         return res
 
     def device_errors(self) -> int:
@@ -152,6 +153,39 @@ class Run:
         if seqs is None:
             return oracle.attention_jobs(q_raw, hist, lens, cfg.windows[layer], cfg.scale)
         lens_used = [lens[s] if s in seqs else 0 for s in range(cfg.batch)]
+        return oracle.attention_jobs(q_raw, hist, lens_used, cfg.windows[layer], cfg.scale)
+
+    def layer_histories(self, layer: int, seqs=None) -> dict:
+        """Host rows of every (seq, kv head) of ``layer`` covering the windows of all steps done:
+        {(s, h): (p_lo, K rows, V rows)} from the oldest position any step's window holds to the
+        newest appended one (drawn once, then sliced per step by ``reference_hoisted``)."""
+        cfg = self.cfg
+        out = {}
+        for s in range(cfg.batch):
+            if seqs is not None and s not in seqs:
+                continue
+            hi = cfg.prefill[s] + self.steps_done
+            for h in range(cfg.kv_heads):
+                lo, _ = oracle.window_span(cfg.prefill[s] + 1, int(cfg.windows[layer][h]))
+                hk, hv = self.history(layer, s, h, lo, hi)
+                out[(s, h)] = (lo, hk, hv)
+        return out
+
+    def reference_hoisted(self, hist_all: dict, step: int, layer: int, q_raw: np.ndarray, seqs=None) -> np.ndarray:
+        """As ``reference``, with each head's rows sliced out of ``layer_histories``."""
+        cfg = self.cfg
+        lens = [cfg.prefill[s] + step + 1 for s in range(cfg.batch)]
+        hist = {}
+        empty = workloads.to_raw(torch.zeros((0, cfg.head_dim), dtype=cfg.torch_dtype))
+        for s in range(cfg.batch):
+            for h in range(cfg.kv_heads):
+                lo, hi = oracle.window_span(lens[s], int(cfg.windows[layer][h]))
+                if seqs is not None and s not in seqs:
+                    hist[(s, h)] = (hi, empty, empty)
+                    continue
+                p_lo, hk, hv = hist_all[(s, h)]
+                hist[(s, h)] = (lo, hk[lo - p_lo:hi - p_lo], hv[lo - p_lo:hi - p_lo])
+        lens_used = lens if seqs is None else [lens[s] if s in seqs else 0 for s in range(cfg.batch)]
         return oracle.attention_jobs(q_raw, hist, lens_used, cfg.windows[layer], cfg.scale)
 
     def expected_ring_blocks(self, l, s, h):

@@ -130,3 +130,34 @@ def test_prepared_launch_equals_plain_calls_bit_for_bit():
         run.close()
     assert torch.equal(results[0][0], results[1][0])
     assert torch.equal(results[0][1], results[1][1])
+
+
+def test_advance_positions_in_place_out_of_place_and_wrapping():
+    windows = np.full((1, 2), 32, dtype=np.int32)
+    pool = hw.Pool(1, 2, 64, 16, windows, 5, torch.bfloat16)
+    pos = torch.tensor([0, 7, 2**31 - 1, -3, 1000], dtype=torch.int32, device="cuda")
+    out = torch.full_like(pos, 12345)
+    before = hw.binding.hwkv_kernel_launches()
+    pool.advance_positions(pos, out=out)
+    pool.advance_positions(pos, delta=-2)
+    torch.cuda.synchronize()
+    assert hw.binding.hwkv_kernel_launches() - before == 2
+    assert out.cpu().tolist() == [1, 8, -2**31, -2, 1001]
+    assert pos.cpu().tolist() == [-2, 5, 2**31 - 3, -5, 998]
+    pool.close()
+
+
+def test_replayed_step_launches_only_library_kernels():
+    """Every kernel a captured step records is counted by the library: one per layer and the
+    position advance (fused path)."""
+    cfg = small_config(name="graph_count", layers=2, kv_heads=2, windows=((64, 512), (256, 32)), prefill=(300,),
+                       steps=1)
+    run = Run(cfg)
+    run.materialize()
+    before = hw.binding.hwkv_kernel_launches()
+    g = DecodeStepGraph(run.pool, cfg.scale, cfg.q_heads, run.prefill, fused=True)
+    assert hw.binding.hwkv_kernel_launches() - before == cfg.layers + 1
+    g.replay()
+    torch.cuda.synchronize()
+    assert g.pos.cpu().tolist() == [cfg.prefill[0] + 1]
+    run.close()
