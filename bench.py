@@ -251,28 +251,53 @@ def oracle_sample(cfg, wl, budget_s: float, device, layers_order=None, step: int
 # --------------------------------------------------------------------------------------
 # reference arm: the oracle timed on the host cores
 # --------------------------------------------------------------------------------------
+def oracle_whole_step(cfg, wl, step: int, steps_in, device, threads: int) -> float:
+    """Seconds of fp64 oracle time for every layer (all sequences and query heads) of decode
+    step ``step``; ``steps_in`` holds the host inputs of steps 0 .. step (the appended tokens
+    are part of the windows).  The host copies of each layer's windows are drawn untimed."""
+    import oracle
+    import workloads
+    lens = [cfg.prefill[s] + step + 1 for s in range(cfg.batch)]
+    spent = 0.0
+    for l in range(cfg.layers):
+        hist = {}
+        for s in range(cfg.batch):
+            k, v = wl.prefill_seq(l, s, device)
+            for h in range(cfg.kv_heads):
+                lo, hi = oracle.window_span(lens[s], int(cfg.windows[l][h]))
+                hk, hv = wl.history(l, s, h, lo, hi, prefill=(k, v), steps=steps_in)
+                hist[(s, h)] = (lo, hk, hv)
+            del k, v
+        q = workloads.to_raw(steps_in[step][0][l])
+        t0 = time.perf_counter()
+        oracle.attention_jobs(q, hist, lens, cfg.windows[l], cfg.scale, threads=threads)
+        spent += time.perf_counter() - t0
+    return spent
+
+
 def run_reference(args, cfg):
+    """The reference arm: the fp64 oracle on the host cores, K whole decode steps (every layer,
+    sequence and query head of steps W .. W+K-1), each timed; the W warm-up steps run layer 0
+    of steps 0 .. W-1 untimed."""
     ws, rank, local = dist_env()
     if rank != 0:
         return
     import torch
+    import oracle
     import workloads
     device = torch.device("cuda", local) if torch.cuda.is_available() else torch.device("cpu")
     wl = workloads.Workload(cfg, device="cpu" if cfg.single_cpu_stream or device.type == "cpu" else device)
-    times, per_layer = [], []
-    total_steps = args.warmup + args.steps
-    threads = None
-    for i in range(total_steps):
-        l = i % cfg.layers
-        t, done, threads = oracle_sample(cfg, wl, budget_s=0.0, device=device, layers_order=[l], max_layers=1)
-        if i >= args.warmup:
-            times.append(t)
-            per_layer.append(l)
-    mean_layer_s = float(np.mean(times))
-    step_s = mean_layer_s * cfg.layers
+    threads = oracle.default_threads()
+    total = args.warmup + args.steps
+    steps_in = [tuple(t.cpu() for t in wl.step_inputs(i, device)) for i in range(total)]
+    one_layer = cfg.with_layers(1)
+    for i in range(args.warmup):
+        oracle_whole_step(one_layer, wl, i, steps_in, device, threads)
+    times = [oracle_whole_step(cfg, wl, args.warmup + k, steps_in, device, threads) for k in range(args.steps)]
+    step_s = float(np.mean(times))
     value = cfg.batch / step_s
-    sample = (f"one whole layer (all {cfg.batch} seqs x {cfg.q_heads} q heads, full resident windows) of decode "
-              f"step 0 per timed step, layers cycled; per-step time = mean layer time x {cfg.layers} layers")
+    sample = (f"{args.steps} whole decode steps (all {cfg.layers} layers x {cfg.batch} seqs x {cfg.q_heads} q heads, "
+              f"full resident windows), each timed; {sum(times):.1f} s of fp64 oracle time on {threads} threads")
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": ws,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": step_s * 1e3, "higher_is_better": True,
@@ -506,7 +531,7 @@ def run_hwkv(args, cfg):
             for l in range(cfg.layers):
                 pool.append_decode(l, d_q[l], cfg.scale, d_k[l], d_v[l], d_pos, out=d_out[l], early_reads=early)
         else:
-            torch.add(d_pos, 1, out=d_lens)
+            pool.advance_positions(d_pos, out=d_lens)
             for l in range(cfg.layers):
                 pool.append(l, d_k[l], d_v[l], d_pos)
                 pool.decode(l, d_q[l], cfg.scale, d_lens, out=d_out[l])
@@ -537,12 +562,21 @@ def run_hwkv(args, cfg):
                "sample": f"{done} of {cfg.layers} layers (all seqs and q heads) of decode step 0, "
                          f"{spent:.1f} s of fp64 oracle time; per-step time scaled by {cfg.layers}/{done}"}
 
+    pool_nbytes = pool.nbytes
+    use_graph = graph is not None
+    pool.close()
     if rank != 0:
-        pool.close()
         return
     peak, peak_kind = measured_peak()
+    secondary = None
+    if args.secondary and ws == 1:
+        # the headline workload's buffers go first: the ragged pool alone is 91 GB
+        del pool, graph, qs, kns, vns, outs, launchers, d_in, d_outs, h_q, h_k, h_v, h_out
+        gc.collect()
+        torch.cuda.empty_cache()
+        secondary = secondary_block(args, dev, stream, peak)
     isolated = dec_bytes / (dec_ms / 1e3) / 1e9  # launches separated by events: no overlap
-    if fused and graph is None:
+    if fused and not use_graph:
         # every launch of the timed region is the decode kernel: its average duration there is
         # the timed region over the launches (consecutive launches overlap by design)
         achieved = timed_dec_bytes / (local_ms / 1e3) / 1e9
@@ -577,10 +611,87 @@ def run_hwkv(args, cfg):
         "clocks": clock_info,
         "materialize": {"gbs": mat_bytes / (mat_ms / 1e3) / 1e9, "ms": mat_ms, "bytes": mat_bytes,
                         "frac": mat_bytes / (mat_ms / 1e3) / 1e9 / peak},
-        "pool_bytes": pool.nbytes,
+        "pool_bytes": pool_nbytes,
+        "secondary": secondary,
     }
-    pool.close()
     print(json.dumps(line), flush=True)
+
+
+# --------------------------------------------------------------------------------------
+# secondary workloads of the default line: short timed regions in the same run
+# --------------------------------------------------------------------------------------
+SECONDARY = ("ragged", "long", "long_full")
+
+
+def measure_secondary(name: str, args, dev, stream, peak: float) -> dict:
+    """Materialises workload ``name`` into its own pool and times ``steps`` fused decode steps
+    (every layer, prepared launches with early reads, as the headline line) after ``warmup``
+    untimed ones.  The pool and inputs are freed before returning."""
+    import torch
+    import workloads
+    import head_budgeted_kv_gb300 as hw
+    cfg = workloads.config(name)
+    warmup = args.warmup
+    steps = max(1, min(args.steps, cfg.steps - warmup))
+    wl = workloads.Workload(cfg, device=dev)
+    pool = hw.Pool(cfg.layers, cfg.kv_heads, cfg.head_dim, cfg.block_size, cfg.windows_array(), cfg.batch,
+                   cfg.torch_dtype, q_heads=cfg.q_heads, device=dev)
+    prefill = torch.tensor(cfg.prefill, dtype=torch.int32, device=dev)
+    for l in range(cfg.layers):
+        K, V = wl.prefill_layer(l, dev)
+        pool.materialize(l, K, V, prefill)
+        del K, V
+    torch.cuda.synchronize()
+    torch.cuda.empty_cache()
+    total = warmup + steps
+    inputs = [wl.step_inputs(i, dev) for i in range(total)]
+    pos_all = [(prefill + i).contiguous() for i in range(total)]
+    outs = torch.empty((cfg.layers, cfg.batch, cfg.q_heads, cfg.head_dim), dtype=cfg.torch_dtype, device=dev)
+    launchers = [[pool.decode_launch(l, inputs[i][0][l], cfg.scale, pos_all[i], outs[l], inputs[i][1][l],
+                                     inputs[i][2][l], early_reads=True) for l in range(cfg.layers)]
+                 for i in range(total)]
+    torch.cuda.synchronize()
+    for i in range(warmup):
+        for launch in launchers[i]:
+            launch()
+    torch.cuda.synchronize()
+    clocks = ClockSampler(torch.cuda.current_device())
+    clocks.start()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    launches0 = hw.binding.hwkv_kernel_launches()
+    clocks.mark_start()
+    e0.record(stream)
+    for i in range(warmup, total):
+        for launch in launchers[i]:
+            launch()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    clocks.mark_end()
+    launches = hw.binding.hwkv_kernel_launches() - launches0
+    clock_info = clocks.stop()
+    ms = e0.elapsed_time(e1)
+    bits = pool.check_device_errors()
+    pool.close()
+    del pool, inputs, pos_all, outs, launchers
+    torch.cuda.empty_cache()
+    if bits:
+        raise RuntimeError(f"device error bits {bits:#x} in the {name} workload")
+    step_bytes = mean_step_bytes(cfg, warmup, steps)
+    gbs = step_bytes / (ms / steps / 1e3) / 1e9
+    return {"workload": workload_desc(cfg), "steps": steps, "warmup": warmup, "ms_per_step": ms / steps,
+            "tokens_per_s": cfg.batch * steps / (ms / 1e3), "bytes_per_step": step_bytes, "resident_kv_gbs": gbs,
+            "frac": gbs / peak, "peak": peak, "gpu_launches": launches, "clocks": clock_info}
+
+
+def secondary_block(args, dev, stream, peak: float) -> dict:
+    out = {}
+    for name in args.secondary:
+        out[name] = measure_secondary(name, args, dev, stream, peak)
+    if "long" in out and "long_full" in out:
+        w, f = out["long"], out["long_full"]
+        out["long_full"]["vs_long"] = {"bytes_ratio": f["bytes_per_step"] / w["bytes_per_step"],
+                                       "tokens_per_s_ratio": w["tokens_per_s"] / f["tokens_per_s"]}
+    return out
 
 
 # --------------------------------------------------------------------------------------
@@ -797,6 +908,9 @@ def main(argv=None):
     p.add_argument("--no-early-reads", action="store_true",
                    help="decode without HWKV_DECODE_EARLY_READS (schedule waits for the previous launch)")
     p.add_argument("--cpu-budget", type=float, default=12.0)
+    p.add_argument("--secondary", default="auto",
+                   help="comma-separated workloads timed after the headline one in the same run ('none' to skip; "
+                        "'auto': ragged,long,long_full for the default full-workload decode line)")
     args = p.parse_args(argv)
     if args.warmup < 3:
         raise SystemExit("--warmup must be >= 3")
@@ -804,6 +918,16 @@ def main(argv=None):
     cfg = workloads.config(args.workload)
     if args.layers:
         cfg = cfg.with_layers(args.layers)
+    if args.secondary == "auto":
+        default_line = (args.workload == "full" and not args.layers and args.path == "fused" and not args.graph
+                        and not args.kernel and not args.workers and not args.split and not args.no_early_reads)
+        args.secondary = list(SECONDARY) if default_line else []
+    elif args.secondary == "none":
+        args.secondary = []
+    else:
+        args.secondary = [n for n in args.secondary.split(",") if n]
+        for n in args.secondary:
+            workloads.config(n)  # unknown names fail here
     if args.impl == "reference":
         run_reference(args, cfg)
     elif args.mode == "prefill":

@@ -83,3 +83,38 @@ def test_reference_arm_line_on_cpu(monkeypatch, capsys):
     line = json.loads(capsys.readouterr().out.strip())
     assert line["impl"] == "reference" and line["value"] > 0
     assert line["cpu_baseline"]["kind"] == "oracle" and line["e2e"]["h2d_bytes_per_step"] == 0
+
+
+def test_reference_arm_times_whole_steps(monkeypatch, capsys):
+    """Each timed step of the reference arm is a whole decode step (every layer), so the line's
+    ms_per_step x steps is oracle time actually spent."""
+    import json
+    monkeypatch.delenv("RANK", raising=False)
+    monkeypatch.delenv("WORLD_SIZE", raising=False)
+    calls = []
+    real = bench.oracle_whole_step
+
+    def spy(cfg, wl, step, steps_in, device, threads):
+        calls.append((cfg.layers, step))
+        return real(cfg, wl, step, steps_in, device, threads)
+
+    monkeypatch.setattr(bench, "oracle_whole_step", spy)
+    bench.main(["--impl", "reference", "--workload", "tiny", "--steps", "2", "--warmup", "3"])
+    line = json.loads(capsys.readouterr().out.strip())
+    assert line["steps"] == 2 and line["warmup"] == 3
+    cfg = workloads.config("tiny")
+    assert calls[3:] == [(cfg.layers, 3), (cfg.layers, 4)]
+    assert "2 whole decode steps" in line["cpu_baseline"]["sample"]
+
+
+def test_secondary_workloads_default_only_for_the_headline_line(monkeypatch):
+    seen = {}
+    monkeypatch.setattr(bench, "run_hwkv", lambda args, cfg: seen.setdefault("sec", args.secondary))
+    bench.main(["--steps", "1", "--warmup", "3"])
+    assert seen.pop("sec") == ["ragged", "long", "long_full"]
+    bench.main(["--steps", "1", "--warmup", "3", "--workload", "long"])
+    assert seen.pop("sec") == []
+    bench.main(["--steps", "1", "--warmup", "3", "--secondary", "none"])
+    assert seen.pop("sec") == []
+    with pytest.raises(KeyError):
+        bench.main(["--steps", "1", "--warmup", "3", "--secondary", "nosuch"])
