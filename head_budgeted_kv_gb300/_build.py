@@ -19,7 +19,8 @@ LIB = os.path.join(BUILD, "libhwkv.so")
 
 SOURCES = ("hwkv_host.cpp", "hwkv_copy.cu", "hwkv_decode_simt.cu", "hwkv_decode_tc.cu", "hwkv_noalloc.cu", "hwkv_prefill.cu")
 HEADERS = (os.path.join(CSRC, "hwkv_internal.h"), os.path.join(CSRC, "hwkv_device.cuh"),
-           os.path.join(CSRC, "hwkv_tcgen05.cuh"), os.path.join(INCLUDE, "hwkv.h"))
+           os.path.join(CSRC, "hwkv_tcgen05.cuh"), os.path.join(CSRC, "hwkv_decode_tile.cuh"),
+           os.path.join(INCLUDE, "hwkv.h"))
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-I", INCLUDE, "-I", CSRC]
 

@@ -29,53 +29,12 @@
 //   loaded once with ldmatrix.trans).
 //
 // Waits are bounded (~2 s); a timeout records HWKV_DEVERR_WAIT_TIMEOUT and the warp stops.
-#include "hwkv_device.cuh"
+#include "hwkv_decode_tile.cuh"
 
 namespace hwkv {
 namespace {
 
-constexpr int kWarps = 4;
 constexpr int kFlatMerge = 24;  // most contributors one CTA merges directly
-
-// One (seq, kv head) group at this step: its resident window and needed tiles.
-struct Group {
-  int s, h;
-  int len;         // length after the append
-  Resident rs;     // resident slots
-  int C16;         // ring capacity in tiles
-  int t_first;     // tile of the oldest resident slot
-  int tiles;       // needed tiles, cyclically from t_first
-  const int32_t* tbl;
-};
-
-constexpr int kLensCache = 256;  // sequence lengths a CTA stages in shared memory
-
-// length of sequence s after the append, clamped at 0
-__device__ __forceinline__ int seq_len(const DecodeArgs& a, int s) {
-  const int len = __ldcg(a.lens + s) + a.len_add;  // L2: may be read before the dependent-launch wait
-  return len < 0 ? 0 : len;
-}
-
-// Group g; its sequence length comes from `s_lens` (shared memory) when that is non-null.
-__device__ __forceinline__ Group load_group(const DecodeArgs& a, const int* s_lens, int g) {
-  Group gr;
-  const int H = a.pv.kv_heads;
-  gr.s = g / H;
-  gr.h = g - gr.s * H;
-  gr.len = s_lens != nullptr ? s_lens[gr.s] : seq_len(a, gr.s);
-  const int C = (a.g.nblk_prefix[gr.h + 1] - a.g.nblk_prefix[gr.h]) * a.pv.block_size;
-  gr.rs = resident(gr.len, a.g.window[gr.h], C);
-  gr.C16 = C >> 4;
-  gr.t_first = gr.rs.first_slot >> 4;
-  if (gr.rs.n > 0) {
-    const uint32_t last = (uint32_t)gr.rs.first_slot + (uint32_t)gr.rs.n - 1u;
-    gr.tiles = min(gr.C16, (int)(last >> 4) - gr.t_first + 1);
-  } else {
-    gr.tiles = 0;
-  }
-  gr.tbl = a.pv.tbl + a.g.tbl_base + (int64_t)gr.s * a.g.tbl_seq_stride + a.g.nblk_prefix[gr.h];
-  return gr;
-}
 
 // Line positions charged for each group's boundary.  A group with tiles spans kGapTiles
 // positions that hold no tile, then its tiles; a CTA whose range takes in a group's start thus
@@ -97,49 +56,6 @@ __host__ __device__ constexpr int l2_prefetch() {
 constexpr int kL2PrefetchMin = 64;
 
 __device__ __forceinline__ int group_span(const Group& gr) { return gr.tiles > 0 ? gr.tiles + kGapTiles : 0; }
-
-// ring slot of the first token of the i-th needed tile of a group
-__device__ __forceinline__ int tile_slot(const Group& gr, long long i) {
-  int t = gr.t_first + (int)i;
-  if (t >= gr.C16) t -= gr.C16;
-  return t << 4;
-}
-
-// first tile of CTA c when T tiles are split over n CTAs
-__device__ __forceinline__ long long range_start(long long T, int c, int n) { return T * c / n; }
-
-// CTA whose range holds tile t
-__device__ __forceinline__ int cta_of(long long t, long long T, int n) { return (int)(((t + 1) * n - 1) / T); }
-
-// Byte offset of element (row, d) of a 16-row tile stored as D/64 TMA boxes of [16 rows][64
-// elements] with the 128-byte swizzle: box hf = d / 64 at hf * 2048; inside a box row r is
-// the 128-byte line r and its 16-byte chunk c sits at chunk c ^ (r % 8).
-__device__ __forceinline__ uint32_t swz(int row, int d) {
-  return (uint32_t)((d >> 6) * 2048 + row * 128 + ((((d & 63) >> 3) ^ (row & 7)) << 4) + (d & 7) * 2);
-}
-
-template <int W>
-__device__ __forceinline__ long long block_exclusive_scan(long long v, long long* s_warp, long long& total) {
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  long long x = v;
-#pragma unroll
-  for (int off = 1; off < 32; off <<= 1) {
-    const long long y = __shfl_up_sync(0xffffffffu, x, off);
-    if (lane >= off) x += y;
-  }
-  if (lane == 31) s_warp[warp] = x;
-  __syncthreads();
-  long long base = 0, tot = 0;
-#pragma unroll
-  for (int w = 0; w < W; ++w) {
-    const long long sw = s_warp[w];
-    if (w < warp) base += sw;
-    tot += sw;
-  }
-  total = tot;
-  __syncthreads();
-  return base + x - v;
-}
 
 // Writes a merged (M, L, acc) of query head q, columns 4*d4 .. 4*d4 + 3: normalised to the bf16
 // output `out_grp` when it is non-null, else unnormalised to partial slot `dst_slot`.
@@ -335,11 +251,9 @@ template <int D, int GP, int NS>
 __global__ void __launch_bounds__(kWarps * 32, D == 64 ? 3 : 2) decode_sk_kernel(const __grid_constant__ CUtensorMap tmap,
                                                                 const __grid_constant__ DecodeArgs a) {
   constexpr int W = kWarps;
-  constexpr int kHalves = D / 64;
   constexpr int kTileBytes = kTile * D * 2;    // 16 rows of bf16
   constexpr int kStageBytes = 2 * kTileBytes;  // K tile + V tile
   constexpr int kSteps = D / 16;               // k-steps of QK, m-tiles of PV
-  constexpr int kRowVecs = D * 2 / 16;         // 16-byte vectors per row
   constexpr int NT = (GP + 7) / 8;             // 8-column n-tiles of query heads
   constexpr int SG = merge_heads<D, GP>();      // query heads merged per pass in shared memory
   constexpr int kPasses = GP < 8 ? 1 : 8 / SG;  // passes per 8-column n-tile
@@ -452,24 +366,9 @@ __global__ void __launch_bounds__(kWarps * 32, D == 64 ? 3 : 2) decode_sk_kernel
     }
     if (lane == issuer) {
       const int st = issued % NS;
-      const int t0 = tile_slot(igr, j_issue - ipre - kGapTiles);
-      const int jb = t0 / bs;
-      const int r0 = t0 - jb * bs;
       // the first stages may be issued before the dependent-launch wait: read through L2
-      int32_t blk = issued < NS ? __ldcg(igr.tbl + jb) : igr.tbl[jb];
-      if (blk < 0 || (int64_t)blk >= a.pv.total_blocks) {
-        atomicOr(a.pv.err, HWKV_DEVERR_BAD_BLOCK);
-        blk = 0;  // keep the barrier accounting intact; the result is flagged
-      }
-      const int row_k = blk * 2 * bs + r0;
-      const int row_v = row_k + bs;
-      const uint32_t dst = wstage + st * kStageBytes;
-      mbar_arrive_expect_tx(&wbar[st], kStageBytes);
-#pragma unroll
-      for (int hf = 0; hf < kHalves; ++hf) {
-        tma_load_2d(dst + hf * 2048, &tmap, hf * 64, row_k, &wbar[st], policy);
-        tma_load_2d(dst + kTileBytes + hf * 2048, &tmap, hf * 64, row_v, &wbar[st], policy);
-      }
+      issue_tile<D>(&tmap, a, igr, tile_slot(igr, j_issue - ipre - kGapTiles), wstage + st * kStageBytes, &wbar[st],
+                    policy, issued < NS);
     }
     j_issue += W;
     ++issued;
@@ -512,14 +411,7 @@ __global__ void __launch_bounds__(kWarps * 32, D == 64 ? 3 : 2) decode_sk_kernel
   }
   if (!has_range) return;
 
-  // ldmatrix lane roles: matrix mi = lane/8, row rr = lane%8
-  const int mi = lane >> 3, rr = lane & 7;
-  const int a_row = rr + ((mi & 1) << 3);   // K tile (non-transposed A operand): token row
-  const int a_dof = (mi >> 1) << 3;         //                                    +8 dims
-  const int v_row = rr + ((mi >> 1) << 3);  // V tile (transposed A operand): token row
-  const int v_dof = (mi & 1) << 3;          //                                +8 dims
   const int gq = lane >> 2, q4 = lane & 3;  // accumulator roles: token/dim row, column pair
-  const float sl2 = a.scale_log2;
 
   int sg = g_start;            // segment cursor (uniform in the CTA)
   long long spre = pre_start;
@@ -538,20 +430,8 @@ __global__ void __launch_bounds__(kWarps * 32, D == 64 ? 3 : 2) decode_sk_kernel
     const bool more = spre + group_span(sgr) + kGapTiles < t_hi;
     while (j_cons < seg_begin) j_cons += W;  // over the group's gap
 
-    // Q of this group as the B operand of S = K . Q^T: in n-tile nt the lane holds
-    // q[g][16i + 2*q4 + {0,1}] and the same +8, g = 8*nt + lane/4; heads g >= G are zero.
     uint32_t qf[NT][kSteps][2];
-#pragma unroll
-    for (int nt = 0; nt < NT; ++nt) {
-      const int g = 8 * nt + gq;
-      const __nv_bfloat16* qrow =
-          static_cast<const __nv_bfloat16*>(a.q) + ((int64_t)sgr.s * Hq + sgr.h * G + g) * D;
-#pragma unroll
-      for (int i = 0; i < kSteps; ++i) {
-        qf[nt][i][0] = g < G ? *reinterpret_cast<const uint32_t*>(qrow + 16 * i + 2 * q4) : 0u;
-        qf[nt][i][1] = g < G ? *reinterpret_cast<const uint32_t*>(qrow + 16 * i + 2 * q4 + 8) : 0u;
-      }
-    }
+    load_q_frags<D, NT>(a, sgr, G, lane, qf);
     float acc[kSteps][NT][4];
 #pragma unroll
     for (int j = 0; j < kSteps; ++j)
@@ -571,92 +451,9 @@ __global__ void __launch_bounds__(kWarps * 32, D == 64 ? 3 : 2) decode_sk_kernel
       }
       if (drain_from < 0) {
         const uint32_t sK = wstage + st * kStageBytes;
-        const uint32_t sV = sK + kTileBytes;
         const int t0 = tile_slot(sgr, j_cons - spre - kGapTiles);
-
-        // fused append: the new token's rows replace the tile's copy of its slot and go to
-        // the pool (no other CTA reads this tile in this launch)
-        if (new_slot >= t0 && new_slot < t0 + kTile) {
-          const int r = new_slot - t0;
-          const int jb = new_slot / bs;
-          const int32_t blk = sgr.tbl[jb];
-          const bool blk_ok = blk >= 0 && (int64_t)blk < a.pv.total_blocks;
-          const int64_t src = ((int64_t)sgr.s * H + sgr.h) * D * 2;
-          char* dstk = static_cast<char*>(a.pv.pool) +
-                       ((int64_t)(blk_ok ? blk : 0) * 2 * bs + (new_slot - jb * bs)) * D * 2;
-          for (int i = lane; i < 2 * kRowVecs; i += 32) {
-            const int kv = i / kRowVecs, c = i - kv * kRowVecs;
-            const uint4 val = *reinterpret_cast<const uint4*>(
-                static_cast<const char*>(kv ? a.v_new : a.k_new) + src + c * 16);
-            const uint32_t sa = (kv ? sV : sK) + swz(r, c * 8);
-            asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(sa), "r"(val.x), "r"(val.y), "r"(val.z),
-                         "r"(val.w)
-                         : "memory");
-            if (blk_ok) *reinterpret_cast<uint4*>(dstk + (int64_t)kv * bs * D * 2 + c * 16) = val;
-          }
-          __syncwarp();
+        if (consume_tile<D, NT>(a, sgr, t0, new_slot, sK, sK + kTileBytes, qf, acc, mx, ls, lane))
           patched_stage = true;
-        }
-
-        // S[16 tok][8 q] = K_tile . Q^T per n-tile (two accumulation chains each)
-        float sa[NT][4], sb[NT][4];
-#pragma unroll
-        for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-          for (int e = 0; e < 4; ++e) sa[nt][e] = sb[nt][e] = 0.f;
-#pragma unroll
-        for (int i = 0; i < kSteps; ++i) {
-          uint32_t af[4];
-          ldsm_x4(af, sK + swz(a_row, 16 * i + a_dof));
-#pragma unroll
-          for (int nt = 0; nt < NT; ++nt) {
-            if (i & 1) mma_bf16(sb[nt], af, qf[nt][i][0], qf[nt][i][1]);
-            else mma_bf16(sa[nt], af, qf[nt][i][0], qf[nt][i][1]);
-          }
-        }
-        const bool v0 = slot_valid(sgr.rs, t0 + gq), v1 = slot_valid(sgr.rs, t0 + gq + 8);
-        float al[NT][2];
-        uint32_t pb[NT][2];
-#pragma unroll
-        for (int nt = 0; nt < NT; ++nt) {
-          const float s0 = v0 ? sa[nt][0] + sb[nt][0] : kNegInf;
-          const float s1 = v0 ? sa[nt][1] + sb[nt][1] : kNegInf;
-          const float s2 = v1 ? sa[nt][2] + sb[nt][2] : kNegInf;
-          const float s3 = v1 ? sa[nt][3] + sb[nt][3] : kNegInf;
-          float mx0 = fmaxf(s0, s2), mx1 = fmaxf(s1, s3);
-#pragma unroll
-          for (int off = 4; off < 32; off <<= 1) {
-            mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, off));
-            mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, off));
-          }
-          const float n0 = fmaxf(mx[nt][0], mx0 * sl2), n1 = fmaxf(mx[nt][1], mx1 * sl2);
-          const float b0 = n0 == kNegInf ? 0.f : n0, b1 = n1 == kNegInf ? 0.f : n1;
-          al[nt][0] = ex2(mx[nt][0] - b0);
-          al[nt][1] = ex2(mx[nt][1] - b1);
-          const float p0 = ex2(fmaf(s0, sl2, -b0)), p1 = ex2(fmaf(s1, sl2, -b1));
-          const float p2 = ex2(fmaf(s2, sl2, -b0)), p3 = ex2(fmaf(s3, sl2, -b1));
-          ls[nt][0] = fmaf(ls[nt][0], al[nt][0], p0 + p2);
-          ls[nt][1] = fmaf(ls[nt][1], al[nt][1], p1 + p3);
-          mx[nt][0] = n0;
-          mx[nt][1] = n1;
-          pb[nt][0] = movmatrix_trans(pack_bf16(p0, p1));
-          pb[nt][1] = movmatrix_trans(pack_bf16(p2, p3));
-        }
-
-        // O^T[D][8 q] = alpha * O^T + V_tile^T . P per n-tile
-#pragma unroll
-        for (int j = 0; j < kSteps; ++j) {
-          uint32_t af[4];
-          ldsm_x4_trans(af, sV + swz(v_row, 16 * j + v_dof));
-#pragma unroll
-          for (int nt = 0; nt < NT; ++nt) {
-            acc[j][nt][0] *= al[nt][0];
-            acc[j][nt][1] *= al[nt][1];
-            acc[j][nt][2] *= al[nt][0];
-            acc[j][nt][3] *= al[nt][1];
-            mma_bf16(acc[j][nt], af, pb[nt][0], pb[nt][1]);
-          }
-        }
       }
       __syncwarp();
       ++consumed;
