@@ -135,7 +135,6 @@ __device__ __forceinline__ void merge_slots_regs(const float* src_acc, const flo
     store_merged<D>(M, L, acc, q, d4, G, out_grp, dst_acc, dst_ml, dst_slot);
   }
 }
-constexpr int kMergeMax = 64;          // most slots the shared-memory merge takes
 constexpr uint32_t kBulkChunk = 16384;  // bytes per bulk copy of a partial block
 
 // Shared-memory resources a merge may use: the stage buffers (free once the CTA has consumed
@@ -150,19 +149,21 @@ struct MergeStage {
 
 // Folds `count` consecutive partial slots [first, first + count) into the output or partial
 // slot of store_merged.  When every slot holds a partial (`dense`), the stage buffers are free
-// and the accumulators fit, they are fetched in one bulk copy while the (m, l) of every
-// (slot, head) are read into `s_ml` (2 * count * G floats); the maxima M = max_i m_i and the
-// weights w_i = 2^(m_i - M) are formed once per (slot, head), and each thread sums
-// w_i * acc_i over its 4 columns of one query head out of shared memory, L = sum_i w_i * l_i.
-// The whole merge then waits for about one round trip to L2.  Otherwise the register merge
-// above runs, with the same arithmetic.  `live(i)` tells whether slot first + i holds a partial.
+// and the accumulators fit them and the (m, l) of every (slot, head) fit `s_ml` (2 * count * G
+// <= ml_cap floats), the accumulators are fetched in one bulk copy while those (m, l) are read
+// into `s_ml`; each thread then forms its head's maximum M = max_i m_i and, slot after slot,
+// w_i = 2^(m_i - M), L = fma(l_i, w_i, L) and the sum of w_i * acc_i over its 4 columns out of
+// shared memory (the threads of a warp share a head, so the reads are broadcasts).  The whole
+// merge waits for about one round trip to L2.  Otherwise the register merge above runs, with
+// the same arithmetic, so an output does not depend on which path its last arriver took.
+// `live(i)` tells whether slot first + i holds a partial.
 template <int D, typename Live>
 __device__ __forceinline__ void merge_slots(const float* src_acc, const float* src_ml, long long first, int count,
                                             int G, Live live, bool dense, __nv_bfloat16* out_grp, float* dst_acc,
-                                            float* dst_ml, long long dst_slot, float* s_ml, float* s_ML,
+                                            float* dst_ml, long long dst_slot, float* s_ml, int ml_cap,
                                             MergeStage& ms, int32_t* err) {
   const uint32_t bytes = (uint32_t)count * (uint32_t)G * D * 4u;
-  if (!dense || ms.buf == nullptr || count > kMergeMax || bytes > ms.bytes) {
+  if (!dense || ms.buf == nullptr || 2 * count * G > ml_cap || bytes > ms.bytes) {
     merge_slots_regs<D>(src_acc, src_ml, first, count, G, live, out_grp, dst_acc, dst_ml, dst_slot);
     return;
   }
@@ -180,20 +181,6 @@ __device__ __forceinline__ void merge_slots(const float* src_acc, const float* s
     s_ml[count * G + p] = ml.y;
   }
   __syncthreads();
-  if (threadIdx.x < G) {
-    const int q = threadIdx.x;
-    float M = kNegInf;
-    for (int i = 0; i < count; ++i) M = fmaxf(M, s_ml[i * G + q]);
-    float L = 0.f;
-    for (int i = 0; i < count; ++i) {
-      const float w = M == kNegInf ? 0.f : ex2(s_ml[i * G + q] - M);
-      s_ml[i * G + q] = w;
-      L = fmaf(s_ml[count * G + i * G + q], w, L);
-    }
-    s_ML[q] = M;
-    s_ML[G + q] = L;
-  }
-  __syncthreads();
   const bool landed = mbar_wait_bounded(ms.bar, ms.phase & 1u);
   ++ms.phase;
   if (!landed && threadIdx.x == 0) atomicOr(err, HWKV_DEVERR_WAIT_TIMEOUT);
@@ -201,10 +188,14 @@ __device__ __forceinline__ void merge_slots(const float* src_acc, const float* s
   const float4* sacc = reinterpret_cast<const float4*>(ms.buf);
   for (int e = threadIdx.x; e < G * kV; e += blockDim.x) {
     const int q = e / kV, d4 = e - (e / kV) * kV;
+    float M = kNegInf;
+    for (int i = 0; i < count; ++i) M = fmaxf(M, s_ml[i * G + q]);
+    float L = 0.f;
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-    if (landed) {
-      for (int i = 0; i < count; ++i) {
-        const float w = s_ml[i * G + q];
+    for (int i = 0; i < count; ++i) {
+      const float w = M == kNegInf ? 0.f : ex2(s_ml[i * G + q] - M);
+      L = fmaf(s_ml[count * G + i * G + q], w, L);
+      if (landed) {
         const float4 v = sacc[(i * G + q) * kV + d4];
         acc.x = fmaf(v.x, w, acc.x);
         acc.y = fmaf(v.y, w, acc.y);
@@ -212,7 +203,7 @@ __device__ __forceinline__ void merge_slots(const float* src_acc, const float* s
         acc.w = fmaf(v.w, w, acc.w);
       }
     }
-    store_merged<D>(s_ML[q], s_ML[G + q], acc, q, d4, G, out_grp, dst_acc, dst_ml, dst_slot);
+    store_merged<D>(M, L, acc, q, d4, G, out_grp, dst_acc, dst_ml, dst_slot);
   }
   if (!landed) {  // a copy may still be in flight: no later merge reuses the buffer
     ms.stuck = (int)((ms.phase - 1u) & 1u);
@@ -263,10 +254,9 @@ __global__ void __launch_bounds__(kWarps * 32, D == 64 ? 3 : 2) decode_sk_kernel
   float* sc_acc = reinterpret_cast<float*>(smem + W * NS * kStageBytes);  // [W][SG][D]
   __shared__ __align__(8) uint64_t bars[W * NS];
   __shared__ float sc_m[W * SG], sc_l[W * SG];
-  __shared__ float s_ML[2 * kMaxGroup];  // per-head maxima and weight sums of a partial merge
   __shared__ __align__(8) uint64_t merge_bar;  // bulk copies of partial blocks
-  // the partial merge's (m, l) scratch reuses the warps' merge area
-  static_assert(2 * kMergeMax * GP <= W * SG * D, "partial-merge scratch exceeds the warp merge area");
+  // the partial merge's (m, l) scratch reuses the warps' merge area: 2 * slots * G floats
+  constexpr int kMlCap = W * SG * D;
   __shared__ long long s_scan[W];
   __shared__ long long s_start[2];
   __shared__ int s_last;
@@ -536,7 +526,9 @@ __global__ void __launch_bounds__(kWarps * 32, D == 64 ? 3 : 2) decode_sk_kernel
       // The partial is published; count arrivals.  Up to kFlatMerge contributors: the last
       // CTA of the group merges them all.  More (long windows at small batch): blocks of
       // kMergeBlock consecutive contributors are merged by their last arriver into a second-
-      // level partial, and the last of those merges the blocks.
+      // level partial, and the last of those merges the blocks (one level of ~100 partials,
+      // streamed through the stage buffers in chunks by one CTA, was slower at batch 1: 877
+      // against 955 tokens/s; it moves ~200 KB through one SM where the tree spreads it).
       // After the last segment no copy is in flight (unless a wait timed out): merges may
       // stage partial blocks in the stage buffers.
       if (!more) ms.buf = __syncthreads_or(drain_from >= 0) ? nullptr : reinterpret_cast<float*>(smem);
@@ -555,7 +547,7 @@ __global__ void __launch_bounds__(kWarps * 32, D == 64 ? 3 : 2) decode_sk_kernel
             return all_live || range_start(T, c_lo + i + 1, nctas) > range_start(T, c_lo + i, nctas);
           };
           merge_slots<D>(a.part_acc, a.part_ml, (long long)sg + c_lo, k, G, live, all_live, out_grp, nullptr,
-                         nullptr, 0, sc_acc, s_ML, ms, a.pv.err);
+                         nullptr, 0, sc_acc, kMlCap, ms, a.pv.err);
         }
       } else {
         auto live = [](int) { return true; };
@@ -566,10 +558,10 @@ __global__ void __launch_bounds__(kWarps * 32, D == 64 ? 3 : 2) decode_sk_kernel
         const long long slot2 = (long long)sg * a.merge_blocks + b;
         if (arrive_last(&a.counters1[slot2], b_n, &s_last)) {
           merge_slots<D>(a.part_acc, a.part_ml, (long long)sg + b_lo, b_n, G, live, true, nullptr, a.part2_acc,
-                         a.part2_ml, slot2, sc_acc, s_ML, ms, a.pv.err);
+                         a.part2_ml, slot2, sc_acc, kMlCap, ms, a.pv.err);
           if (arrive_last(&a.counters[sg], nb, &s_last))
             merge_slots<D>(a.part2_acc, a.part2_ml, (long long)sg * a.merge_blocks, nb, G, live, true, out_grp,
-                           nullptr, nullptr, 0, sc_acc, s_ML, ms, a.pv.err);
+                           nullptr, nullptr, 0, sc_acc, kMlCap, ms, a.pv.err);
         }
       }
     }

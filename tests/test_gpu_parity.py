@@ -175,6 +175,24 @@ def test_tensor_core_partition_changes_rounding_only(workers):
     run.close()
 
 
+@pytest.mark.parametrize("workers", [40, 60, 100, 160, 288])
+def test_long_window_merge_at_batch_one(workers):
+    """A 64K window at batch 1 spread over 40 .. 288 CTAs: its ~40 .. 280 contributors are
+    merged in two levels (blocks of 8, then the blocks); every variant matches the oracle and
+    repeats bit for bit."""
+    cfg = small_config(name="merge1", kv_heads=2, windows=((65536, 1024),), prefill=(70000,))
+    runs = [Run(cfg, kernel=hw.HWKV_KERNEL_TENSOR, workers=workers, fused=True) for _ in range(2)]
+    for r in runs:
+        r.materialize()
+    for i in range(2):
+        a, b = (r.step(keep_layers=[0]) for r in runs)
+        assert np.array_equal(a[0][1], b[0][1]), f"workers {workers} step {i}"
+        assert_close(a[0][1], runs[0].reference(i, 0, a[0][0]), cfg, f"workers {workers} step {i}")
+    for r in runs:
+        assert r.device_errors() == 0
+        r.close()
+
+
 @pytest.mark.parametrize("kernel", [hw.HWKV_KERNEL_TENSOR, hw.HWKV_KERNEL_SIMT])
 def test_launches_are_deterministic(kernel):
     """No output depends on which CTA arrives last at a merge: two pools driven with the same
