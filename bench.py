@@ -695,6 +695,69 @@ def secondary_block(args, dev, stream, peak: float) -> dict:
 
 
 # --------------------------------------------------------------------------------------
+# decode by shape: the full geometry's first 8 layers at other head dims, groups and dtypes
+# --------------------------------------------------------------------------------------
+SHAPES = (("bf16 D128 GQA4", {}), ("bf16 D128 GQA8", {"q_heads": 64}), ("bf16 D128 GQA16", {"q_heads": 128}),
+          ("bf16 D64 GQA4", {"head_dim": 64}), ("bf16 D64 GQA8", {"head_dim": 64, "q_heads": 64}),
+          ("bf16 D64 GQA16", {"head_dim": 64, "q_heads": 128}), ("fp32 D128 GQA4", {"dtype": "f32"}),
+          ("fp32 D64 GQA4", {"dtype": "f32", "head_dim": 64}))
+
+
+def run_shapes(args):
+    """Fused append + decode, prepared launches with early reads, on the full workload's first 8
+    layers (batch 4, 112K) for each shape of SHAPES: resident-KV GB/s over W warm-up and K timed
+    steps.  Prints one JSON line."""
+    import dataclasses
+    import torch
+    import workloads
+    import head_budgeted_kv_gb300 as hw
+    dev = torch.device("cuda", 0)
+    hw.binding.load()
+    stream = torch.cuda.current_stream(dev)
+    peak, peak_kind = measured_peak()
+    rows = []
+    for label, kw in SHAPES:
+        cfg = dataclasses.replace(workloads.config("full").with_layers(8), name="full_8l", **kw)
+        wl = workloads.Workload(cfg, device=dev)
+        pool = hw.Pool(cfg.layers, cfg.kv_heads, cfg.head_dim, cfg.block_size, cfg.windows_array(), cfg.batch,
+                       cfg.torch_dtype, q_heads=cfg.q_heads, device=dev)
+        prefill = torch.tensor(cfg.prefill, dtype=torch.int32, device=dev)
+        for l in range(cfg.layers):
+            K, V = wl.prefill_layer(l, dev)
+            pool.materialize(l, K, V, prefill)
+            del K, V
+        total = args.warmup + args.steps
+        inputs = [wl.step_inputs(i, dev) for i in range(total)]
+        pos = [(prefill + i).contiguous() for i in range(total)]
+        outs = torch.empty((cfg.layers, cfg.batch, cfg.q_heads, cfg.head_dim), dtype=cfg.torch_dtype, device=dev)
+        launches = [[pool.decode_launch(l, inputs[i][0][l], cfg.scale, pos[i], outs[l], inputs[i][1][l],
+                                        inputs[i][2][l], early_reads=True) for l in range(cfg.layers)]
+                    for i in range(total)]
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        for i in range(total):
+            if i == args.warmup:
+                e0.record(stream)
+            for launch in launches[i]:
+                launch()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        ms = e0.elapsed_time(e1) / args.steps
+        bits = pool.check_device_errors()
+        pool.close()
+        del pool, wl, inputs, pos, outs, launches
+        torch.cuda.empty_cache()
+        if bits:
+            raise RuntimeError(f"device error bits {bits:#x} for {label}")
+        nbytes = mean_step_bytes(cfg, args.warmup, args.steps)
+        gbs = nbytes / (ms / 1e3) / 1e9
+        rows.append({"shape": label, "ms_per_step": ms, "resident_kv_gbs": gbs, "frac": gbs / peak})
+    print(json.dumps({"metric": "fused decode resident-KV GB/s by shape (full geometry, first 8 layers)",
+                      "unit": "GB/s", "peak": peak, "peak_kind": peak_kind, "steps": args.steps,
+                      "warmup": args.warmup, "shapes": rows}), flush=True)
+
+
+# --------------------------------------------------------------------------------------
 # chunked prefill (hwkv_prefill_attn): not the default line
 # --------------------------------------------------------------------------------------
 def prefill_flops(cfg, layer: int, pos0, n: int) -> int:
@@ -899,7 +962,7 @@ def main(argv=None):
     p.add_argument("--workers", type=int, default=0, help="tensor-core kernel: CTAs of the persistent grid")
     p.add_argument("--path", choices=["fused", "split"], default="fused")
     p.add_argument("--graph", action="store_true", help="replay each decode step as one captured CUDA graph")
-    p.add_argument("--mode", choices=["decode", "prefill"], default="decode")
+    p.add_argument("--mode", choices=["decode", "prefill", "shapes"], default="decode")
     p.add_argument("--chunk", type=int, default=2048, help="prefill mode: tokens per sequence per chunk")
     p.add_argument("--prefill-max-stages", type=int, default=0,
                    help="prefill mode: split key streams longer than this many 64-key stages (0 = automatic)")
@@ -930,6 +993,8 @@ def main(argv=None):
             workloads.config(n)  # unknown names fail here
     if args.impl == "reference":
         run_reference(args, cfg)
+    elif args.mode == "shapes":
+        run_shapes(args)
     elif args.mode == "prefill":
         run_prefill(args, cfg)
     else:

@@ -57,20 +57,24 @@ constexpr int kL2PrefetchMin = 64;
 
 __device__ __forceinline__ int group_span(const Group& gr) { return gr.tiles > 0 ? gr.tiles + kGapTiles : 0; }
 
-// Writes a merged (M, L, acc) of query head q, columns 4*d4 .. 4*d4 + 3: normalised to the bf16
-// output `out_grp` when it is non-null, else unnormalised to partial slot `dst_slot`.
-template <int D>
-__device__ __forceinline__ void store_merged(float M, float L, float4 acc, int q, int d4, int G,
-                                             __nv_bfloat16* out_grp, float* dst_acc, float* dst_ml,
-                                             long long dst_slot) {
+// Writes a merged (M, L, acc) of query head q, columns 4*d4 .. 4*d4 + 3: normalised to the
+// output `out_grp` (bf16 or fp32) when it is non-null, else unnormalised to partial slot `dst_slot`.
+template <typename T, int D>
+__device__ __forceinline__ void store_merged(float M, float L, float4 acc, int q, int d4, int G, T* out_grp,
+                                             float* dst_acc, float* dst_ml, long long dst_slot) {
   if (out_grp != nullptr) {
     const float inv = L > 0.f ? 1.f / L : 0.f;
-    __nv_bfloat162 lo = __floats2bfloat162_rn(acc.x * inv, acc.y * inv);
-    __nv_bfloat162 hi = __floats2bfloat162_rn(acc.z * inv, acc.w * inv);
-    uint2 packed;
-    packed.x = *reinterpret_cast<uint32_t*>(&lo);
-    packed.y = *reinterpret_cast<uint32_t*>(&hi);
-    *reinterpret_cast<uint2*>(out_grp + (int64_t)q * D + d4 * 4) = packed;
+    if constexpr (sizeof(T) == 4) {
+      *reinterpret_cast<float4*>(out_grp + (int64_t)q * D + d4 * 4) =
+          make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
+    } else {
+      __nv_bfloat162 lo = __floats2bfloat162_rn(acc.x * inv, acc.y * inv);
+      __nv_bfloat162 hi = __floats2bfloat162_rn(acc.z * inv, acc.w * inv);
+      uint2 packed;
+      packed.x = *reinterpret_cast<uint32_t*>(&lo);
+      packed.y = *reinterpret_cast<uint32_t*>(&hi);
+      *reinterpret_cast<uint2*>(out_grp + (int64_t)q * D + d4 * 4) = packed;
+    }
   } else {
     const long long slot = dst_slot * G + q;
     reinterpret_cast<float4*>(dst_acc + slot * D)[d4] = acc;
@@ -84,9 +88,9 @@ __device__ __forceinline__ void store_merged(float M, float L, float4 acc, int q
 // same bit for bit.  Each thread owns 4 consecutive output columns of one query head and keeps
 // 8 slots' loads in flight.  Output as store_merged.  `live(i)` tells whether slot first + i
 // holds a partial.
-template <int D, typename Live>
+template <typename T, int D, typename Live>
 __device__ __forceinline__ void merge_slots_regs(const float* src_acc, const float* src_ml, long long first,
-                                                 int count, int G, Live live, __nv_bfloat16* out_grp,
+                                                 int count, int G, Live live, T* out_grp,
                                                  float* dst_acc, float* dst_ml, long long dst_slot) {
   constexpr int kV = D / 4;  // float4 columns per query head
   constexpr int kBatch = 8;
@@ -132,7 +136,7 @@ __device__ __forceinline__ void merge_slots_regs(const float* src_acc, const flo
         }
       }
     }
-    store_merged<D>(M, L, acc, q, d4, G, out_grp, dst_acc, dst_ml, dst_slot);
+    store_merged<T, D>(M, L, acc, q, d4, G, out_grp, dst_acc, dst_ml, dst_slot);
   }
 }
 constexpr uint32_t kBulkChunk = 16384;  // bytes per bulk copy of a partial block
@@ -157,14 +161,14 @@ struct MergeStage {
 // merge waits for about one round trip to L2.  Otherwise the register merge above runs, with
 // the same arithmetic, so an output does not depend on which path its last arriver took.
 // `live(i)` tells whether slot first + i holds a partial.
-template <int D, typename Live>
+template <typename T, int D, typename Live>
 __device__ __forceinline__ void merge_slots(const float* src_acc, const float* src_ml, long long first, int count,
-                                            int G, Live live, bool dense, __nv_bfloat16* out_grp, float* dst_acc,
+                                            int G, Live live, bool dense, T* out_grp, float* dst_acc,
                                             float* dst_ml, long long dst_slot, float* s_ml, int ml_cap,
                                             MergeStage& ms, int32_t* err) {
   const uint32_t bytes = (uint32_t)count * (uint32_t)G * D * 4u;
   if (!dense || ms.buf == nullptr || 2 * count * G > ml_cap || bytes > ms.bytes) {
-    merge_slots_regs<D>(src_acc, src_ml, first, count, G, live, out_grp, dst_acc, dst_ml, dst_slot);
+    merge_slots_regs<T, D>(src_acc, src_ml, first, count, G, live, out_grp, dst_acc, dst_ml, dst_slot);
     return;
   }
   if (threadIdx.x == 0) {
@@ -203,7 +207,7 @@ __device__ __forceinline__ void merge_slots(const float* src_acc, const float* s
         acc.w = fmaf(v.w, w, acc.w);
       }
     }
-    store_merged<D>(M, L, acc, q, d4, G, out_grp, dst_acc, dst_ml, dst_slot);
+    store_merged<T, D>(M, L, acc, q, d4, G, out_grp, dst_acc, dst_ml, dst_slot);
   }
   if (!landed) {  // a copy may still be in flight: no later merge reuses the buffer
     ms.stuck = (int)((ms.phase - 1u) & 1u);
@@ -236,18 +240,25 @@ __host__ __device__ constexpr int merge_heads() {
   return GP < 8 ? GP : (D == 128 ? 4 : 8);
 }
 
-// Two CTAs per SM at head_dim 128; three at 64 (4 stages of half-size tiles fit three in shared
-// memory, and the per-tile instruction chain, twice as long per byte there, needs the warps).
-template <int D, int GP, int NS>
-__global__ void __launch_bounds__(kWarps * 32, D == 64 ? 3 : 2) decode_sk_kernel(const __grid_constant__ CUtensorMap tmap,
-                                                                const __grid_constant__ DecodeArgs a) {
+// CTAs per SM: bf16 two at head_dim 128, three at 64 (4 stages of half-size tiles fit three in
+// shared memory, and the per-tile instruction chain, twice as long per byte there, needs the
+// warps); fp32 tiles are twice the bytes: one at 128, two at 64.
+template <typename T, int D>
+__host__ __device__ constexpr int sk_min_ctas() {
+  return sizeof(T) == 2 ? (D == 64 ? 3 : 2) : (D == 64 ? 2 : 1);
+}
+
+template <typename Elem, int D, int GP, int NS>
+__global__ void __launch_bounds__(kWarps * 32, sk_min_ctas<Elem, D>())
+    decode_sk_kernel(const __grid_constant__ CUtensorMap tmap, const __grid_constant__ DecodeArgs a) {
+  using State = WarpState<Elem, D, GP>;
   constexpr int W = kWarps;
-  constexpr int kTileBytes = kTile * D * 2;    // 16 rows of bf16
+  constexpr int kEB = (int)sizeof(Elem);
+  constexpr int kTileBytes = kTile * D * kEB;  // 16 rows
   constexpr int kStageBytes = 2 * kTileBytes;  // K tile + V tile
-  constexpr int kSteps = D / 16;               // k-steps of QK, m-tiles of PV
-  constexpr int NT = (GP + 7) / 8;             // 8-column n-tiles of query heads
+  constexpr int NT = State::NT;                // 8-column groups of query heads
   constexpr int SG = merge_heads<D, GP>();      // query heads merged per pass in shared memory
-  constexpr int kPasses = GP < 8 ? 1 : 8 / SG;  // passes per 8-column n-tile
+  constexpr int kPasses = GP < 8 ? 1 : 8 / SG;  // passes per 8-column group
 
   extern __shared__ uint8_t smem_dyn[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_dyn) + 1023) & ~uintptr_t(1023));
@@ -261,6 +272,7 @@ __global__ void __launch_bounds__(kWarps * 32, D == 64 ? 3 : 2) decode_sk_kernel
   __shared__ long long s_start[2];
   __shared__ int s_last;
   __shared__ int s_lens_buf[kLensCache];
+  __shared__ __align__(16) float s_p[kEB == 4 ? W * 64 : 4];  // fp32 tiles: each warp's P
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int H = a.pv.kv_heads;
@@ -270,7 +282,7 @@ __global__ void __launch_bounds__(kWarps * 32, D == 64 ? 3 : 2) decode_sk_kernel
   const int G = a.group;
   const int Hq = H * G;
   const int bs = a.pv.block_size;
-  __nv_bfloat16* const out = static_cast<__nv_bfloat16*>(a.out);
+  Elem* const out = static_cast<Elem*>(a.out);
 
   // The next grid in the stream may start at once: its CTAs take the slots this grid's CTAs
   // free, run their own early reads, and wait for this grid before anything else (with the
@@ -357,8 +369,8 @@ __global__ void __launch_bounds__(kWarps * 32, D == 64 ? 3 : 2) decode_sk_kernel
     if (lane == issuer) {
       const int st = issued % NS;
       // the first stages may be issued before the dependent-launch wait: read through L2
-      issue_tile<D>(&tmap, a, igr, tile_slot(igr, j_issue - ipre - kGapTiles), wstage + st * kStageBytes, &wbar[st],
-                    policy, issued < NS);
+      issue_tile<kEB, D>(&tmap, a, igr, tile_slot(igr, j_issue - ipre - kGapTiles), wstage + st * kStageBytes,
+                         &wbar[st], policy, issued < NS);
     }
     j_issue += W;
     ++issued;
@@ -384,9 +396,9 @@ __global__ void __launch_bounds__(kWarps * 32, D == 64 ? 3 : 2) decode_sk_kernel
         const int jb = t0 / bs;
         const int32_t blk = __ldcg(gr.tbl + jb);
         if (blk >= 0 && (int64_t)blk < a.pv.total_blocks) {
-          const char* rows = static_cast<const char*>(a.pv.pool) + ((int64_t)blk * 2 * bs + (t0 - jb * bs)) * D * 2;
-          prefetch_l2_bulk(rows, kTileBytes);                       // K rows of the tile
-          prefetch_l2_bulk(rows + (int64_t)bs * D * 2, kTileBytes);  // V rows
+          const char* rows = static_cast<const char*>(a.pv.pool) + ((int64_t)blk * 2 * bs + (t0 - jb * bs)) * D * kEB;
+          prefetch_l2_bulk(rows, kTileBytes);                         // K rows of the tile
+          prefetch_l2_bulk(rows + (int64_t)bs * D * kEB, kTileBytes);  // V rows
         }
       }
     }
@@ -397,11 +409,9 @@ __global__ void __launch_bounds__(kWarps * 32, D == 64 ? 3 : 2) decode_sk_kernel
     const Group gr = load_group(a, s_lens, g);
     if (gr.tiles == 0)
       for (int e = threadIdx.x; e < G * D; e += W * 32)
-        out[((int64_t)gr.s * Hq + gr.h * G + e / D) * D + e % D] = __float2bfloat16_rn(0.f);
+        store_out<Elem>(out + ((int64_t)gr.s * Hq + gr.h * G + e / D) * D + e % D, 0.f);
   }
   if (!has_range) return;
-
-  const int gq = lane >> 2, q4 = lane & 3;  // accumulator roles: token/dim row, column pair
 
   int sg = g_start;            // segment cursor (uniform in the CTA)
   long long spre = pre_start;
@@ -420,17 +430,8 @@ __global__ void __launch_bounds__(kWarps * 32, D == 64 ? 3 : 2) decode_sk_kernel
     const bool more = spre + group_span(sgr) + kGapTiles < t_hi;
     while (j_cons < seg_begin) j_cons += W;  // over the group's gap
 
-    uint32_t qf[NT][kSteps][2];
-    load_q_frags<D, NT>(a, sgr, G, lane, qf);
-    float acc[kSteps][NT][4];
-#pragma unroll
-    for (int j = 0; j < kSteps; ++j)
-#pragma unroll
-      for (int nt = 0; nt < NT; ++nt) acc[j][nt][0] = acc[j][nt][1] = acc[j][nt][2] = acc[j][nt][3] = 0.f;
-    // online-softmax state of columns g = 8*nt + 2*q4 + {0, 1}
-    float mx[NT][2], ls[NT][2];
-#pragma unroll
-    for (int nt = 0; nt < NT; ++nt) mx[nt][0] = mx[nt][1] = kNegInf, ls[nt][0] = ls[nt][1] = 0.f;
+    State ws;
+    ws.begin(a, sgr, G, lane);
     const int new_slot = (a.k_new != nullptr) ? (sgr.len - 1) % sgr.rs.C : -1;
 
     while (j_cons < seg_end) {
@@ -442,8 +443,7 @@ __global__ void __launch_bounds__(kWarps * 32, D == 64 ? 3 : 2) decode_sk_kernel
       if (drain_from < 0) {
         const uint32_t sK = wstage + st * kStageBytes;
         const int t0 = tile_slot(sgr, j_cons - spre - kGapTiles);
-        if (consume_tile<D, NT>(a, sgr, t0, new_slot, sK, sK + kTileBytes, qf, acc, mx, ls, lane))
-          patched_stage = true;
+        if (ws.consume(a, sgr, t0, new_slot, sK, sK + kTileBytes, s_p + warp * 64, lane)) patched_stage = true;
       }
       __syncwarp();
       ++consumed;
@@ -459,13 +459,7 @@ __global__ void __launch_bounds__(kWarps * 32, D == 64 ? 3 : 2) decode_sk_kernel
     }
 
     // ---- end of segment: merge the warps, then store output or partial -----------------
-#pragma unroll
-    for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-      for (int off = 4; off < 32; off <<= 1) {
-        ls[nt][0] += __shfl_xor_sync(0xffffffffu, ls[nt][0], off);
-        ls[nt][1] += __shfl_xor_sync(0xffffffffu, ls[nt][1], off);
-      }
+    ws.finish();
     const bool whole = seg_begin == spre + kGapTiles && seg_end == spre + group_span(sgr);
     const long long slot = (long long)sg + cta;  // unique per (group, CTA) along the line
     // pass (nt, hh): the warps' states of query heads [8*nt + hh*SG, 8*nt + (hh+1)*SG) meet in
@@ -475,24 +469,7 @@ __global__ void __launch_bounds__(kWarps * 32, D == 64 ? 3 : 2) decode_sk_kernel
 #pragma unroll
     for (int hh = 0; hh < kPasses; ++hh) {
       if (nt > 0 || hh > 0) __syncthreads();  // the previous pass has read the scratch
-      const int c0 = 2 * q4 - hh * SG;  // this lane's first column within the pass
-      if (c0 >= 0 && c0 < SG) {
-        if (gq == 0) {
-          sc_m[warp * SG + c0] = mx[nt][0];
-          sc_m[warp * SG + c0 + 1] = mx[nt][1];
-          sc_l[warp * SG + c0] = ls[nt][0];
-          sc_l[warp * SG + c0 + 1] = ls[nt][1];
-        }
-        float* wacc = sc_acc + warp * SG * D;
-#pragma unroll
-        for (int j = 0; j < kSteps; ++j) {
-          const int d = 16 * j + gq;
-          wacc[c0 * D + d] = acc[j][nt][0];
-          wacc[(c0 + 1) * D + d] = acc[j][nt][1];
-          wacc[c0 * D + d + 8] = acc[j][nt][2];
-          wacc[(c0 + 1) * D + d + 8] = acc[j][nt][3];
-        }
-      }
+      ws.template publish<SG>(nt, hh, warp, lane, sc_m, sc_l, sc_acc);
       __syncthreads();
       const int g0 = 8 * nt + hh * SG;
       const int ng = min(SG, G - g0);  // real query heads of this pass
@@ -512,7 +489,7 @@ __global__ void __launch_bounds__(kWarps * 32, D == 64 ? 3 : 2) decode_sk_kernel
           }
         }
         if (whole) {
-          out[((int64_t)sgr.s * Hq + sgr.h * G + g) * D + d] = __float2bfloat16_rn(Ls > 0.f ? A / Ls : 0.f);
+          store_out<Elem>(out + ((int64_t)sgr.s * Hq + sgr.h * G + g) * D + d, Ls > 0.f ? A / Ls : 0.f);
         } else {
           a.part_acc[(slot * G + g) * D + d] = A;
           if (d == 0) {
@@ -535,7 +512,7 @@ __global__ void __launch_bounds__(kWarps * 32, D == 64 ? 3 : 2) decode_sk_kernel
       const int c_lo = cta_of(spre + kGapTiles, T, nctas), c_hi = cta_of(spre + group_span(sgr) - 1, T, nctas);
       const bool all_live = T >= nctas;  // then no CTA range is empty
       const int k = c_hi - c_lo + 1;
-      __nv_bfloat16* const out_grp = out + ((int64_t)sgr.s * Hq + sgr.h * G) * D;
+      Elem* const out_grp = out + ((int64_t)sgr.s * Hq + sgr.h * G) * D;
       if (!all_live || k <= kFlatMerge) {
         int expected = k;
         if (!all_live) {
@@ -546,7 +523,7 @@ __global__ void __launch_bounds__(kWarps * 32, D == 64 ? 3 : 2) decode_sk_kernel
           auto live = [&](int i) {
             return all_live || range_start(T, c_lo + i + 1, nctas) > range_start(T, c_lo + i, nctas);
           };
-          merge_slots<D>(a.part_acc, a.part_ml, (long long)sg + c_lo, k, G, live, all_live, out_grp, nullptr,
+          merge_slots<Elem, D>(a.part_acc, a.part_ml, (long long)sg + c_lo, k, G, live, all_live, out_grp, nullptr,
                          nullptr, 0, sc_acc, kMlCap, ms, a.pv.err);
         }
       } else {
@@ -557,10 +534,10 @@ __global__ void __launch_bounds__(kWarps * 32, D == 64 ? 3 : 2) decode_sk_kernel
         const int b_n = min(kMergeBlock, c_hi - b_lo + 1);
         const long long slot2 = (long long)sg * a.merge_blocks + b;
         if (arrive_last(&a.counters1[slot2], b_n, &s_last)) {
-          merge_slots<D>(a.part_acc, a.part_ml, (long long)sg + b_lo, b_n, G, live, true, nullptr, a.part2_acc,
+          merge_slots<Elem, D>(a.part_acc, a.part_ml, (long long)sg + b_lo, b_n, G, live, true, (Elem*)nullptr, a.part2_acc,
                          a.part2_ml, slot2, sc_acc, kMlCap, ms, a.pv.err);
           if (arrive_last(&a.counters[sg], nb, &s_last))
-            merge_slots<D>(a.part2_acc, a.part2_ml, (long long)sg * a.merge_blocks, nb, G, live, true, out_grp,
+            merge_slots<Elem, D>(a.part2_acc, a.part2_ml, (long long)sg * a.merge_blocks, nb, G, live, true, out_grp,
                            nullptr, nullptr, 0, sc_acc, kMlCap, ms, a.pv.err);
         }
       }
@@ -581,48 +558,74 @@ __global__ void __launch_bounds__(kWarps * 32, D == 64 ? 3 : 2) decode_sk_kernel
   if (ms.stuck >= 0) mbar_wait_bounded(&merge_bar, (uint32_t)ms.stuck);
 }
 
-template <int D, int GP, int NS>
+template <typename T, int D, int GP, int NS>
 constexpr int sk_smem_bytes() {
   // stages + merge scratch (merge_heads query heads per pass) + align slack
-  return kWarps * NS * (2 * kTile * D * 2) + kWarps * merge_heads<D, GP>() * D * 4 + 1024;
+  return kWarps * NS * (2 * kTile * D * (int)sizeof(T)) + kWarps * merge_heads<D, GP>() * D * 4 + 1024;
 }
 
-// pipeline depth: 3 (head_dim 128) or 4 (head_dim 64) stages of 16 tokens per warp; at 64 the
-// same bytes stay in flight per SM with three CTAs (4 stages: D64 decode 0.75 -> 0.81 of the copy
-// peak against 6 stages and two CTAs)
-template <int D>
+// pipeline depth: bf16 3 (head_dim 128) or 4 (head_dim 64) stages of 16 tokens per warp; at 64
+// the same bytes stay in flight per SM with three CTAs (4 stages: D64 decode 0.75 -> 0.81 of
+// the copy peak against 6 stages and two CTAs).  fp32: 3 stages (192 KB at 128, one CTA per
+// SM; 96 KB at 64, two).
+template <typename T, int D>
 constexpr int stages() {
-  return D == 128 ? 3 : 4;
+  return sizeof(T) == 2 && D == 64 ? 4 : 3;
 }
 
-template <int D, int GP>
+template <typename T, int D, int GP>
 cudaError_t configure_one(int* ctas_per_sm) {
-  constexpr int NS = stages<D>();
-  cudaError_t e = cudaFuncSetAttribute(decode_sk_kernel<D, GP, NS>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       sk_smem_bytes<D, GP, NS>());
+  constexpr int NS = stages<T, D>();
+  cudaError_t e = cudaFuncSetAttribute(decode_sk_kernel<T, D, GP, NS>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       sk_smem_bytes<T, D, GP, NS>());
   if (e != cudaSuccess) return e;
-  return cudaOccupancyMaxActiveBlocksPerMultiprocessor(ctas_per_sm, decode_sk_kernel<D, GP, NS>, kWarps * 32,
-                                                       sk_smem_bytes<D, GP, NS>());
+  return cudaOccupancyMaxActiveBlocksPerMultiprocessor(ctas_per_sm, decode_sk_kernel<T, D, GP, NS>, kWarps * 32,
+                                                       sk_smem_bytes<T, D, GP, NS>());
 }
 
-template <int D, int GP>
+template <typename T, int D, int GP>
 cudaError_t launch_one(const DecodeArgs& a, const CUtensorMap* tmap, int ctas, cudaStream_t st) {
-  constexpr int NS = stages<D>();
+  constexpr int NS = stages<T, D>();
   // programmatic dependent launch: the CTAs may become resident while the previous kernel in
   // the stream finishes; they wait for it (griddepcontrol.wait) before reading anything
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)ctas);
   cfg.blockDim = dim3(kWarps * 32);
-  cfg.dynamicSmemBytes = sk_smem_bytes<D, GP, NS>();
+  cfg.dynamicSmemBytes = sk_smem_bytes<T, D, GP, NS>();
   cfg.stream = st;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  cudaError_t e = cudaLaunchKernelEx(&cfg, decode_sk_kernel<D, GP, NS>, *tmap, a);
+  cudaError_t e = cudaLaunchKernelEx(&cfg, decode_sk_kernel<T, D, GP, NS>, *tmap, a);
   count_launches(1);
   return e != cudaSuccess ? e : cudaGetLastError();
+}
+
+template <int D>
+cudaError_t configure_dim(int dtype, int ctas_per_sm[kGroupPads]) {
+  cudaError_t e;
+  if (dtype == HWKV_F32) {  // fp32: one instance, up to 4 query heads per KV head
+    ctas_per_sm[1] = ctas_per_sm[2] = 0;
+    return configure_one<float, D, 4>(&ctas_per_sm[0]);
+  }
+  if ((e = configure_one<__nv_bfloat16, D, 4>(&ctas_per_sm[0])) != cudaSuccess) return e;
+  if ((e = configure_one<__nv_bfloat16, D, 8>(&ctas_per_sm[1])) != cudaSuccess) return e;
+  return configure_one<__nv_bfloat16, D, 16>(&ctas_per_sm[2]);
+}
+
+template <typename T, int D>
+cudaError_t launch_dim(const DecodeArgs& a, const CUtensorMap* tmap, int ctas, cudaStream_t st) {
+  if constexpr (sizeof(T) == 4) {
+    return a.group <= 4 ? launch_one<T, D, 4>(a, tmap, ctas, st) : cudaErrorInvalidValue;
+  } else {
+    switch (decode_tc_group_pad(a.group)) {
+      case 4: return launch_one<T, D, 4>(a, tmap, ctas, st);
+      case 8: return launch_one<T, D, 8>(a, tmap, ctas, st);
+      default: return launch_one<T, D, 16>(a, tmap, ctas, st);
+    }
+  }
 }
 
 }  // namespace
@@ -631,32 +634,16 @@ int decode_tc_group_pad(int group) { return group <= 4 ? 4 : group <= 8 ? 8 : 16
 
 int decode_tc_pad_index(int group) { return group <= 4 ? 0 : group <= 8 ? 1 : 2; }
 
-template <int D>
-cudaError_t configure_dim(int ctas_per_sm[kGroupPads]) {
-  cudaError_t e;
-  if ((e = configure_one<D, 4>(&ctas_per_sm[0])) != cudaSuccess) return e;
-  if ((e = configure_one<D, 8>(&ctas_per_sm[1])) != cudaSuccess) return e;
-  return configure_one<D, 16>(&ctas_per_sm[2]);
-}
-
-cudaError_t configure_decode_tc(int head_dim, int ctas_per_sm[kGroupPads]) {
-  if (head_dim == 128) return configure_dim<128>(ctas_per_sm);
-  if (head_dim == 64) return configure_dim<64>(ctas_per_sm);
+cudaError_t configure_decode_tc(int head_dim, int dtype, int ctas_per_sm[kGroupPads]) {
+  if (head_dim == 128) return configure_dim<128>(dtype, ctas_per_sm);
+  if (head_dim == 64) return configure_dim<64>(dtype, ctas_per_sm);
   return cudaErrorInvalidValue;
 }
 
-template <int D>
-cudaError_t launch_dim(const DecodeArgs& a, const CUtensorMap* tmap, int ctas, cudaStream_t st) {
-  switch (decode_tc_group_pad(a.group)) {
-    case 4: return launch_one<D, 4>(a, tmap, ctas, st);
-    case 8: return launch_one<D, 8>(a, tmap, ctas, st);
-    default: return launch_one<D, 16>(a, tmap, ctas, st);
-  }
-}
-
 cudaError_t launch_decode_tc(const DecodeArgs& a, const CUtensorMap* tmap, int ctas, cudaStream_t st) {
-  if (a.pv.head_dim == 128) return launch_dim<128>(a, tmap, ctas, st);
-  if (a.pv.head_dim == 64) return launch_dim<64>(a, tmap, ctas, st);
+  const bool f32 = a.pv.elem_bytes == 4;
+  if (a.pv.head_dim == 128) return f32 ? launch_dim<float, 128>(a, tmap, ctas, st) : launch_dim<__nv_bfloat16, 128>(a, tmap, ctas, st);
+  if (a.pv.head_dim == 64) return f32 ? launch_dim<float, 64>(a, tmap, ctas, st) : launch_dim<__nv_bfloat16, 64>(a, tmap, ctas, st);
   return cudaErrorInvalidValue;
 }
 

@@ -1,6 +1,7 @@
-// Tile-level pieces of the tensor-core decode kernel (hwkv_decode_tc.cu): the (seq, kv head)
-// group of a step, the ring tiles it needs, the layout of a TMA tile in shared memory, the
-// loads of one tile, and the work of one warp on one 16-token tile.
+// Tile-level pieces of the stream-K decode kernel (hwkv_decode_tc.cu): the (seq, kv head) group
+// of a step, the ring tiles it needs, the layout of a TMA tile in shared memory, the loads of
+// one tile, and the work of one warp on one 16-token tile -- on the tensor cores for bf16
+// pools, on the CUDA cores for fp32 pools.
 //
 // "HeadWiseKV: Budgeted Per-Head Cache Residency for Hybrid Long-Context Language Models",
 // abstract and section "Grouped-Cache Runtime": attention reads only the materialised window
@@ -67,12 +68,16 @@ __device__ __forceinline__ long long range_start(long long T, int c, int n) { re
 // part whose range holds item t
 __device__ __forceinline__ int cta_of(long long t, long long T, int n) { return (int)(((t + 1) * n - 1) / T); }
 
-// Byte offset of element (row, d) of a 16-row tile stored as D/64 TMA boxes of [16 rows][64
-// elements] with the 128-byte swizzle: box hf = d / 64 at hf * 2048; inside a box row r is
-// the 128-byte line r and its 16-byte chunk c sits at chunk c ^ (r % 8).
-__device__ __forceinline__ uint32_t swz(int row, int d) {
-  return (uint32_t)((d >> 6) * 2048 + row * 128 + ((((d & 63) >> 3) ^ (row & 7)) << 4) + (d & 7) * 2);
+// Byte offset of element (row, d) of a 16-row tile of EB-byte elements stored as TMA boxes of
+// [16 rows][128 bytes] with the 128-byte swizzle: box hf = d * EB / 128 at hf * 2048; inside a
+// box row r is the 128-byte line r and its 16-byte chunk c sits at chunk c ^ (r % 8).
+template <int EB>
+__device__ __forceinline__ uint32_t swz_e(int row, int d) {
+  const int b = d * EB;
+  return (uint32_t)((b >> 7) * 2048 + row * 128 + ((((b & 127) >> 4) ^ (row & 7)) << 4) + (b & 15));
 }
+
+__device__ __forceinline__ uint32_t swz(int row, int d) { return swz_e<2>(row, d); }
 
 template <int W>
 __device__ __forceinline__ long long block_exclusive_scan(long long v, long long* s_warp, long long& total) {
@@ -116,6 +121,36 @@ __device__ __forceinline__ void load_q_frags(const DecodeArgs& a, const Group& g
   }
 }
 
+// Fused append: when the 16-token tile starting at ring slot t0 holds the new token's slot,
+// that row's copy in shared memory (sK / sV, EB-byte elements, 128-byte swizzle) is replaced
+// by k_new / v_new and the row is written to the pool; no other CTA reads this tile in the
+// launch.  Returns true then (the caller fences before TMA refills the stage).
+template <int EB, int D>
+__device__ __forceinline__ bool patch_new_row(const DecodeArgs& a, const Group& gr, int t0, int new_slot, uint32_t sK,
+                                              uint32_t sV, int lane) {
+  if (new_slot < t0 || new_slot >= t0 + kTile) return false;
+  constexpr int kRowBytes = D * EB;
+  constexpr int kRowVecs = kRowBytes / 16;  // 16-byte vectors per row
+  const int bs = a.pv.block_size;
+  const int r = new_slot - t0;
+  const int jb = new_slot / bs;
+  const int32_t blk = gr.tbl[jb];
+  const bool blk_ok = blk >= 0 && (int64_t)blk < a.pv.total_blocks;
+  const int64_t src = ((int64_t)gr.s * a.pv.kv_heads + gr.h) * kRowBytes;
+  char* dstk =
+      static_cast<char*>(a.pv.pool) + ((int64_t)(blk_ok ? blk : 0) * 2 * bs + (new_slot - jb * bs)) * kRowBytes;
+  for (int i = lane; i < 2 * kRowVecs; i += 32) {
+    const int kv = i / kRowVecs, c = i - kv * kRowVecs;
+    const uint4 val = *reinterpret_cast<const uint4*>(static_cast<const char*>(kv ? a.v_new : a.k_new) + src + c * 16);
+    const uint32_t sa = (kv ? sV : sK) + swz_e<EB>(r, c * (16 / EB));
+    asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(sa), "r"(val.x), "r"(val.y), "r"(val.z), "r"(val.w)
+                 : "memory");
+    if (blk_ok) *reinterpret_cast<uint4*>(dstk + (int64_t)kv * bs * kRowBytes + c * 16) = val;
+  }
+  __syncwarp();
+  return true;
+}
+
 // One warp's work on one 16-token tile of group `gr` whose first token sits in ring slot t0,
 // staged at sK (K rows) and sV (V rows):
 //   * fused append: when the tile holds the new token's slot, that row's copy in shared memory
@@ -130,9 +165,6 @@ __device__ __forceinline__ bool consume_tile(const DecodeArgs& a, const Group& g
                                              float (&acc)[D / 16][NT][4], float (&mx)[NT][2], float (&ls)[NT][2],
                                              int lane) {
   constexpr int kSteps = D / 16;
-  constexpr int kRowVecs = D * 2 / 16;  // 16-byte vectors per row
-  const int bs = a.pv.block_size;
-  const int H = a.pv.kv_heads;
   // ldmatrix lane roles: matrix mi = lane/8, row rr = lane%8
   const int mi = lane >> 3, rr = lane & 7;
   const int a_row = rr + ((mi & 1) << 3);   // K tile (non-transposed A operand): token row
@@ -142,27 +174,7 @@ __device__ __forceinline__ bool consume_tile(const DecodeArgs& a, const Group& g
   const int gq = lane >> 2;                 // accumulator roles: token/dim row
   const float sl2 = a.scale_log2;
 
-  bool patched = false;
-  if (new_slot >= t0 && new_slot < t0 + kTile) {
-    const int r = new_slot - t0;
-    const int jb = new_slot / bs;
-    const int32_t blk = gr.tbl[jb];
-    const bool blk_ok = blk >= 0 && (int64_t)blk < a.pv.total_blocks;
-    const int64_t src = ((int64_t)gr.s * H + gr.h) * D * 2;
-    char* dstk = static_cast<char*>(a.pv.pool) + ((int64_t)(blk_ok ? blk : 0) * 2 * bs + (new_slot - jb * bs)) * D * 2;
-    for (int i = lane; i < 2 * kRowVecs; i += 32) {
-      const int kv = i / kRowVecs, c = i - kv * kRowVecs;
-      const uint4 val =
-          *reinterpret_cast<const uint4*>(static_cast<const char*>(kv ? a.v_new : a.k_new) + src + c * 16);
-      const uint32_t sa = (kv ? sV : sK) + swz(r, c * 8);
-      asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(sa), "r"(val.x), "r"(val.y), "r"(val.z),
-                   "r"(val.w)
-                   : "memory");
-      if (blk_ok) *reinterpret_cast<uint4*>(dstk + (int64_t)kv * bs * D * 2 + c * 16) = val;
-    }
-    __syncwarp();
-    patched = true;
-  }
+  const bool patched = patch_new_row<2, D>(a, gr, t0, new_slot, sK, sV, lane);
 
   float sa[NT][4], sb[NT][4];
 #pragma unroll
@@ -225,14 +237,16 @@ __device__ __forceinline__ bool consume_tile(const DecodeArgs& a, const Group& g
 }
 
 // Issues the TMA loads of one 16-token tile (K rows and V rows of ring slot t0 of group `gr`)
-// into the stage at `dst`, completing on `bar`.  `through_l2`: read the table entry with an
-// L2 load (before the dependent-launch wait).  A bad table entry is flagged and block 0 read,
-// so the barrier accounting stays intact.
-template <int D>
+// of EB-byte elements into the stage at `dst`, completing on `bar`: D * EB / 128 boxes of
+// [16 rows][128 bytes] per K or V tile.  `through_l2`: read the table entry with an L2 load
+// (before the dependent-launch wait).  A bad table entry is flagged and block 0 read, so the
+// barrier accounting stays intact.
+template <int EB, int D>
 __device__ __forceinline__ void issue_tile(const CUtensorMap* tmap, const DecodeArgs& a, const Group& gr, int t0,
                                            uint32_t dst, uint64_t* bar, uint64_t policy, bool through_l2) {
-  constexpr int kHalves = D / 64;
-  constexpr int kTileBytes = kTile * D * 2;
+  constexpr int kBoxes = D * EB / 128;
+  constexpr int kBoxElems = 128 / EB;
+  constexpr int kTileBytes = kTile * D * EB;
   const int bs = a.pv.block_size;
   const int jb = t0 / bs;
   const int r0 = t0 - jb * bs;
@@ -245,11 +259,226 @@ __device__ __forceinline__ void issue_tile(const CUtensorMap* tmap, const Decode
   const int row_v = row_k + bs;
   mbar_arrive_expect_tx(bar, 2 * kTileBytes);
 #pragma unroll
-  for (int hf = 0; hf < kHalves; ++hf) {
-    tma_load_2d(dst + hf * 2048, tmap, hf * 64, row_k, bar, policy);
-    tma_load_2d(dst + kTileBytes + hf * 2048, tmap, hf * 64, row_v, bar, policy);
+  for (int hf = 0; hf < kBoxes; ++hf) {
+    tma_load_2d(dst + hf * 2048, tmap, hf * kBoxElems, row_k, bar, policy);
+    tma_load_2d(dst + kTileBytes + hf * 2048, tmap, hf * kBoxElems, row_v, bar, policy);
   }
 }
+
+// fp32 query, key and value rows: one warp's work on one 16-token tile of group `gr`, on the
+// CUDA cores (fp32 keeps full precision: no tensor-core rounding of the operands).  Lane l holds
+// dims [DPL*l, DPL*l + DPL) of every row (DPL = D / 32) and of q and of the accumulator of each
+// of the G <= 4 query heads; m, l (log2 units) are kept in every lane.
+//   * the 16 x 4 partial dot products of the tile are summed over the 32 lanes by a butterfly
+//     that halves the values a lane holds each round (62 shuffles for the tile, not 5 per dot):
+//     lane l ends with the scores of token l / 2, heads 2 (l % 2) and 2 (l % 2) + 1;
+//   * per head: tile maximum and, after exponentiation, tile sum over the 16 lanes of that
+//     parity, the online-softmax update (alpha = 2^(m_old - m_new));
+//   * P (16 x 4 fp32) goes through the warp's 64 floats of `p_s`, and O += P^T . V as FMAs.
+template <int D>
+__device__ __forceinline__ bool consume_tile_f32(const DecodeArgs& a, const Group& gr, int t0, int new_slot,
+                                                 uint32_t sK, uint32_t sV, const float (&q)[4][D / 32],
+                                                 float (&acc)[4][D / 32], float (&m)[4], float (&l)[4],
+                                                 float* p_s, int lane) {
+  constexpr int DPL = D / 32;
+  const bool patched = patch_new_row<4, D>(a, gr, t0, new_slot, sK, sV, lane);
+  float v[64];  // partial <q_g, k_t> over this lane's dims, index t * 4 + g
+#pragma unroll
+  for (int t = 0; t < kTile; ++t) {
+    float k[DPL];
+    const uint32_t ad = sK + swz_e<4>(t, lane * DPL);
+    if constexpr (DPL == 4) {
+      asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];" : "=f"(k[0]), "=f"(k[1]), "=f"(k[2]), "=f"(k[3]) : "r"(ad));
+    } else {
+      asm volatile("ld.shared.v2.f32 {%0, %1}, [%2];" : "=f"(k[0]), "=f"(k[1]) : "r"(ad));
+    }
+#pragma unroll
+    for (int g = 0; g < 4; ++g) {
+      float d = q[g][0] * k[0];
+#pragma unroll
+      for (int j = 1; j < DPL; ++j) d = fmaf(q[g][j], k[j], d);
+      v[t * 4 + g] = d;
+    }
+  }
+  // butterfly: at distance 16, 8, 4, 2, 1 a lane keeps the lower or upper half of its values
+  // (by that bit of its lane index) and adds the partner's copy of the same half
+#pragma unroll
+  for (int r = 0; r < 5; ++r) {
+    const int k = 16 >> r, half = 32 >> r;
+    const bool upper = (lane & k) != 0;
+#pragma unroll
+    for (int i = 0; i < half; ++i) {
+      const float send = upper ? v[i] : v[half + i];
+      const float keep = upper ? v[half + i] : v[i];
+      v[i] = keep + __shfl_xor_sync(0xffffffffu, send, k);
+    }
+  }
+  const int par = lane & 1;  // this lane's heads: 2 par, 2 par + 1
+  const bool valid = slot_valid(gr.rs, t0 + (lane >> 1));
+  const float sl2 = a.scale_log2;
+  const float s0 = valid ? v[0] * sl2 : kNegInf, s1 = valid ? v[1] * sl2 : kNegInf;
+  float x0 = s0, x1 = s1;
+#pragma unroll
+  for (int off = 2; off < 32; off <<= 1) {
+    x0 = fmaxf(x0, __shfl_xor_sync(0xffffffffu, x0, off));
+    x1 = fmaxf(x1, __shfl_xor_sync(0xffffffffu, x1, off));
+  }
+  const float y0 = __shfl_xor_sync(0xffffffffu, x0, 1), y1 = __shfl_xor_sync(0xffffffffu, x1, 1);
+  const float tmax[4] = {par ? y0 : x0, par ? y1 : x1, par ? x0 : y0, par ? x1 : y1};
+  float base[4], alpha[4];
+#pragma unroll
+  for (int g = 0; g < 4; ++g) {
+    const float mn = fmaxf(m[g], tmax[g]);
+    base[g] = mn == kNegInf ? 0.f : mn;
+    alpha[g] = ex2(m[g] - base[g]);
+    m[g] = mn;
+  }
+  const float p0 = ex2(s0 - (par ? base[2] : base[0])), p1 = ex2(s1 - (par ? base[3] : base[1]));
+  float u0 = p0, u1 = p1;
+#pragma unroll
+  for (int off = 2; off < 32; off <<= 1) {
+    u0 += __shfl_xor_sync(0xffffffffu, u0, off);
+    u1 += __shfl_xor_sync(0xffffffffu, u1, off);
+  }
+  const float w0 = __shfl_xor_sync(0xffffffffu, u0, 1), w1 = __shfl_xor_sync(0xffffffffu, u1, 1);
+  const float tsum[4] = {par ? w0 : u0, par ? w1 : u1, par ? u0 : w0, par ? u1 : w1};
+#pragma unroll
+  for (int g = 0; g < 4; ++g) l[g] = fmaf(l[g], alpha[g], tsum[g]);
+  p_s[2 * lane] = p0;  // index t * 4 + g with t = lane / 2, g = 2 (lane % 2)
+  p_s[2 * lane + 1] = p1;
+  __syncwarp();
+#pragma unroll
+  for (int g = 0; g < 4; ++g)
+#pragma unroll
+    for (int j = 0; j < DPL; ++j) acc[g][j] *= alpha[g];
+  const uint32_t ps_addr = smem_addr(p_s);
+#pragma unroll
+  for (int t = 0; t < kTile; ++t) {
+    float p[4], vv[DPL];
+    asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];" : "=f"(p[0]), "=f"(p[1]), "=f"(p[2]), "=f"(p[3])
+                 : "r"(ps_addr + t * 16));
+    const uint32_t ad = sV + swz_e<4>(t, lane * DPL);
+    if constexpr (DPL == 4) {
+      asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];" : "=f"(vv[0]), "=f"(vv[1]), "=f"(vv[2]), "=f"(vv[3])
+                   : "r"(ad));
+    } else {
+      asm volatile("ld.shared.v2.f32 {%0, %1}, [%2];" : "=f"(vv[0]), "=f"(vv[1]) : "r"(ad));
+    }
+#pragma unroll
+    for (int g = 0; g < 4; ++g)
+#pragma unroll
+      for (int j = 0; j < DPL; ++j) acc[g][j] = fmaf(p[g], vv[j], acc[g][j]);
+  }
+  __syncwarp();  // p_s is rewritten by the next tile
+  return patched;
+}
+
+// The state one warp carries through a segment, by element type.
+template <typename T, int D, int GP>
+struct WarpState;
+
+// bf16: the GQA group on the N side of mma.sync (GP columns in 8-column n-tiles), fp32
+// accumulators in the mma layout; ls holds this lane's partial row sums until finish().
+template <int D, int GP>
+struct WarpState<__nv_bfloat16, D, GP> {
+  static constexpr int NT = (GP + 7) / 8;
+  static constexpr int kEB = 2;
+  uint32_t qf[NT][D / 16][2];
+  float acc[D / 16][NT][4];
+  float mx[NT][2], ls[NT][2];
+
+  __device__ __forceinline__ void begin(const DecodeArgs& a, const Group& gr, int G, int lane) {
+    load_q_frags<D, NT>(a, gr, G, lane, qf);
+#pragma unroll
+    for (int j = 0; j < D / 16; ++j)
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt) acc[j][nt][0] = acc[j][nt][1] = acc[j][nt][2] = acc[j][nt][3] = 0.f;
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) mx[nt][0] = mx[nt][1] = kNegInf, ls[nt][0] = ls[nt][1] = 0.f;
+  }
+  __device__ __forceinline__ bool consume(const DecodeArgs& a, const Group& gr, int t0, int new_slot, uint32_t sK,
+                                          uint32_t sV, float*, int lane) {
+    return consume_tile<D, NT>(a, gr, t0, new_slot, sK, sV, qf, acc, mx, ls, lane);
+  }
+  __device__ __forceinline__ void finish() {
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+      for (int off = 4; off < 32; off <<= 1) {
+        ls[nt][0] += __shfl_xor_sync(0xffffffffu, ls[nt][0], off);
+        ls[nt][1] += __shfl_xor_sync(0xffffffffu, ls[nt][1], off);
+      }
+  }
+  // this warp's states of query heads [8 nt + hh SG, 8 nt + (hh + 1) SG) into the merge scratch
+  template <int SG>
+  __device__ __forceinline__ void publish(int nt, int hh, int warp, int lane, float* sc_m, float* sc_l,
+                                          float* sc_acc) const {
+    const int gq = lane >> 2, q4 = lane & 3;
+    const int c0 = 2 * q4 - hh * SG;  // this lane's first column within the pass
+    if (c0 < 0 || c0 >= SG) return;
+    if (gq == 0) {
+      sc_m[warp * SG + c0] = mx[nt][0];
+      sc_m[warp * SG + c0 + 1] = mx[nt][1];
+      sc_l[warp * SG + c0] = ls[nt][0];
+      sc_l[warp * SG + c0 + 1] = ls[nt][1];
+    }
+    float* wacc = sc_acc + warp * SG * D;
+#pragma unroll
+    for (int j = 0; j < D / 16; ++j) {
+      const int d = 16 * j + gq;
+      wacc[c0 * D + d] = acc[j][nt][0];
+      wacc[(c0 + 1) * D + d] = acc[j][nt][1];
+      wacc[c0 * D + d + 8] = acc[j][nt][2];
+      wacc[(c0 + 1) * D + d + 8] = acc[j][nt][3];
+    }
+  }
+};
+
+// fp32: CUDA-core tile work (consume_tile_f32), up to 4 query heads.
+template <int D, int GP>
+struct WarpState<float, D, GP> {
+  static_assert(GP == 4, "fp32 tile decode holds 4 query-head columns");
+  static constexpr int NT = 1;
+  static constexpr int kEB = 4;
+  static constexpr int DPL = D / 32;
+  float q[4][DPL], acc[4][DPL], m[4], l[4];
+
+  __device__ __forceinline__ void begin(const DecodeArgs& a, const Group& gr, int G, int lane) {
+    const int Hq = a.pv.kv_heads * G;
+    const float* qrow = static_cast<const float*>(a.q) + ((int64_t)gr.s * Hq + gr.h * G) * D + lane * DPL;
+#pragma unroll
+    for (int g = 0; g < 4; ++g) {
+#pragma unroll
+      for (int j = 0; j < DPL; ++j) {
+        q[g][j] = g < G ? qrow[g * D + j] : 0.f;
+        acc[g][j] = 0.f;
+      }
+      m[g] = kNegInf;
+      l[g] = 0.f;
+    }
+  }
+  __device__ __forceinline__ bool consume(const DecodeArgs& a, const Group& gr, int t0, int new_slot, uint32_t sK,
+                                          uint32_t sV, float* p_s, int lane) {
+    return consume_tile_f32<D>(a, gr, t0, new_slot, sK, sV, q, acc, m, l, p_s, lane);
+  }
+  __device__ __forceinline__ void finish() {}
+  template <int SG>
+  __device__ __forceinline__ void publish(int, int, int warp, int lane, float* sc_m, float* sc_l,
+                                          float* sc_acc) const {
+    static_assert(SG == 4, "one merge pass of 4 query heads");
+    if (lane == 0) {
+#pragma unroll
+      for (int g = 0; g < 4; ++g) {
+        sc_m[warp * SG + g] = m[g];
+        sc_l[warp * SG + g] = l[g];
+      }
+    }
+#pragma unroll
+    for (int g = 0; g < 4; ++g)
+#pragma unroll
+      for (int j = 0; j < DPL; ++j) sc_acc[(warp * SG + g) * D + lane * DPL + j] = acc[g][j];
+  }
+};
 
 }  // namespace
 }  // namespace hwkv

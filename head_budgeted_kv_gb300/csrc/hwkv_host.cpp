@@ -189,7 +189,8 @@ struct hwkv_pool {
   int64_t max_layer_tiles = 0;  // most 16-token ring tiles of one layer (all sequences and heads)
   int kernel_choice = HWKV_KERNEL_AUTO;
   std::vector<LayerPlan> plans;
-  bool has_tmap = false;
+  bool has_tmap = false;       // the pool's 2-D tensor map (16-row tiles)
+  bool has_stage_map = false;  // bf16: the 3-D stage map of the prefill
   alignas(64) CUtensorMap tmap;
   // the pool as (head_dim, 2 * block_size rows, block): one box of stage_tb rows of 64 / stage_tb
   // consecutive blocks is 64 keys (K or V) of a prefill stage
@@ -203,14 +204,21 @@ struct hwkv_pool {
 
 namespace {
 
+// The stream-K decode kernel takes bf16 pools (tensor cores) and fp32 pools (CUDA cores, up to
+// 4 query heads per KV head) whose block size is a multiple of 16 (one TMA box of 16 rows).
 bool tc_eligible(const hwkv_pool* p) {
-  return p->g.dtype == HWKV_BF16 && p->g.block_size % 16 == 0 && p->has_tmap;
+  return (p->g.dtype == HWKV_BF16 || p->g.dtype == HWKV_F32) && p->g.block_size % 16 == 0 && p->has_tmap;
 }
 
-bool use_tc(const hwkv_pool* p) {
+bool tc_group_ok(const hwkv_pool* p, int group) { return p->g.dtype == HWKV_BF16 || group <= 4; }
+
+bool use_tc(const hwkv_pool* p, int group) {
   if (p->kernel_choice == HWKV_KERNEL_SIMT) return false;
-  return tc_eligible(p);
+  return tc_eligible(p) && tc_group_ok(p, group);
 }
+
+// chunked prefill: bf16 pools with the 3-D stage map
+bool prefill_eligible(const hwkv_pool* p) { return p->g.dtype == HWKV_BF16 && tc_eligible(p) && p->has_stage_map; }
 
 void plan_decode(hwkv_pool* p) {
   const Geometry& g = p->g;
@@ -413,7 +421,7 @@ uint64_t align256(uint64_t x) { return (x + 255) & ~uint64_t(255); }
 WorkspaceLayout workspace_layout(const hwkv_pool* p, int group) {
   WorkspaceLayout w;
   const int64_t groups = (int64_t)p->g.num_seqs * p->g.kv_heads;
-  if (use_tc(p)) {
+  if (use_tc(p, group)) {
     w.slots1 = groups + tc_workers(p, group);
     w.slots2 = groups * merge_blocks_for(tc_workers(p, group));
   } else {
@@ -586,6 +594,21 @@ int hwkv_pool_create(int layers, int kv_heads, int head_dim, int block_size, con
     return cleanup_fail("zero-fill of the pool", e);
   if ((e = cudaStreamSynchronize(st)) != cudaSuccess) return cleanup_fail("cudaStreamSynchronize", e);
 
+  if (p->g.dtype == HWKV_F32 && p->g.block_size % 16 == 0) {
+    // fp32: boxes of 16 rows x 32 elements (128 bytes), the decode kernel's tiles
+    PFN_cuTensorMapEncodeTiled_v12000 encode = tensor_map_encoder();
+    if (encode) {
+      const int64_t rows = p->g.total_blocks * 2 * p->g.block_size;
+      cuuint64_t dims[2] = {(cuuint64_t)p->g.head_dim, (cuuint64_t)rows};
+      cuuint64_t strides[1] = {(cuuint64_t)p->g.head_dim * 4};
+      cuuint32_t box[2] = {32, 16};
+      cuuint32_t estr[2] = {1, 1};
+      CUresult cr = encode(&p->tmap, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, p->dev_pool, dims, strides, box, estr,
+                           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+      p->has_tmap = cr == CUDA_SUCCESS;
+    }
+  }
   if (p->g.dtype == HWKV_BF16 && p->g.block_size % 16 == 0) {
     PFN_cuTensorMapEncodeTiled_v12000 encode = tensor_map_encoder();
     if (encode) {
@@ -608,10 +631,11 @@ int hwkv_pool_create(int layers, int kv_heads, int head_dim, int block_size, con
                             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
       p->stage_tb = (bs == 16 || bs == 32 || bs % 64 == 0) ? tb : 0;
       p->has_tmap = cr == CUDA_SUCCESS && cr2 == CUDA_SUCCESS;
+      p->has_stage_map = p->has_tmap;
     }
   }
   if (p->has_tmap) {
-    e = configure_decode_tc(p->g.head_dim, p->ctas_per_sm);
+    e = configure_decode_tc(p->g.head_dim, p->g.dtype, p->ctas_per_sm);
     if (e != cudaSuccess) return cleanup_fail("cudaFuncSetAttribute", e);
   }
   plan_decode(p);
@@ -783,7 +807,7 @@ int decode_common(hwkv_pool_t p, int layer, const void* q, int q_heads, float sc
   }
   const int G = q_heads / g.kv_heads;
   const LayerPlan& lp = p->plans[layer];
-  const bool tc = use_tc(p);
+  const bool tc = use_tc(p, G);
   const uint64_t need = workspace_bytes(p, G);
   if (tc || lp.multi_chunk) {
     if (!workspace || ws_bytes < need)
@@ -794,8 +818,9 @@ int decode_common(hwkv_pool_t p, int layer, const void* q, int q_heads, float sc
   int rc = check_device(p);
   if (rc != HWKV_OK) return rc;
   NvtxRange range_(len_add ? "hwkv_append_decode_attn" : "hwkv_decode_attn", layer);
-  if (p->kernel_choice == HWKV_KERNEL_TENSOR && !tc_eligible(p))
-    return fail(HWKV_ERR_UNSUPPORTED, "tensor-core decode needs bf16 and block_size % 16 == 0");
+  if (p->kernel_choice == HWKV_KERNEL_TENSOR && !(tc_eligible(p) && tc_group_ok(p, G)))
+    return fail(HWKV_ERR_UNSUPPORTED,
+                "the stream-K decode needs block_size % 16 == 0, and up to 4 query heads per KV head for fp32");
 
   DecodeArgs a;
   std::memset(&a, 0, sizeof a);
@@ -921,7 +946,7 @@ int hwkv_prefill_attn(hwkv_pool_t p, int layer, const void* q, int q_heads, floa
   if (!p) return fail(HWKV_ERR_INVALID_ARG, "pool is NULL");
   const Geometry& g = p->g;
   if (layer < 0 || layer >= g.layers) return fail(HWKV_ERR_INVALID_ARG, "layer %d out of range", layer);
-  if (!tc_eligible(p)) return fail(HWKV_ERR_UNSUPPORTED, "prefill needs a bf16 pool with block_size % 16 == 0");
+  if (!prefill_eligible(p)) return fail(HWKV_ERR_UNSUPPORTED, "prefill needs a bf16 pool with block_size % 16 == 0");
   if (q_heads < g.kv_heads || q_heads % g.kv_heads != 0)
     return fail(HWKV_ERR_UNSUPPORTED, "q_heads must be a multiple of kv_heads");
   const int G = q_heads / g.kv_heads;
@@ -1010,7 +1035,7 @@ int hwkv_set_decode_config(hwkv_pool_t p, int split_tokens, int workers, int ker
   if (kernel != HWKV_KERNEL_AUTO && kernel != HWKV_KERNEL_TENSOR && kernel != HWKV_KERNEL_SIMT)
     return fail(HWKV_ERR_INVALID_ARG, "unknown kernel %d", kernel);
   if (kernel == HWKV_KERNEL_TENSOR && !tc_eligible(p))
-    return fail(HWKV_ERR_UNSUPPORTED, "tensor-core decode needs bf16 and block_size % 16 == 0");
+    return fail(HWKV_ERR_UNSUPPORTED, "the stream-K decode needs block_size % 16 == 0");
   p->split_override = split_tokens;
   p->workers_override = workers;
   p->kernel_choice = kernel;

@@ -113,9 +113,10 @@ cudaError_t launch_advance_positions(const int32_t* in, int32_t* out, int n, int
 // max_rows: the most positions any (seq, head) of the layer copies, min(max window, max_len)
 cudaError_t launch_materialize(const CopyArgs& a, int dtype, int max_rows, cudaStream_t st);
 // once per device before the first launch; returns resident CTAs per SM of the instances
-// for 4, 8 and 16 query-head columns
-cudaError_t configure_decode_tc(int head_dim, int ctas_per_sm[kGroupPads]);
-// tensor-core kernel: `ctas` persistent CTAs split the resident tiles of the layer evenly
+// for 4, 8 and 16 query-head columns (fp32 pools: 4 only, the others 0)
+cudaError_t configure_decode_tc(int head_dim, int dtype, int ctas_per_sm[kGroupPads]);
+// stream-K kernel (tensor cores for bf16, CUDA cores for fp32 with group <= 4): `ctas`
+// persistent CTAs split the resident tiles of the layer evenly
 cudaError_t launch_decode_tc(const DecodeArgs& a, const CUtensorMap* tmap, int ctas, cudaStream_t st);
 int decode_tc_group_pad(int group);  // query-head columns the kernel instance holds (4, 8 or 16)
 int decode_tc_pad_index(int group);  // 0, 1, 2 for 4, 8, 16 columns

@@ -61,9 +61,10 @@ extern "C" {
 #define HWKV_BF16 1
 
 /* decode kernel selection for hwkv_set_decode_config */
-#define HWKV_KERNEL_AUTO 0   /* tensor-core kernel where supported, else CUDA-core kernel */
-#define HWKV_KERNEL_TENSOR 1 /* bf16, bs % 16 == 0 only                                     */
-#define HWKV_KERNEL_SIMT 2   /* CUDA-core kernel, any supported shape                          */
+#define HWKV_KERNEL_AUTO 0   /* stream-K kernel where supported, else the split kernel       */
+#define HWKV_KERNEL_TENSOR 1 /* stream-K kernel: tensor cores for bf16, CUDA cores for fp32
+                                (fp32: up to 4 query heads per KV head); bs % 16 == 0 only  */
+#define HWKV_KERNEL_SIMT 2   /* split-K CUDA-core kernel, any supported shape                  */
 
 /* bits of the device error word */
 #define HWKV_DEVERR_NEG_LENGTH 1     /* a length / position below 0                    */

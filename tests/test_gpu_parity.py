@@ -36,9 +36,11 @@ def _check_all_pool_blocks(run: Run):
 # ---------------------------------------------------------------------------------------
 # the tiny fp32 workload: everything, every step
 # ---------------------------------------------------------------------------------------
-def test_tiny_fp32_every_step_every_head():
+@pytest.mark.parametrize("kernel", [hw.HWKV_KERNEL_AUTO, hw.HWKV_KERNEL_SIMT])
+def test_tiny_fp32_every_step_every_head(kernel):
+    """The fp32 workload through the stream-K kernel (automatic choice) and the split kernel."""
     cfg = workloads.config("tiny")
-    run = Run(cfg)
+    run = Run(cfg, kernel=kernel)
     exp_bytes = oracle.pool_bytes(cfg.windows_array(), cfg.batch, cfg.head_dim, cfg.block_size, cfg.elem_bytes)
     assert run.pool.nbytes == exp_bytes == 81920
     assert run.pool.geometry()[0] == exp_bytes
@@ -96,8 +98,11 @@ EDGE = {
                         prefill=(5000, 700, 64)),
     # odd block size -> CUDA-core kernel
     "bs5": dict(kv_heads=2, block_size=5, windows=((23, 60),), prefill=(100, 9)),
-    # fp32 with several layers and GQA 4
+    # fp32 with several layers and GQA 4 (stream-K tiles), GQA 8 (split kernel), head_dim 64
     "f32": dict(layers=2, kv_heads=2, dtype="f32", head_dim=128, windows=((100, 37), (16, 300)), prefill=(400, 20)),
+    "f32_g8": dict(kv_heads=2, group=8, dtype="f32", head_dim=128, windows=((700, 48),), prefill=(900, 30)),
+    "f32_d64_long": dict(kv_heads=3, group=3, dtype="f32", head_dim=64, windows=((4096, 64, 1000),),
+                         prefill=(5000, 20)),
     # spiky keys (x8) as in the ragged workload
     "spikes": dict(kv_heads=2, windows=((1024, 512),), prefill=(2000, 1500), spike_frac=0.05),
 }
@@ -366,6 +371,38 @@ def _random_case(seed: int):
     cfg = small_config(name=f"random{seed}", cfg_id=200 + seed, layers=layers, kv_heads=kv_heads, group=group,
                        head_dim=head_dim, block_size=block_size, windows=windows, prefill=prefill, steps=2)
     return cfg, fused, workers
+
+
+def _random_case_f32(seed: int):
+    """As _random_case, fp32 pools: up to 4 query heads per KV head take the stream-K kernel
+    (CUDA-core tiles), more the split kernel."""
+    rng = np.random.default_rng(3000 + seed)
+    kv_heads = int(rng.integers(1, 5))
+    group = int(rng.choice([1, 2, 3, 4, 4, 6]))
+    layers = int(rng.integers(1, 3))
+    batch = int(rng.integers(1, 4))
+    windows = tuple(tuple(int(rng.choice([int(rng.integers(1, 200)), 256, 1000, 4096]))
+                          for _ in range(kv_heads)) for _ in range(layers))
+    prefill = tuple(int(rng.integers(0, 5000)) for _ in range(batch))
+    cfg = small_config(name=f"random_f32_{seed}", cfg_id=300 + seed, layers=layers, kv_heads=kv_heads, group=group,
+                       head_dim=int(rng.choice([64, 128])), block_size=int(rng.choice([16, 32, 64])),
+                       dtype="f32", windows=windows, prefill=prefill, steps=2)
+    return cfg, bool(rng.integers(0, 2)), int(rng.choice([0, 0, 1, 5, 64, 500]))
+
+
+@pytest.mark.parametrize("seed", range(8))
+def test_random_f32_geometries_match_the_oracle(seed):
+    cfg, fused, workers = _random_case_f32(seed)
+    run = Run(cfg, fused=fused, workers=workers)
+    run.materialize()
+    for i in range(cfg.steps):
+        res = run.step(keep_layers=range(cfg.layers))
+        for l, (q_raw, got) in res.items():
+            ref = run.reference(i, l, q_raw)
+            assert_close(got, ref, cfg, f"random f32 {seed} (fused {fused}, workers {workers}) step {i} layer {l}")
+    _check_all_pool_blocks(run)
+    assert run.device_errors() == 0
+    run.close()
 
 
 @pytest.mark.parametrize("seed", range(16))
