@@ -34,11 +34,12 @@ sys.path.insert(0, ROOT)
 METRIC = "decode tokens/s and resident-KV HBM GB/s (fraction of GB300 peak), 1 GPU"
 FALLBACK_HBM_GBS = 6800.0
 
-# dram__bytes_read.sum + dram__bytes_write.sum per decode launch from one ncu capture of
-# the tensor-core decode kernel, with the sha256 of hwkv_decode_tc.cu it was taken on.  When
-# the kernel source changes the figure no longer applies and is reported as null.
-DECODE_TRAFFIC = {"source_sha256": "2713eb527014c59ef868f1168f40222c47e18470ab5f3b3fc9db627c8656f95e",
-                  "bytes_per_launch": (621.362176 + 3.148288 + 489.192960 + 0.108800) / 2 * 1e6,
+# dram__bytes_read.sum + dram__bytes_write.sum per decode launch from one ncu capture of the
+# stream-K decode kernel, with the sha256 of its sources (hwkv_decode_tc.cu, then
+# hwkv_decode_tile.cuh) it was taken on.  When the kernel source changes the figure no longer
+# applies and is reported as null.
+DECODE_TRAFFIC = {"source_sha256": "c2e7e396276721e117cac3ed075e8d1a9d59c7e6465648790106efa4db33c90b",
+                  "bytes_per_launch": (621.387008 + 2.754048 + 489.207552 + 0.464896) / 2 * 1e6,
                   "launch": "layers 0 and 1 of the full workload (2-layer run, same per-launch shape)"}
 
 
@@ -154,8 +155,11 @@ def measured_peak():
 
 
 def decode_source_sha() -> str:
-    with open(os.path.join(ROOT, "head_budgeted_kv_gb300", "csrc", "hwkv_decode_tc.cu"), "rb") as f:
-        return hashlib.sha256(f.read()).hexdigest()
+    h = hashlib.sha256()
+    for name in ("hwkv_decode_tc.cu", "hwkv_decode_tile.cuh"):
+        with open(os.path.join(ROOT, "head_budgeted_kv_gb300", "csrc", name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()
 
 
 # --------------------------------------------------------------------------------------
@@ -717,6 +721,8 @@ def run_shapes(args):
     peak, peak_kind = measured_peak()
     rows = []
     for label, kw in SHAPES:
+        if args.shape and args.shape != label:
+            continue
         cfg = dataclasses.replace(workloads.config("full").with_layers(8), name="full_8l", **kw)
         wl = workloads.Workload(cfg, device=dev)
         pool = hw.Pool(cfg.layers, cfg.kv_heads, cfg.head_dim, cfg.block_size, cfg.windows_array(), cfg.batch,
@@ -964,6 +970,7 @@ def main(argv=None):
     p.add_argument("--graph", action="store_true", help="replay each decode step as one captured CUDA graph")
     p.add_argument("--mode", choices=["decode", "prefill", "shapes"], default="decode")
     p.add_argument("--chunk", type=int, default=2048, help="prefill mode: tokens per sequence per chunk")
+    p.add_argument("--shape", default="", help="shapes mode: measure only this shape (e.g. 'fp32 D128 GQA4')")
     p.add_argument("--prefill-max-stages", type=int, default=0,
                    help="prefill mode: split key streams longer than this many 64-key stages (0 = automatic)")
     p.add_argument("--kernel", type=int, default=0)
