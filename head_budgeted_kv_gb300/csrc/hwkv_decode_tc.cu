@@ -142,13 +142,14 @@ __device__ __forceinline__ void merge_slots_regs(const float* src_acc, const flo
 constexpr uint32_t kBulkChunk = 16384;  // bytes per bulk copy of a partial block
 
 // Shared-memory resources a merge may use: the stage buffers (free once the CTA has consumed
-// its last tile), an mbarrier for the bulk copy and the phase it is at.
+// its last tile), two mbarriers for bulk copies into them and the phases they are at.
 struct MergeStage {
-  float* buf;      // null: not available
+  float* buf;               // null: not available
   uint32_t bytes;
-  uint64_t* bar;
-  uint32_t phase;  // completed uses of `bar` (uniform in the CTA)
-  int stuck;       // parity of a use whose wait timed out, else -1
+  uint64_t* bar0;           // copies into the whole buffer or its first half ...
+  uint64_t* bar1;           // ... and into its second half
+  uint32_t phase0, phase1;  // completed uses of bar0 / bar1 (uniform in the CTA)
+  int stuck0, stuck1;       // parity of a use that may still be in flight after a timeout, else -1
 };
 
 // Folds `count` consecutive partial slots [first, first + count) into the output or partial
@@ -162,7 +163,7 @@ struct MergeStage {
 // the same arithmetic, so an output does not depend on which path its last arriver took.
 // `live(i)` tells whether slot first + i holds a partial.
 template <typename T, int D, typename Live>
-__device__ __forceinline__ void merge_slots(const float* src_acc, const float* src_ml, long long first, int count,
+__device__ __forceinline__ void merge_slots_one(const float* src_acc, const float* src_ml, long long first, int count,
                                             int G, Live live, bool dense, T* out_grp, float* dst_acc,
                                             float* dst_ml, long long dst_slot, float* s_ml, int ml_cap,
                                             MergeStage& ms, int32_t* err) {
@@ -174,10 +175,10 @@ __device__ __forceinline__ void merge_slots(const float* src_acc, const float* s
   if (threadIdx.x == 0) {
     // the partials were written and acquired, and the buffer last read, through the generic proxy
     fence_proxy_async_all();
-    mbar_arrive_expect_tx(ms.bar, bytes);
+    mbar_arrive_expect_tx(ms.bar0, bytes);
     const char* src = reinterpret_cast<const char*>(src_acc + first * G * D);
     for (uint32_t off = 0; off < bytes; off += kBulkChunk)
-      bulk_load(smem_addr(ms.buf) + off, src + off, bytes - off < kBulkChunk ? bytes - off : kBulkChunk, ms.bar);
+      bulk_load(smem_addr(ms.buf) + off, src + off, bytes - off < kBulkChunk ? bytes - off : kBulkChunk, ms.bar0);
   }
   for (int p = threadIdx.x; p < count * G; p += blockDim.x) {
     const float2 ml = __ldcg(reinterpret_cast<const float2*>(src_ml) + first * G + p);
@@ -185,8 +186,8 @@ __device__ __forceinline__ void merge_slots(const float* src_acc, const float* s
     s_ml[count * G + p] = ml.y;
   }
   __syncthreads();
-  const bool landed = mbar_wait_bounded(ms.bar, ms.phase & 1u);
-  ++ms.phase;
+  const bool landed = mbar_wait_bounded(ms.bar0, ms.phase0 & 1u);
+  ++ms.phase0;
   if (!landed && threadIdx.x == 0) atomicOr(err, HWKV_DEVERR_WAIT_TIMEOUT);
   constexpr int kV = D / 4;  // float4 columns per query head
   const float4* sacc = reinterpret_cast<const float4*>(ms.buf);
@@ -210,9 +211,148 @@ __device__ __forceinline__ void merge_slots(const float* src_acc, const float* s
     store_merged<T, D>(M, L, acc, q, d4, G, out_grp, dst_acc, dst_ml, dst_slot);
   }
   if (!landed) {  // a copy may still be in flight: no later merge reuses the buffer
-    ms.stuck = (int)((ms.phase - 1u) & 1u);
+    ms.stuck0 = (int)((ms.phase0 - 1u) & 1u);
     ms.buf = nullptr;
   }
+}
+
+// Folds `count` consecutive partial slots [first, first + count) into the output or partial
+// slot of store_merged.  When every slot holds a partial (`dense`), the stage buffers are free
+// and the accumulators fit them and the (m, l) of every (slot, head) fit `s_ml` (2 * count * G
+// <= ml_cap floats), the accumulators are fetched in one bulk copy while those (m, l) are read
+// into `s_ml`; each thread then forms its head's maximum M = max_i m_i and, slot after slot,
+// w_i = 2^(m_i - M), L = fma(l_i, w_i, L) and the sum of w_i * acc_i over its 4 columns out of
+// shared memory (the threads of a warp share a head, so the reads are broadcasts).  The whole
+// merge waits for about one round trip to L2.  Accumulators larger than the buffers (large GQA
+// groups: 8 KB per partial at 16 query heads) are merged in passes over subsets of the query
+// heads, one bulk copy per slot and pass, the next pass landing in one half of the buffers
+// while the previous one is summed out of the other.  Otherwise the register merge above runs.
+// Every path has the same arithmetic, so an output does not depend on which one its last
+// arriver took.  `live(i)` tells whether slot first + i holds a partial.
+template <typename T, int D, typename Live>
+__device__ __forceinline__ void merge_slots_passes(const float* src_acc, const float* src_ml, long long first, int count,
+                                            int G, Live live, bool dense, T* out_grp, float* dst_acc,
+                                            float* dst_ml, long long dst_slot, float* s_ml, int ml_cap,
+                                            MergeStage& ms, int32_t* err) {
+  constexpr int kV = D / 4;  // float4 columns per query head
+  const uint32_t bytes = (uint32_t)count * (uint32_t)G * D * 4u;
+  const bool one = bytes <= ms.bytes;
+  // heads per pass when the accumulators exceed the buffers: the largest power of two dividing
+  // G whose pass fits half the buffers and gives every column its own thread
+  int hp = one ? G : 0;
+  if (!one)
+    for (int h = G; h >= 1; h >>= 1)
+      if (G % h == 0 && (uint32_t)count * (uint32_t)h * D * 4u <= ms.bytes / 2u && h * kV <= (int)blockDim.x) {
+        hp = h;
+        break;
+      }
+  if (!dense || ms.buf == nullptr || 2 * count * G > ml_cap || hp == 0) {
+    merge_slots_regs<T, D>(src_acc, src_ml, first, count, G, live, out_grp, dst_acc, dst_ml, dst_slot);
+    return;
+  }
+  const int passes = G / hp;
+  const uint32_t pass_bytes = (uint32_t)count * (uint32_t)hp * D * 4u;
+  // pass p: heads [p hp, (p + 1) hp) of every slot, into half p % 2 (the whole buffer with one pass)
+  auto issue = [&](int p) {
+    uint64_t* bar = (p & 1) ? ms.bar1 : ms.bar0;
+    // the partials were written and acquired, and the buffer last read, through the generic proxy
+    fence_proxy_async_all();
+    mbar_arrive_expect_tx(bar, pass_bytes);
+    const uint32_t dst = smem_addr(ms.buf) + (uint32_t)(p & 1) * (ms.bytes / 2u);
+    if (one) {
+      const char* src = reinterpret_cast<const char*>(src_acc + first * G * D);
+      for (uint32_t off = 0; off < pass_bytes; off += kBulkChunk)
+        bulk_load(dst + off, src + off, pass_bytes - off < kBulkChunk ? pass_bytes - off : kBulkChunk, bar);
+    } else {
+      const uint32_t row = (uint32_t)hp * D * 4u;
+      for (int i = 0; i < count; ++i)
+        bulk_load(dst + (uint32_t)i * row, src_acc + ((first + i) * G + (long long)p * hp) * D, row, bar);
+    }
+  };
+  const uint32_t base0 = ms.phase0, base1 = ms.phase1;
+  if (threadIdx.x == 0) {
+    issue(0);
+    if (passes > 1) issue(1);
+  }
+  for (int p = threadIdx.x; p < count * G; p += blockDim.x) {
+    const float2 ml = __ldcg(reinterpret_cast<const float2*>(src_ml) + first * G + p);
+    s_ml[p] = ml.x;
+    s_ml[count * G + p] = ml.y;
+  }
+  __syncthreads();
+  ms.phase0 = base0 + (uint32_t)((passes + 1) / 2);
+  ms.phase1 = base1 + (uint32_t)(passes / 2);
+  // the weighted sum of heads [p hp, (p + 1) hp) out of the buffer half holding pass p
+  auto sum_pass = [&](int p, bool landed) {
+    const float4* sacc = reinterpret_cast<const float4*>(ms.buf) + (size_t)(p & 1) * (ms.bytes / 32u);
+    for (int e = threadIdx.x; e < hp * kV; e += blockDim.x) {
+      const int ql = e / kV, d4 = e - (e / kV) * kV;
+      const int q = p * hp + ql;
+      float M = kNegInf;
+      for (int i = 0; i < count; ++i) M = fmaxf(M, s_ml[i * G + q]);
+      float L = 0.f;
+      float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+      for (int i = 0; i < count; ++i) {
+        const float w = M == kNegInf ? 0.f : ex2(s_ml[i * G + q] - M);
+        L = fmaf(s_ml[count * G + i * G + q], w, L);
+        if (landed) {
+          const float4 v = sacc[(i * hp + ql) * kV + d4];
+          acc.x = fmaf(v.x, w, acc.x);
+          acc.y = fmaf(v.y, w, acc.y);
+          acc.z = fmaf(v.z, w, acc.z);
+          acc.w = fmaf(v.w, w, acc.w);
+        }
+      }
+      store_merged<T, D>(M, L, acc, q, d4, G, out_grp, dst_acc, dst_ml, dst_slot);
+    }
+  };
+  if (one) {  // every thread waits for the one copy itself: no CTA barrier on the merge chain
+    const bool landed = mbar_wait_bounded(ms.bar0, base0 & 1u);
+    if (!landed && threadIdx.x == 0) atomicOr(err, HWKV_DEVERR_WAIT_TIMEOUT);
+    sum_pass(0, landed);
+    if (!landed) {  // a copy may still be in flight: no later merge reuses the buffer
+      ms.stuck0 = (int)(base0 & 1u);
+      ms.buf = nullptr;
+    }
+    return;
+  }
+  bool ok = true;
+  for (int p = 0; p < passes; ++p) {
+    const int h = p & 1;
+    const uint32_t parity = ((h ? base1 : base0) + (uint32_t)(p >> 1)) & 1u;
+    ok = __syncthreads_and(ok && mbar_wait_bounded(h ? ms.bar1 : ms.bar0, parity));
+    sum_pass(p, ok);
+    if (!ok) {  // copies of this and the next pass may still be in flight: no later merge reuses the buffer
+      if (threadIdx.x == 0) atomicOr(err, HWKV_DEVERR_WAIT_TIMEOUT);
+      const int next = p + 1 < passes ? (int)(((h ? base0 : base1) + (uint32_t)((p + 1) >> 1)) & 1u) : -1;
+      if (h) {
+        ms.stuck1 = (int)parity;
+        ms.stuck0 = next;
+      } else {
+        ms.stuck0 = (int)parity;
+        ms.stuck1 = next;
+      }
+      ms.buf = nullptr;
+      break;
+    }
+    __syncthreads();  // half h is read: the copy of pass p + 2 may land there
+    if (threadIdx.x == 0 && p + 2 < passes) issue(p + 2);
+  }
+}
+
+// The merge of a group's partials: instances holding 16 query-head columns may meet partials
+// larger than the stage buffers and take the head-pass merge; the others the one-copy merge.
+template <typename T, int D, int GP, typename Live>
+__device__ __forceinline__ void merge_slots(const float* src_acc, const float* src_ml, long long first, int count,
+                                            int G, Live live, bool dense, T* out_grp, float* dst_acc,
+                                            float* dst_ml, long long dst_slot, float* s_ml, int ml_cap,
+                                            MergeStage& ms, int32_t* err) {
+  if constexpr (GP == 16)
+    merge_slots_passes<T, D>(src_acc, src_ml, first, count, G, live, dense, out_grp, dst_acc, dst_ml, dst_slot, s_ml,
+                             ml_cap, ms, err);
+  else
+    merge_slots_one<T, D>(src_acc, src_ml, first, count, G, live, dense, out_grp, dst_acc, dst_ml, dst_slot, s_ml,
+                          ml_cap, ms, err);
 }
 
 // Bumps an arrival counter and tells the whole CTA whether it arrived last; the last arriver
@@ -265,7 +405,7 @@ __global__ void __launch_bounds__(kWarps * 32, sk_min_ctas<Elem, D>())
   float* sc_acc = reinterpret_cast<float*>(smem + W * NS * kStageBytes);  // [W][SG][D]
   __shared__ __align__(8) uint64_t bars[W * NS];
   __shared__ float sc_m[W * SG], sc_l[W * SG];
-  __shared__ __align__(8) uint64_t merge_bar;  // bulk copies of partial blocks
+  __shared__ __align__(8) uint64_t merge_bar[2];  // bulk copies of partial blocks
   // the partial merge's (m, l) scratch reuses the warps' merge area: 2 * slots * G floats
   constexpr int kMlCap = W * SG * D;
   __shared__ long long s_scan[W];
@@ -332,7 +472,8 @@ __global__ void __launch_bounds__(kWarps * 32, sk_min_ctas<Elem, D>())
   }
   if (threadIdx.x == 0) {
     for (int i = 0; i < W * NS; ++i) mbar_init(&bars[i], 1);
-    mbar_init(&merge_bar, 1);
+    mbar_init(&merge_bar[0], 1);
+    mbar_init(&merge_bar[1], 1);
     fence_mbar_init();
   }
   __syncthreads();
@@ -420,7 +561,7 @@ __global__ void __launch_bounds__(kWarps * 32, sk_min_ctas<Elem, D>())
   int consumed = 0;
   int drain_from = -1;         // set when a wait timed out
   bool patched_stage = false;  // a generic-proxy write went into the stage just released
-  MergeStage ms{nullptr, (uint32_t)(W * NS * kStageBytes), &merge_bar, 0u, -1};
+  MergeStage ms{nullptr, (uint32_t)(W * NS * kStageBytes), &merge_bar[0], &merge_bar[1], 0u, 0u, -1, -1};
 
   for (;;) {
     // the segment: the group's tiles within the range
@@ -523,7 +664,7 @@ __global__ void __launch_bounds__(kWarps * 32, sk_min_ctas<Elem, D>())
           auto live = [&](int i) {
             return all_live || range_start(T, c_lo + i + 1, nctas) > range_start(T, c_lo + i, nctas);
           };
-          merge_slots<Elem, D>(a.part_acc, a.part_ml, (long long)sg + c_lo, k, G, live, all_live, out_grp, nullptr,
+          merge_slots<Elem, D, GP>(a.part_acc, a.part_ml, (long long)sg + c_lo, k, G, live, all_live, out_grp, nullptr,
                          nullptr, 0, sc_acc, kMlCap, ms, a.pv.err);
         }
       } else {
@@ -534,10 +675,10 @@ __global__ void __launch_bounds__(kWarps * 32, sk_min_ctas<Elem, D>())
         const int b_n = min(kMergeBlock, c_hi - b_lo + 1);
         const long long slot2 = (long long)sg * a.merge_blocks + b;
         if (arrive_last(&a.counters1[slot2], b_n, &s_last)) {
-          merge_slots<Elem, D>(a.part_acc, a.part_ml, (long long)sg + b_lo, b_n, G, live, true, (Elem*)nullptr, a.part2_acc,
+          merge_slots<Elem, D, GP>(a.part_acc, a.part_ml, (long long)sg + b_lo, b_n, G, live, true, (Elem*)nullptr, a.part2_acc,
                          a.part2_ml, slot2, sc_acc, kMlCap, ms, a.pv.err);
           if (arrive_last(&a.counters[sg], nb, &s_last))
-            merge_slots<Elem, D>(a.part2_acc, a.part2_ml, (long long)sg * a.merge_blocks, nb, G, live, true, out_grp,
+            merge_slots<Elem, D, GP>(a.part2_acc, a.part2_ml, (long long)sg * a.merge_blocks, nb, G, live, true, out_grp,
                            nullptr, nullptr, 0, sc_acc, kMlCap, ms, a.pv.err);
         }
       }
@@ -555,7 +696,8 @@ __global__ void __launch_bounds__(kWarps * 32, sk_min_ctas<Elem, D>())
     for (int c = drain_from; c < issued; ++c)
       if (!mbar_wait_bounded(&wbar[c % NS], (uint32_t)(c / NS) & 1u)) break;
   }
-  if (ms.stuck >= 0) mbar_wait_bounded(&merge_bar, (uint32_t)ms.stuck);
+  if (ms.stuck0 >= 0) mbar_wait_bounded(&merge_bar[0], (uint32_t)ms.stuck0);
+  if (ms.stuck1 >= 0) mbar_wait_bounded(&merge_bar[1], (uint32_t)ms.stuck1);
 }
 
 template <typename T, int D, int GP, int NS>

@@ -198,6 +198,25 @@ def test_long_window_merge_at_batch_one(workers):
         r.close()
 
 
+@pytest.mark.parametrize("head_dim,workers", [(128, 40), (128, 56), (64, 48), (64, 64)])
+def test_large_group_merge_in_head_passes(head_dim, workers):
+    """GQA 16: a partial is 16 x head_dim floats, so a one-level merge of 13-24 partials exceeds
+    the stage buffers and runs in passes over subsets of the query heads; it must match the
+    oracle and repeat bit for bit."""
+    cfg = small_config(name="bigg", kv_heads=2, group=16, head_dim=head_dim, windows=((8192, 4096),),
+                       prefill=(9000, 9000))
+    runs = [Run(cfg, kernel=hw.HWKV_KERNEL_TENSOR, workers=workers, fused=True) for _ in range(2)]
+    for r in runs:
+        r.materialize()
+    for i in range(2):
+        a, b = (r.step(keep_layers=[0]) for r in runs)
+        assert np.array_equal(a[0][1], b[0][1]), f"D{head_dim} workers {workers} step {i}"
+        assert_close(a[0][1], runs[0].reference(i, 0, a[0][0]), cfg, f"D{head_dim} workers {workers} step {i}")
+    for r in runs:
+        assert r.device_errors() == 0
+        r.close()
+
+
 @pytest.mark.parametrize("kernel", [hw.HWKV_KERNEL_TENSOR, hw.HWKV_KERNEL_SIMT])
 def test_launches_are_deterministic(kernel):
     """No output depends on which CTA arrives last at a merge: two pools driven with the same
