@@ -1,5 +1,7 @@
-// Tensor-core split-K decode attention over per-head paged rings (bf16, block_size % 16 == 0,
-// head_dim 64 or 128), optionally fused with the append of the step's new token.
+// Stream-K split-K decode attention over per-head paged rings (block_size % 16 == 0, head_dim
+// 64 or 128), optionally fused with the append of the step's new token: tile work on the
+// tensor cores for bf16 pools (up to 16 query heads per KV head), on the CUDA cores for fp32
+// pools (up to 4).
 //
 // "HeadWiseKV: Budgeted Per-Head Cache Residency for Hybrid Long-Context Language Models",
 // abstract and section "Grouped-Cache Runtime": attention reads only the materialised window
@@ -20,13 +22,16 @@
 // The sequence lengths are staged in shared memory once, so crossing into the next group
 // costs no global round trip.
 //
-// Per tile (16 tokens), per warp, with the GQA group (G <= 16 query heads, zero-padded to one
-// or two 8-column n-tiles) on the N side of mma.sync.m16n8k16 bf16 -> fp32:
+// Per tile (16 tokens), per warp, bf16 (hwkv_decode_tile.cuh, consume_tile), with the GQA
+// group (G <= 16 query heads, zero-padded to one or two 8-column n-tiles) on the N side of
+// mma.sync.m16n8k16 bf16 -> fp32:
 //   S[16 tok][8 q] = K_tile . Q^T over head_dim per n-tile (K tile loaded once with ldmatrix
 //   from the 128-byte-swizzled TMA tile and shared by the n-tiles), masked to resident slots,
 //   online softmax in fp32 in the log2 domain; P is moved from the accumulator layout to the
 //   operand layout with movmatrix.trans; O^T[D][8 q] = alpha * O^T + V_tile^T . P (V tile
 //   loaded once with ldmatrix.trans).
+// fp32 (consume_tile_f32): lanes own consecutive dims; the tile's 16 x 4 dot products are summed
+// over the warp by a butterfly transpose-reduction, P goes through shared memory for the FMAs.
 //
 // Waits are bounded (~2 s); a timeout records HWKV_DEVERR_WAIT_TIMEOUT and the warp stops.
 #include "hwkv_decode_tile.cuh"

@@ -165,14 +165,17 @@ int hwkv_decode_workspace_bytes(hwkv_pool_t pool, int q_heads, uint64_t* out);
  *     out[s][q] = sum_{p in [max(0,len_s-w), len_s)} softmax_p(scale * <q, k_p>) v_p
  * computed with fp32 accumulation and an online softmax; out has the pool's dtype.
  *   q, out: device [num_seqs][q_heads][D], 16-byte aligned; q_heads = G * kv_heads, G <= 16
- *           (the tensor-core kernel pads the group to 4, 8 or 16 query-head columns).
+ *           (the stream-K kernel pads the group to 4, 8 or 16 query-head columns on the
+ *           tensor cores for bf16 pools, to 4 on the CUDA cores for fp32 pools).
  *   lens_dev: device int32 [num_seqs], lengths AFTER this step's append.  len 0 gives 0s.
  *   workspace: device scratch of >= hwkv_decode_workspace_bytes(), 16-byte aligned; its
  *              contents need no initialisation and are clobbered.  Launches that may run
  *              at the same time need distinct workspaces.
- * The tensor-core kernel splits the layer's resident tiles evenly over a persistent grid and
+ * The stream-K kernel splits the layer's resident tiles evenly over a persistent grid and
  * merges partial results through per-(seq, head) arrival counters that the library keeps in
  * its own device memory (one set per layer); concurrent launches of the SAME layer race.
+ * Other shapes (block_size not a multiple of 16, fp32 groups above 4) take the split-K
+ * CUDA-core kernel and a merge kernel.
  * Errors: HWKV_ERR_INVALID_ARG, HWKV_ERR_ALIGNMENT, HWKV_ERR_WORKSPACE_TOO_SMALL,
  *         HWKV_ERR_UNSUPPORTED, HWKV_ERR_CUDA (launch failure). */
 int hwkv_decode_attn(hwkv_pool_t pool, int layer, const void* q, int q_heads, float scale,
