@@ -38,8 +38,8 @@ FALLBACK_HBM_GBS = 6800.0
 # stream-K decode kernel, with the sha256 of its sources (hwkv_decode_tc.cu, then
 # hwkv_decode_tile.cuh) it was taken on.  When the kernel source changes the figure no longer
 # applies and is reported as null.
-DECODE_TRAFFIC = {"source_sha256": "c2e7e396276721e117cac3ed075e8d1a9d59c7e6465648790106efa4db33c90b",
-                  "bytes_per_launch": (621.387008 + 2.754048 + 489.207552 + 0.464896) / 2 * 1e6,
+DECODE_TRAFFIC = {"source_sha256": "1c00563c90368234af1ad9540ba43971664c11ae329c77154a06aa51d334f0e1",
+                  "bytes_per_launch": (621.369856 + 2.454272 + 489.221632 + 0.178432) / 2 * 1e6,
                   "launch": "layers 0 and 1 of the full workload (2-layer run, same per-launch shape)"}
 
 
