@@ -22,7 +22,7 @@ from .binding import (HWKV_BF16, HWKV_F32, HWKV_KERNEL_AUTO, HWKV_KERNEL_SIMT, H
                       hwkv_decode_attn, hwkv_decode_workspace_bytes, hwkv_materialize, hwkv_pool_bytes,
                       hwkv_pool_create, hwkv_pool_destroy, hwkv_pool_geometry, hwkv_prefill_attn,
                       hwkv_prefill_plan, hwkv_prefill_workspace_bytes, hwkv_set_block_table, hwkv_set_decode_config,
-                      hwkv_set_prefill_config)
+                      hwkv_set_prefill_config, hwkv_wait_selftest)
 
 __all__ = [
     "Pool", "DecodeLaunch", "HwkvError", "binding", "HWKV_F32", "HWKV_BF16", "HWKV_KERNEL_AUTO", "HWKV_KERNEL_TENSOR",
@@ -30,7 +30,7 @@ __all__ = [
     "hwkv_check_device_errors", "hwkv_kernel_launches",
     "hwkv_decode_attn", "hwkv_decode_workspace_bytes", "hwkv_materialize", "hwkv_pool_bytes", "hwkv_pool_create",
     "hwkv_pool_destroy", "hwkv_pool_geometry", "hwkv_prefill_attn", "hwkv_prefill_plan", "hwkv_prefill_workspace_bytes",
-    "hwkv_set_block_table", "hwkv_set_decode_config", "hwkv_set_prefill_config",
+    "hwkv_set_block_table", "hwkv_set_decode_config", "hwkv_set_prefill_config", "hwkv_wait_selftest",
 ]
 
 

@@ -56,6 +56,7 @@ SIGNATURES = [
     ("hwkv_materialize", _i, [_vp, _i, _vp, _vp, _i64, _i64, _i64, _vp, _vp]),
     ("hwkv_append", _i, [_vp, _i, _vp, _vp, _vp, _vp]),
     ("hwkv_advance_positions", _i, [_vp, _vp, _vp, ctypes.c_int32, _vp]),
+    ("hwkv_wait_selftest", _i, [ctypes.c_uint32, _vp, _vp]),
     ("hwkv_decode_workspace_bytes", _i, [_vp, _i, _c_u64p]),
     ("hwkv_decode_attn", _i, [_vp, _i, _vp, _i, ctypes.c_float, _vp, _vp, _vp, _u64, _vp]),
     ("hwkv_append_decode_attn", _i, [_vp, _i, _vp, _i, ctypes.c_float, _vp, _vp, _vp, _vp, _vp, _u64, _vp]),
@@ -213,6 +214,12 @@ def hwkv_append(pool: int, layer: int, k_new: torch.Tensor, v_new: torch.Tensor,
     if not (k_new.is_contiguous() and v_new.is_contiguous()):
         raise ValueError("k_new and v_new must be contiguous")
     _check(load().hwkv_append(pool, layer, _ptr(k_new), _ptr(v_new), _ptr(pos), _stream_ptr(stream)))
+
+
+def hwkv_wait_selftest(limit_us: int, out: torch.Tensor, stream=None):
+    """Runs the library's bounded wait on a completed and on a never-completing mbarrier phase;
+    out: int32 [3] on the device (error bits, first wait succeeded, microseconds waited)."""
+    _check(load().hwkv_wait_selftest(int(limit_us), _ptr(out), _stream_ptr(stream)))
 
 
 def hwkv_advance_positions(pool: int, pos: torch.Tensor, out: torch.Tensor, delta: int = 1, stream=None):

@@ -9,6 +9,7 @@
 // Both kernels are HBM copies: 16-byte vector loads and stores, one physical-block lookup
 // per row.  They never fault on bad lengths or table entries: those are recorded in the
 // device error word and the row is skipped.
+#include "hwkv_device.cuh"
 #include "hwkv_internal.h"
 #include "../../include/hwkv.h"
 
@@ -130,7 +131,39 @@ __global__ void __launch_bounds__(256) advance_positions_kernel(const int32_t* i
   if (i < n) out[i] = (int32_t)((uint32_t)in[i] + (uint32_t)delta);
 }
 
+// The bounded wait every kernel of the library uses, run on its own: a phase that has
+// completed (one arrival, no bytes) must be seen at once, a phase nothing will complete must be
+// given up after limit_ns.  out[0]: the error bits recorded (HWKV_DEVERR_WAIT_TIMEOUT when the
+// second wait gave up), out[1]: 1 when the first wait succeeded, out[2]: microseconds the
+// second wait took.
+__global__ void __launch_bounds__(32) wait_selftest_kernel(int32_t* out, uint64_t limit_ns) {
+  __shared__ __align__(8) uint64_t bar[2];
+  if (threadIdx.x == 0) {
+    mbar_init(&bar[0], 1);
+    mbar_init(&bar[1], 1);
+    fence_mbar_init();
+  }
+  __syncwarp();
+  if (threadIdx.x == 0) {
+    mbar_arrive_expect_tx(&bar[1], 0);
+    const bool seen = mbar_wait_bounded(&bar[1], 0, limit_ns);
+    const uint64_t t0 = global_timer_ns();
+    const bool never = mbar_wait_bounded(&bar[0], 0, limit_ns);
+    const uint64_t t1 = global_timer_ns();
+    out[0] = never ? 0 : HWKV_DEVERR_WAIT_TIMEOUT;
+    out[1] = seen ? 1 : 0;
+    const uint64_t us = (t1 - t0) / 1000ull;
+    out[2] = us > 0x7FFFFFFFull ? 0x7FFFFFFF : (int32_t)us;
+  }
+}
+
 }  // namespace
+
+cudaError_t launch_wait_selftest(int32_t* out, uint32_t limit_us, cudaStream_t st) {
+  wait_selftest_kernel<<<1, 32, 0, st>>>(out, (uint64_t)limit_us * 1000ull);
+  count_launches(1);
+  return cudaGetLastError();
+}
 
 cudaError_t launch_advance_positions(const int32_t* in, int32_t* out, int n, int32_t delta, cudaStream_t st) {
   advance_positions_kernel<<<(n + 255) / 256, 256, 0, st>>>(in, out, n, delta);

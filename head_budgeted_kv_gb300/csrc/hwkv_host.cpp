@@ -772,6 +772,14 @@ int hwkv_advance_positions(hwkv_pool_t p, const int32_t* pos_dev, int32_t* out_d
   return ok();
 }
 
+int hwkv_wait_selftest(uint32_t limit_us, int32_t* out_dev, void* stream) {
+  if (limit_us < 1 || limit_us > 2000000u) return fail(HWKV_ERR_INVALID_ARG, "limit_us must be in [1, 2000000]");
+  if (!out_dev) return fail(HWKV_ERR_INVALID_ARG, "NULL output");
+  if (!aligned(out_dev, 4)) return fail(HWKV_ERR_ALIGNMENT, "out_dev must be 4-byte aligned");
+  HWKV_CUDA_TRY(launch_wait_selftest(out_dev, limit_us, static_cast<cudaStream_t>(stream)), "wait self-test launch");
+  return ok();
+}
+
 int hwkv_decode_workspace_bytes(hwkv_pool_t p, int q_heads, uint64_t* out) {
   if (!p || !out) return fail(HWKV_ERR_INVALID_ARG, "NULL argument");
   if (q_heads < p->g.kv_heads || q_heads % p->g.kv_heads != 0 || q_heads / p->g.kv_heads > kMaxGroup)

@@ -110,6 +110,8 @@ int check_pool_device(const struct ::hwkv_pool* p);
 cudaError_t launch_append(const CopyArgs& a, int dtype, cudaStream_t st);
 // out[i] = in[i] + delta for i < n (in == out allowed)
 cudaError_t launch_advance_positions(const int32_t* in, int32_t* out, int n, int32_t delta, cudaStream_t st);
+// the bounded wait of every kernel, on a phase that completes and one that never does
+cudaError_t launch_wait_selftest(int32_t* out, uint32_t limit_us, cudaStream_t st);
 // max_rows: the most positions any (seq, head) of the layer copies, min(max window, max_len)
 cudaError_t launch_materialize(const CopyArgs& a, int dtype, int max_rows, cudaStream_t st);
 // once per device before the first launch; returns resident CTAs per SM of the instances

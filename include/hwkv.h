@@ -155,6 +155,19 @@ int hwkv_append(hwkv_pool_t pool, int layer, const void* k_new, const void* v_ne
  *   pos_dev, out_dev: device int32 [num_seqs], 4-byte aligned.  One kernel on `stream`. */
 int hwkv_advance_positions(hwkv_pool_t pool, const int32_t* pos_dev, int32_t* out_dev, int32_t delta, void* stream);
 
+/* Check of the bounded waits (a service of this library; the pages have no counterpart).
+ * Every wait of every kernel here gives up after a time limit (~2 s) and records
+ * HWKV_DEVERR_WAIT_TIMEOUT in the error word instead of spinning forever.  This runs that same
+ * wait loop on its own, in one warp, so a host can see the path work without faulting or
+ * hanging a GPU: first on an mbarrier phase that has completed, then on one that nothing will
+ * complete, given up after limit_us microseconds.
+ *   out_dev: device int32 [3], 4-byte aligned, written by the kernel: [0] the error bits it
+ *            recorded (HWKV_DEVERR_WAIT_TIMEOUT when the second wait gave up), [1] 1 when the
+ *            first wait returned true, [2] the microseconds the second wait took.
+ *   limit_us: 1 .. 2 000 000 (HWKV_ERR_INVALID_ARG otherwise).
+ * One kernel on `stream`, on the current device; HWKV_ERR_CUDA if it cannot be launched. */
+int hwkv_wait_selftest(uint32_t limit_us, int32_t* out_dev, void* stream);
+
 /* Bytes of scratch hwkv_decode_attn / hwkv_append_decode_attn need for the current decode
  * configuration (fp32 split-K partials; maximum over layers). */
 int hwkv_decode_workspace_bytes(hwkv_pool_t pool, int q_heads, uint64_t* out);

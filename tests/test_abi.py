@@ -114,6 +114,14 @@ def test_null_pool_handles_are_rejected(lib):
     assert lib.hwkv_append_decode_attn(None, 0, None, 4, 1.0, None, None, None, None, None, 0, None) == binding.HWKV_ERR_INVALID_ARG
 
 
+def test_wait_selftest_rejects_bad_arguments_before_any_launch(lib):
+    # checked on the host: no device is touched (this runs without a GPU)
+    assert lib.hwkv_wait_selftest(0, ctypes.c_void_p(16), None) == binding.HWKV_ERR_INVALID_ARG
+    assert lib.hwkv_wait_selftest(2000001, ctypes.c_void_p(16), None) == binding.HWKV_ERR_INVALID_ARG
+    assert lib.hwkv_wait_selftest(1000, None, None) == binding.HWKV_ERR_INVALID_ARG
+    assert lib.hwkv_wait_selftest(1000, ctypes.c_void_p(18), None) == binding.HWKV_ERR_ALIGNMENT
+
+
 def test_last_error_is_thread_local(lib):
     import threading
     _status(lib, 0, 2, 64, 16, [[16, 32]], 1, 0)
