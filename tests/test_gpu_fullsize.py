@@ -13,6 +13,8 @@ runs all of its decode steps without a host synchronisation between them, then:
 * copies: the whole pool region of layers {0, 1, last} is compared bit for bit with the
   oracle's expected pool, and for every (layer, seq, head) the slots of the newest appended
   position and of the oldest resident one hold exactly those positions' K and V rows."""
+import dataclasses
+
 import numpy as np
 import pytest
 import torch
@@ -134,4 +136,38 @@ def test_full_size_parity(name):
     for l in sorted({0, 1, cfg.layers - 1}):
         _check_layer_pool(run, cfg, l, name)
     _check_newest_and_oldest_slots(run, cfg, name)
+    run.close()
+
+
+# the other decode shapes bench.py --mode shapes times, as it builds them
+SHAPES = {"bf16_d64_gqa4": {"head_dim": 64}, "bf16_d64_gqa16": {"head_dim": 64, "q_heads": 128},
+          "bf16_d128_gqa16": {"q_heads": 128}, "fp32_d128_gqa4": {"dtype": "f32"}}
+
+
+@pytest.mark.parametrize("shape", sorted(SHAPES))
+def test_decode_shapes_full_geometry_parity(shape):
+    """The full geometry's first 8 layers (batch 4, 112K, the page's per-head windows) at another
+    head_dim, GQA group or dtype, in the launch configuration the shapes benchmark times: every
+    query head of steps {0, 2, 5} of layers {0, 1, 7} against the oracle; the pool of layers
+    {0, 7} bit for bit; newest and oldest resident slots of every (layer, seq, head)."""
+    cfg = dataclasses.replace(workloads.config("full").with_layers(8).with_steps(6), name="full_8l", **SHAPES[shape])
+    free, _ = torch.cuda.mem_get_info()
+    need = oracle.pool_bytes(cfg.windows_array(), cfg.batch, cfg.head_dim, cfg.block_size, cfg.elem_bytes)
+    if need * 1.6 > free:
+        pytest.skip(f"needs ~{need * 1.6 / 1e9:.0f} GB of device memory")
+    run = Run(cfg, fused=True)
+    run.materialize()
+    pairs = {(i, l) for i in (0, 2, 5) for l in (0, 1, 7)}
+    res = run.run_prepared(pairs=pairs)
+    assert run.device_errors() == 0
+    for l in (0, 1, 7):
+        hist = run.layer_histories(l, None)
+        for i in (0, 2, 5):
+            q_raw, got = res.pop((i, l))
+            assert_close(got, run.reference_hoisted(hist, i, l, q_raw), cfg, f"{shape} step {i} layer {l}")
+        del hist
+    assert not res
+    for l in (0, 7):
+        _check_layer_pool(run, cfg, l, shape)
+    _check_newest_and_oldest_slots(run, cfg, shape)
     run.close()
