@@ -105,6 +105,9 @@ EDGE = {
                          prefill=(5000, 20)),
     # spiky keys (x8) as in the ragged workload
     "spikes": dict(kv_heads=2, windows=((1024, 512),), prefill=(2000, 1500), spike_frac=0.05),
+    # more sequences than a CTA stages lengths for in shared memory (256): the lengths are read
+    # from global memory; ragged, some prefills empty
+    "many_seqs": dict(kv_heads=2, windows=((48, 200),), prefill=tuple((i * 37) % 400 for i in range(300))),
 }
 
 
@@ -436,4 +439,20 @@ def test_random_geometries_match_the_oracle(seed):
             assert_close(got, ref, cfg, f"random {seed} (fused {fused}, workers {workers}) step {i} layer {l}")
     _check_all_pool_blocks(run)
     assert run.device_errors() == 0
+    run.close()
+
+
+def test_many_sequences_through_prepared_fused_launches():
+    """300 sequences (beyond the 256 whose lengths a CTA stages in shared memory) through the
+    launches the benchmark issues: prepared fused append + decode with early reads, back to
+    back; every step and layer against the oracle, every pool block bit for bit."""
+    cfg = small_config(name="many_prep", layers=2, kv_heads=2, windows=((48, 200), (300, 16)),
+                       prefill=tuple((i * 53) % 700 for i in range(300)), steps=3)
+    run = Run(cfg, fused=True)
+    run.materialize()
+    res = run.run_prepared(keep_steps=range(cfg.steps), keep_layers=range(cfg.layers))
+    assert run.device_errors() == 0
+    for (i, l), (q_raw, got) in sorted(res.items()):
+        assert_close(got, run.reference(i, l, q_raw), cfg, f"step {i} layer {l}")
+    _check_all_pool_blocks(run)
     run.close()
